@@ -1,0 +1,577 @@
+#!/usr/bin/env python3
+"""Benchmark of the DCP LSE merge on GB300: µs per call and achieved HBM GB/s.
+
+Default workload (one "call" = one step): the MLA decode merge, N = 8 ranks,
+B = 128 tokens, H = 128 heads, D = 512 (absorbed-MLA kv_lora_rank), bf16
+partial outputs, base-2 LSE.  One step is the whole hot path for all 8 ranks
+held on one GPU: the peer-inside pack of every source rank (one launch, G = 8)
+followed by the LSE combine for every destination rank (one launch, G = 8)
+over the receive views; the all-to-all between them is a zero-copy view of
+the sender stack.  L2 is flushed (a 2x-L2 memset) before every kernel, outside
+the timed events, so every kernel reads its inputs from HBM.
+
+Also measured in the same run and reported under "secondary": the in-place
+sanitising combine of the cached-extend workload (N = 8, 16384 tokens, 96
+heads, D = 512, fp32; 29 GB per call) and the largest long-context sweep
+point through the fused unpack+combine (N = 8, B = 256, H = 64, D = 512, fp16).
+
+`--impl reference` times the fp64 CPU oracle instead, on a bounded sample of
+the same workload, and reports it in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DCP LSE-merge µs/call and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+UNIT = "µs/call"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what each call must move, whatever the implementation)
+# ---------------------------------------------------------------------------
+
+def bytes_pack(G, B, H, D, e):
+    """Read O and LSE of G*B*H rows, write the same bytes to the send layout."""
+    return 2 * G * B * H * (D * e + 4)
+
+
+def bytes_merge(G, N, B, Hc, D, e, return_lse=True):
+    """Read N rank rows (payload + LSE word) per output row, write the row (+ LSE)."""
+    rows = G * B * Hc
+    return N * rows * (D * e + 4) + rows * D * e + (rows * 4 if return_lse else 0)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU under torchrun; weak scaling)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a host float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks (nvidia-smi sampled while the GPU works)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        samples = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                samples.append((float(parts[0]), float(parts[1]), float(parts[2]),
+                                float(parts[3]), parts[4:8]))
+            except ValueError:
+                continue
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [s for s in samples if s[3] > 0] or samples
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in busy for i, v in enumerate(s[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[0] for s in busy),
+                "sm_max_mhz": max(s[1] for s in samples),
+                "power_w_max": max(s[2] for s in samples),
+                "reasons": reasons, "samples": len(samples), "samples_busy": len(busy)}
+
+
+# ---------------------------------------------------------------------------
+# GPU timing
+# ---------------------------------------------------------------------------
+
+class L2Flush:
+    def __init__(self, device):
+        import torch
+
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.buf = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=device)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_sequence(launches, steps, warmup, flush, device):
+    """Run `steps` iterations of the launch sequence; before each launch flush
+    L2 (unless flush is None), bracket each launch with CUDA events on the
+    current stream.  Returns per-launch lists of durations in ms."""
+    import torch
+
+    for _ in range(warmup):
+        for f in launches:
+            if flush:
+                flush()
+            f()
+    torch.cuda.synchronize(device)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in launches] for _ in range(steps)]
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        for j, f in enumerate(launches):
+            if flush:
+                flush()
+            ev[i][j][0].record()
+            f()
+            ev[i][j][1].record()
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    barrier(device)
+    per = [[ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(steps)] for j in range(len(launches))]
+    return per, wall
+
+
+def kernel_record(name, ms_list, nbytes, peak_gbs):
+    avg = statistics.fmean(ms_list)
+    gbs = nbytes / (avg * 1e-3) / 1e9
+    return {"kernel": name, "us_per_launch": round(avg * 1e3, 3),
+            "us_median": round(statistics.median(ms_list) * 1e3, 3),
+            "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak_gbs, 4)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "decode_context_attention_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get("kernels", {}).get(kernel)
+    if not ent or ent.get("csrc_digest") != csrc_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# the workloads as launch sequences
+# ---------------------------------------------------------------------------
+
+def setup_mla_decode(device, seed_offset=0):
+    import torch
+
+    from decode_context_attention_gb300 import binding, layouts
+    from decode_context_attention_gb300.workloads import WORKLOADS, generate, scaled
+
+    w = WORKLOADS["mla_decode"]
+    if seed_offset:
+        w = scaled(w, seed=w.seed + 100 * seed_offset)
+    d = generate(w, device)
+    S, B, H, D = d["o"].shape
+    N, H_pr = w.N, w.H_pr
+    partial_o, stats = layouts.alloc_peer_inside(S, B, H_pr, N, D, d["o"].dtype, device)
+    dst_o, dst_lse = layouts.peer_inside_send_views(partial_o, stats)
+    ro, rl = layouts.exchange_peer_inside(partial_o, stats)
+    out = torch.empty((N, B, H_pr, D), dtype=d["o"].dtype, device=device)
+    out_lse = torch.empty((N, B, H_pr), dtype=torch.float32, device=device)
+    pack = binding.prepare_pack_send(d["o"], d["lse"], dst_o, dst_lse)
+    comb = binding.prepare_lse_combine(ro, rl, out, out_lse, base=w.base)
+    e = d["o"].element_size()
+    return {
+        "w": w, "d": d, "out": out, "out_lse": out_lse, "partial_o": partial_o, "stats": stats,
+        "launches": [pack, comb],
+        "names": ["dcp_pack_send (peer-inside, G=8 sources)",
+                  "dcp_lse_combine (strided recv views, G=8 destinations)"],
+        "kernels": ["pack_kernel", "combine_kernel"],
+        "bytes": [bytes_pack(S, B, H, D, e), bytes_merge(N, S, B, H_pr, D, e)],
+    }
+
+
+def setup_cached_extend(device):
+    import torch
+
+    from decode_context_attention_gb300 import binding
+    from decode_context_attention_gb300.workloads import WORKLOADS, generate
+
+    w = WORKLOADS["cached_extend"]
+    d = generate(w, device)
+    o, lse = d["o"], d["lse"]
+    N, T, H, D = o.shape
+    out_lse = torch.empty((T, H), dtype=torch.float32, device=device)
+    comb = binding.prepare_lse_combine(o, lse, o[0], out_lse, base=w.base, sanitize=True,
+                                       inplace=True)
+    return {"w": w, "launches": [comb], "keep": (o, lse, out_lse),
+            "names": ["dcp_lse_combine (in place, sanitise, fp32)"],
+            "bytes": [bytes_merge(1, N, T, H, D, 4)]}
+
+
+def setup_sweep_max(device):
+    import torch
+
+    from decode_context_attention_gb300 import binding, layouts
+    from decode_context_attention_gb300.workloads import generate, sweep_points
+
+    w = [p for p in sweep_points() if p.layout == "peer_major" and p.N == 8 and p.B == 256
+         and p.D == 512][0]
+    d = generate(w, device)
+    S, B, H, D = d["o"].shape
+    N, H_pr = w.N, w.H_pr
+    send = layouts.alloc_peer_major(S, N, B, H_pr, D, d["o"].dtype, device)
+    pay, words = layouts.peer_major_views(send, D)
+    binding.pack_send(d["o"], d["lse"], pay, words)
+    recv = layouts.exchange_peer_major(send)
+    out = torch.empty((N, B, H_pr, D), dtype=d["o"].dtype, device=device)
+    out_lse = torch.empty((N, B, H_pr), dtype=torch.float32, device=device)
+    pack = binding.prepare_pack_send(d["o"], d["lse"], pay, words)
+    fused = binding.prepare_unpack_combine(recv, D, out, out_lse, base=w.base)
+    e = d["o"].element_size()
+    return {"w": w, "launches": [pack, fused], "keep": (d, send, out, out_lse),
+            "names": ["dcp_pack_send (peer-major interleaved, G=8)",
+                      "dcp_unpack_combine (interleaved recv, G=8)"],
+            "bytes": [bytes_pack(S, B, H, D, e), bytes_merge(N, S, B, H_pr, D, e)]}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_inputs(mla):
+    """Host copies of one source rank's pack inputs and one destination's
+    combine inputs of the MLA decode workload (1/8 of a call each)."""
+    import numpy as np
+    import torch
+
+    d, w = mla["d"], mla["w"]
+    o0 = d["o"][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    l0 = d["lse"][0].cpu().numpy()
+    po = mla["partial_o"][:, :, :, 0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    st = mla["stats"][:, :, :, 0, 0].contiguous().cpu().numpy()
+    return w, o0, l0, po, st
+
+
+def oracle_one_eighth(w, o0, l0, po, st, rows=None):
+    """One source's pack and one destination's combine through the oracle
+    (optionally only the first `rows` tokens).  Returns the fraction of a full
+    call that was processed."""
+    import numpy as np
+
+    import oracle
+
+    B = o0.shape[0] if rows is None else rows
+    N, H_pr, D = w.N, w.H_pr, w.D
+    dst = np.empty((B, H_pr, N, D), dtype=np.uint16)
+    stats = np.zeros((B, H_pr, N, 2), dtype=np.float32)
+    oracle.pack("bf16", N, o0[None, :B], l0[None, :B], dst.transpose(2, 0, 1, 3)[None],
+                stats[..., 0].transpose(2, 0, 1)[None])
+    # destination 0 receives partial_o[s, :, :, 0] from every source s
+    oracle.combine("bf16", po[None, :, :B], st[None, :, :B], base=w.base)
+    return (B / w.B) / w.N
+
+
+def time_oracle(mla, budget_s: float):
+    """Oracle µs per full call, extrapolated from repeated 1/8-call samples."""
+    w, o0, l0, po, st = oracle_sample_inputs(mla)
+    done, t0 = 0.0, time.perf_counter()
+    n = 0
+    while True:
+        done += oracle_one_eighth(w, o0, l0, po, st)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return el / done * 1e6, el, n
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+
+    from decode_context_attention_gb300 import binding, build
+
+    rank, world = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if local == 0:
+        build.build()
+    barrier(device)
+    binding.load()
+    peak, peak_kind = load_peaks()
+    flush = L2Flush(device)
+    clocks = ClockSampler(local)
+    clocks.start()
+
+    # --- headline: MLA decode merge, pack + combine, all 8 ranks ----------------
+    mla = setup_mla_decode(device, seed_offset=rank)
+    per, wall = time_sequence(mla["launches"], args.steps, args.warmup, flush, device)
+    step_ms = [sum(x) for x in zip(*per)]
+    ms_per_step = max_over_ranks(statistics.fmean(step_ms), device)
+    kernels = [kernel_record(n, p, b, peak) for n, p, b in zip(mla["names"], per, mla["bytes"])]
+    dom = max(range(len(kernels)), key=lambda j: kernels[j]["us_per_launch"])
+
+    # --- e2e: host buffers in, host result out, through the public binding ------
+    e2e = run_e2e(mla, args, device)
+
+    # --- secondary workloads (same run) ----------------------------------------
+    secondary = []
+    if not args.no_secondary:
+        sw = setup_sweep_max(device)
+        p2, _ = time_sequence(sw["launches"], max(20, args.steps // 10), args.warmup, flush, device)
+        secondary.append({"workload": sw["w"].name,
+                          "kernels": [kernel_record(n, p, b, peak)
+                                      for n, p, b in zip(sw["names"], p2, sw["bytes"])]})
+        del sw
+        ce = setup_cached_extend(device)
+        p3, _ = time_sequence(ce["launches"], args.ext_steps, 3, None, device)
+        secondary.append({"workload": "cached_extend N=8 T=16384 H=96 D=512 fp32",
+                          "inputs_vs_l2": "24 GiB stack, far larger than L2 (no flush)",
+                          "kernels": [kernel_record(ce["names"][0], p3[0], ce["bytes"][0], peak)]})
+        del ce
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        us, el, n = time_oracle(mla, args.cpu_budget)
+        cpu = {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} x (one source's pack + one destination's combine = 1/8 of a "
+                         f"call), {el:.1f} s single-threaded fp64 C, scaled to one call"}
+
+    if rank != 0:
+        return
+    k = kernels[dom]
+    traffic = ncu_traffic(mla["kernels"][dom])
+    w = mla["w"]
+    line = {
+        "metric": METRIC, "value": round(ms_per_step * 1e3, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded O ~ N(0,1), LSE ~ U(0,20) base 2)",
+        "config": {"workload": f"mla_decode N={w.N} B={w.B} H={w.H} D={w.D} bf16 base-2, "
+                               "peer-inside pack + combine over strided recv views, all ranks on "
+                               "one GPU", "calls_per_step_per_gpu": 1,
+                   "l2": "flushed (2x L2 memset) before every kernel, outside the timed events",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "roofline": {"bound": "hbm", "kernel": k["kernel"], "achieved": k["achieved_gbs"],
+                     "peak": peak, "unit": "GB/s", "frac": k["frac_of_measured_hbm"],
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic, "algorithmic_bytes": k["algorithmic_bytes"]},
+        "kernels": kernels,
+        "secondary": secondary,
+        "e2e": e2e,
+        "gpu_launches": len(mla["launches"]) * args.steps,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(mla, args, device):
+    """µs per call with the inputs copied from pinned host memory and the
+    merged result copied back, all inside the timed region."""
+    import torch
+
+    from decode_context_attention_gb300 import binding, layouts
+
+    d, w = mla["d"], mla["w"]
+    o_h = d["o"].cpu().pin_memory()
+    l_h = d["lse"].cpu().pin_memory()
+    out_h = torch.empty(mla["out"].shape, dtype=mla["out"].dtype).pin_memory()
+    lse_h = torch.empty(mla["out_lse"].shape, dtype=torch.float32).pin_memory()
+    o_d = torch.empty_like(d["o"])
+    l_d = torch.empty_like(d["lse"])
+    dst_o, dst_lse = layouts.peer_inside_send_views(mla["partial_o"], mla["stats"])
+    ro, rl = layouts.exchange_peer_inside(mla["partial_o"], mla["stats"])
+
+    def step():
+        o_d.copy_(o_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        binding.pack_send(o_d, l_d, dst_o, dst_lse)
+        binding.lse_combine(ro, rl, mla["out"], mla["out_lse"], base=w.base)
+        out_h.copy_(mla["out"], non_blocking=True)
+        lse_h.copy_(mla["out_lse"], non_blocking=True)
+
+    steps = max(10, args.steps // 20)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = max_over_ranks(a.elapsed_time(b) / steps, device)
+    h2d = o_h.numel() * o_h.element_size() + l_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    return {"value": round(ms * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "api": "decode_context_attention_gb300.binding.pack_send + lse_combine"}
+
+
+def run_reference(args):
+    """The fp64 CPU oracle on a bounded sample of the same workload, same unit."""
+    import torch
+
+    rank, world = dist_env()[0], dist_env()[1]
+    if world > 1 and rank != 0:
+        return
+    from decode_context_attention_gb300.workloads import WORKLOADS, generate
+
+    w = WORKLOADS["mla_decode"]
+    d = generate(w, "cpu")
+    S, B, H, D = d["o"].shape
+    partial_o = d["o"].view(S, B, w.N, w.H_pr, D).permute(0, 1, 3, 2, 4).contiguous()
+    stats = torch.zeros((S, B, w.H_pr, w.N, 2))
+    stats[..., 0] = d["lse"].view(S, B, w.N, w.H_pr).permute(0, 1, 3, 2)
+    mla = {"d": d, "w": w, "partial_o": partial_o, "stats": stats}
+    # size each step so warmup + steps finish in about two minutes
+    samp = oracle_sample_inputs(mla)
+    t0 = time.perf_counter()
+    oracle_one_eighth(*samp, rows=4)
+    probe = time.perf_counter() - t0
+    per_row = probe / 4
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(B, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_one_eighth(*samp, rows=rows)
+    times = []
+    frac = None
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        frac = oracle_one_eighth(*samp, rows=rows)
+        times.append(time.perf_counter() - t)
+    us = statistics.fmean(times) / frac * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload)",
+        "config": {"workload": f"mla_decode N={w.N} B={w.B} H={w.H} D={w.D} bf16 base-2, "
+                               "peer-inside pack + combine"},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: one source's pack + one destination's combine "
+                                   f"over the first {rows} of {B} tokens, scaled to one call"},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--ext-steps", type=int, default=40, help="timed calls of the 29 GB workload")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

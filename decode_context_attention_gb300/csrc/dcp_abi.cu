@@ -1,0 +1,399 @@
+// dcp_abi.cu -- the extern "C" entry points declared in include/dcp.h:
+// argument validation on the host (sizes, pointer alignment, aliasing) and
+// dispatch to the kernels.  Nothing here touches device memory: a rejected
+// call launches nothing.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "dcp.h"
+#include "dcp_internal.h"
+
+namespace dcp {
+
+int device_sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int ctas_per_sm(const void* kernel) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({dev, kernel});
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
+        n = 1;
+    cache[{dev, kernel}] = n;
+    return n;
+}
+
+}  // namespace dcp
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+dcp_status_t fail(dcp_status_t s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+dcp_status_t ok() {
+    g_msg[0] = '\0';
+    return DCP_OK;
+}
+
+int elem_size(int dtype) {
+    switch (dtype) {
+        case DCP_F32: return 4;
+        case DCP_F16:
+        case DCP_BF16: return 2;
+        default: return 0;
+    }
+}
+
+// A strided set of rows: `nd` outer dimensions (size, stride in BYTES) and
+// `inner` contiguous bytes per row.
+struct View {
+    uintptr_t base = 0;
+    int nd = 0;
+    int64_t size[5] = {0, 0, 0, 0, 0};
+    int64_t stride[5] = {0, 0, 0, 0, 0};
+    int64_t inner = 0;
+
+    View(const void* p, int64_t inner_bytes) : base((uintptr_t)p), inner(inner_bytes) {}
+    View& dim(int64_t n, int64_t stride_bytes) {
+        size[nd] = n;
+        stride[nd] = stride_bytes;
+        ++nd;
+        return *this;
+    }
+    bool empty() const {
+        for (int i = 0; i < nd; ++i)
+            if (size[i] == 0) return true;
+        return inner == 0;
+    }
+    // Byte range [lo, hi) that the rows can touch.
+    void extent(uintptr_t& lo, uintptr_t& hi) const {
+        lo = base;
+        hi = base + (uintptr_t)inner;
+        for (int i = 0; i < nd; ++i)
+            if (size[i] > 1) hi += (uintptr_t)((size[i] - 1) * stride[i]);
+    }
+    // True when distinct index tuples address disjoint byte ranges: sorted by
+    // stride, every stride spans at least the block of the smaller dimensions.
+    bool rows_disjoint() const { return rows_disjoint_with_inner(inner); }
+    bool rows_disjoint_with_inner(int64_t row_bytes) const {
+        int idx[5];
+        int m = 0;
+        for (int i = 0; i < nd; ++i)
+            if (size[i] > 1) idx[m++] = i;
+        for (int a = 1; a < m; ++a)
+            for (int b = a; b > 0 && stride[idx[b]] < stride[idx[b - 1]]; --b) std::swap(idx[b], idx[b - 1]);
+        int64_t span = row_bytes;
+        for (int a = 0; a < m; ++a) {
+            const int i = idx[a];
+            if (stride[i] < span) return false;
+            span = stride[i] * (size[i] - 1) + span;
+        }
+        return true;
+    }
+    // Largest power of two (<= 16) dividing every row start.
+    int align() const {
+        uint64_t bits = (uint64_t)base | 16u;
+        for (int i = 0; i < nd; ++i)
+            if (size[i] > 1) bits |= (uint64_t)stride[i];
+        return (int)(bits & (~bits + 1));
+    }
+};
+
+bool overlap(const View& a, const View& b) {
+    if (a.empty() || b.empty()) return false;
+    uintptr_t alo, ahi, blo, bhi;
+    a.extent(alo, ahi);
+    b.extent(blo, bhi);
+    return alo < bhi && blo < ahi;
+}
+
+bool any_negative(std::initializer_list<int64_t> s) {
+    for (int64_t v : s)
+        if (v < 0) return true;
+    return false;
+}
+
+// Widest vector (16, 4 or 2 bytes) that divides the row length and every row
+// start of the views given by their alignments.
+int pick_vb(int row_bytes, int align_a, int align_b, int e) {
+    const int a = align_a < align_b ? align_a : align_b;
+    if (a % 16 == 0 && row_bytes % 16 == 0) return 16;
+    if (a % 4 == 0 && row_bytes % 4 == 0) return 4;
+    return e == 2 ? 2 : 4;
+}
+
+int lanes_per_row(int vectors) {
+    int l = 1;
+    while (l < vectors && l < 32) l <<= 1;
+    return l;
+}
+
+dcp_status_t launched(cudaError_t e, const char* what) {
+    if (e != cudaSuccess)
+        return fail(DCP_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+constexpr int kMaxRanks = 4096;
+
+}  // namespace
+
+extern "C" {
+
+int dcp_lse_pack_dim(int dtype) {
+    const int e = elem_size(dtype);
+    return e ? 4 / e : -1;
+}
+
+const char* dcp_status_string(int status) {
+    switch (status) {
+        case DCP_OK: return "success";
+        case DCP_ERR_INVALID_ARG: return "invalid argument";
+        case DCP_ERR_UNSUPPORTED_DTYPE: return "unsupported payload dtype (f32, f16 and bf16 only)";
+        case DCP_ERR_HEADS_NOT_DIVISIBLE: return "number of heads is not a multiple of the rank count";
+        case DCP_ERR_MISALIGNED: return "misaligned pointer, stride or head dim";
+        case DCP_ERR_ALIAS: return "an output overlaps an input or itself";
+        case DCP_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+const char* dcp_last_error_message(void) { return g_msg; }
+
+dcp_status_t dcp_pack_send(int dtype, int N, int B, int H, int D, int G,
+                           const void* o, int64_t o_sg, int64_t o_sb, int64_t o_sh,
+                           const float* lse, int64_t l_sg, int64_t l_sb, int64_t l_sh,
+                           void* dst_o, int64_t do_sg, int64_t do_sn, int64_t do_sb, int64_t do_sh,
+                           float* dst_lse, int64_t dl_sg, int64_t dl_sn, int64_t dl_sb, int64_t dl_sh,
+                           void* stream) {
+    const int e = elem_size(dtype);
+    if (!e) return fail(DCP_ERR_UNSUPPORTED_DTYPE, "dcp_pack_send: dtype %d", dtype);
+    if (N < 1 || N > kMaxRanks || D < 1 || B < 0 || H < 0 || G < 0)
+        return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: sizes N=%d B=%d H=%d D=%d G=%d", N, B, H, D, G);
+    if (H % N)
+        return fail(DCP_ERR_HEADS_NOT_DIVISIBLE, "dcp_pack_send: H=%d is not a multiple of N=%d", H, N);
+    if (G == 0 || B == 0 || H == 0) return ok();
+    if (!o || !lse || !dst_o || !dst_lse)
+        return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: NULL pointer");
+    if (any_negative({o_sg, o_sb, o_sh, l_sg, l_sb, l_sh, do_sg, do_sn, do_sb, do_sh, dl_sg, dl_sn,
+                      dl_sb, dl_sh}))
+        return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: negative stride");
+    if ((uintptr_t)o % e || (uintptr_t)dst_o % e || (uintptr_t)lse % 4 || (uintptr_t)dst_lse % 4)
+        return fail(DCP_ERR_MISALIGNED, "dcp_pack_send: pointer not aligned to its element type");
+    const int H_pr = H / N;
+    const int64_t rb = (int64_t)D * e;
+    View vo = View(o, rb).dim(G, o_sg * e).dim(B, o_sb * e).dim(H, o_sh * e);
+    View vl = View(lse, 4).dim(G, l_sg * 4).dim(B, l_sb * 4).dim(H, l_sh * 4);
+    View vdo = View(dst_o, rb).dim(G, do_sg * e).dim(N, do_sn * e).dim(B, do_sb * e).dim(H_pr, do_sh * e);
+    View vdl = View(dst_lse, 4).dim(G, dl_sg * 4).dim(N, dl_sn * 4).dim(B, dl_sb * 4).dim(H_pr, dl_sh * 4);
+    if (overlap(vdo, vo) || overlap(vdo, vl) || overlap(vdl, vo) || overlap(vdl, vl))
+        return fail(DCP_ERR_ALIAS, "dcp_pack_send: destination overlaps the source");
+    if (!vdo.rows_disjoint() || !vdl.rows_disjoint())
+        return fail(DCP_ERR_ALIAS, "dcp_pack_send: destination rows overlap one another");
+    if (overlap(vdo, vdl)) {
+        // only the interleaved send buffer: the LSE word sits after the payload
+        // of the same row, with the same byte strides
+        bool same = true;
+        for (int i = 0; i < 4; ++i)
+            if (vdo.size[i] > 1 && vdo.stride[i] != vdl.stride[i]) same = false;
+        const int64_t off = (int64_t)((uintptr_t)dst_lse - (uintptr_t)dst_o);
+        if (!same || (uintptr_t)dst_lse < (uintptr_t)dst_o || off < rb ||
+            !vdo.rows_disjoint_with_inner(off + 4))
+            return fail(DCP_ERR_ALIAS,
+                        "dcp_pack_send: dst_lse overlaps dst_o other than as the interleaved "
+                        "[payload | LSE word] row layout");
+    }
+    dcp::PackParams p;
+    p.N = N; p.B = B; p.H = H; p.D = D; p.G = G; p.H_pr = H_pr;
+    p.rows = (int64_t)G * B * H;
+    p.row_bytes = (int)rb;
+    p.vb = pick_vb((int)rb, vo.align(), vdo.align(), e);
+    p.lpr = lanes_per_row((int)(rb / p.vb));
+    p.copy_payload = 1;
+    p.copy_lse = 1;
+    p.o = (const unsigned char*)o; p.o_sg = o_sg * e; p.o_sb = o_sb * e; p.o_sh = o_sh * e;
+    p.lse = lse; p.l_sg = l_sg; p.l_sb = l_sb; p.l_sh = l_sh;
+    p.dst_o = (unsigned char*)dst_o;
+    p.do_sg = do_sg * e; p.do_sn = do_sn * e; p.do_sb = do_sb * e; p.do_sh = do_sh * e;
+    p.dst_lse = dst_lse; p.dl_sg = dl_sg; p.dl_sn = dl_sn; p.dl_sb = dl_sb; p.dl_sh = dl_sh;
+    return launched(dcp::launch_pack(p, (cudaStream_t)stream), "dcp_pack_send");
+}
+
+// Shared tail of the two merge entry points once the views are validated.
+static dcp_status_t run_merge(const char* who, int dtype, int e, int N, int B, int Hc, int D, int G,
+                              const unsigned char* o, int64_t o_sg, int64_t o_sn, int64_t o_sb,
+                              int64_t o_sh, const float* lse, int64_t l_sg, int64_t l_sn,
+                              int64_t l_sb, int64_t l_sh, void* out, int64_t u_sg, int64_t u_sb,
+                              int64_t u_sh, float* out_lse, int64_t ul_sg, int64_t ul_sb,
+                              int64_t ul_sh, int lse_base, int return_lse, unsigned flags,
+                              int in_align, int out_align, bool inplace, cudaStream_t stream) {
+    const int64_t rb = (int64_t)D * e;
+    if (N == 1) {
+        // single rank: the input is returned unchanged (bit copy)
+        if (inplace && !return_lse) return ok();
+        dcp::PackParams p;
+        p.N = 1; p.B = B; p.H = Hc; p.D = D; p.G = G; p.H_pr = Hc;
+        p.rows = (int64_t)G * B * Hc;
+        p.row_bytes = (int)rb;
+        p.vb = pick_vb((int)rb, in_align, out_align, e);
+        p.lpr = lanes_per_row((int)(rb / p.vb));
+        p.copy_payload = inplace ? 0 : 1;
+        p.copy_lse = return_lse ? 1 : 0;
+        p.o = o; p.o_sg = o_sg; p.o_sb = o_sb; p.o_sh = o_sh;
+        p.lse = lse; p.l_sg = l_sg; p.l_sb = l_sb; p.l_sh = l_sh;
+        p.dst_o = (unsigned char*)out; p.do_sg = u_sg; p.do_sn = 0; p.do_sb = u_sb; p.do_sh = u_sh;
+        p.dst_lse = out_lse; p.dl_sg = ul_sg; p.dl_sn = 0; p.dl_sb = ul_sb; p.dl_sh = ul_sh;
+        return launched(dcp::launch_pack(p, stream), who);
+    }
+    dcp::CombineParams p;
+    p.N = N; p.B = B; p.Hc = Hc; p.D = D; p.G = G;
+    p.rows = (int64_t)G * B * Hc;
+    const int vb = pick_vb((int)rb, in_align, out_align, e);
+    p.vec_per_row = (int)(rb / vb);
+    p.lpr = lanes_per_row(p.vec_per_row);
+    p.base2 = lse_base == DCP_LSE_BASE_2;
+    p.return_lse = return_lse ? 1 : 0;
+    p.sanitize = (flags & DCP_SANITIZE_O) ? 1 : 0;
+    p.o = o; p.o_sg = o_sg; p.o_sn = o_sn; p.o_sb = o_sb; p.o_sh = o_sh;
+    p.lse = lse; p.l_sg = l_sg; p.l_sn = l_sn; p.l_sb = l_sb; p.l_sh = l_sh;
+    p.out = (unsigned char*)out; p.u_sg = u_sg; p.u_sb = u_sb; p.u_sh = u_sh;
+    p.out_lse = out_lse; p.ul_sg = ul_sg; p.ul_sb = ul_sb; p.ul_sh = ul_sh;
+    cudaError_t err;
+    switch (dtype) {
+        case DCP_F32: err = dcp::launch_combine_f32(p, vb, stream); break;
+        case DCP_F16: err = dcp::launch_combine_f16(p, vb, stream); break;
+        default: err = dcp::launch_combine_bf16(p, vb, stream); break;
+    }
+    return launched(err, who);
+}
+
+dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
+                             const void* o, int64_t o_sg, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                             const float* lse, int64_t l_sg, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                             void* out, int64_t u_sg, int64_t u_sb, int64_t u_sh,
+                             float* out_lse, int64_t ul_sg, int64_t ul_sb, int64_t ul_sh,
+                             int lse_base, int return_lse, unsigned flags, void* stream) {
+    const char* who = "dcp_lse_combine";
+    const int e = elem_size(dtype);
+    if (!e) return fail(DCP_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", who, dtype);
+    if (N < 1 || N > kMaxRanks || D < 1 || B < 0 || Hc < 0 || G < 0)
+        return fail(DCP_ERR_INVALID_ARG, "%s: sizes N=%d B=%d Hc=%d D=%d G=%d", who, N, B, Hc, D, G);
+    if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)
+        return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
+    if (flags & ~(unsigned)(DCP_SANITIZE_O | DCP_INPLACE_RANK0))
+        return fail(DCP_ERR_INVALID_ARG, "%s: unknown flags 0x%x", who, flags);
+    if (G == 0 || B == 0 || Hc == 0) return ok();
+    if (!o || !lse || !out || (return_lse && !out_lse))
+        return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (any_negative({o_sg, o_sn, o_sb, o_sh, l_sg, l_sn, l_sb, l_sh, u_sg, u_sb, u_sh}) ||
+        (return_lse && any_negative({ul_sg, ul_sb, ul_sh})))
+        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride", who);
+    if ((uintptr_t)o % e || (uintptr_t)out % e || (uintptr_t)lse % 4 ||
+        (return_lse && (uintptr_t)out_lse % 4))
+        return fail(DCP_ERR_MISALIGNED, "%s: pointer not aligned to its element type", who);
+    const bool inplace = (flags & DCP_INPLACE_RANK0) != 0;
+    const int64_t rb = (int64_t)D * e;
+    View vo = View(o, rb).dim(G, o_sg * e).dim(N, o_sn * e).dim(B, o_sb * e).dim(Hc, o_sh * e);
+    View vl = View(lse, 4).dim(G, l_sg * 4).dim(N, l_sn * 4).dim(B, l_sb * 4).dim(Hc, l_sh * 4);
+    View vu = View(out, rb).dim(G, u_sg * e).dim(B, u_sb * e).dim(Hc, u_sh * e);
+    if (inplace) {
+        if (out != o || (G > 1 && u_sg != o_sg) || (B > 1 && u_sb != o_sb) || (Hc > 1 && u_sh != o_sh))
+            return fail(DCP_ERR_INVALID_ARG,
+                        "%s: DCP_INPLACE_RANK0 needs out == o with the rank-0 slice's strides", who);
+        if (!vo.rows_disjoint())
+            return fail(DCP_ERR_ALIAS, "%s: in-place combine over overlapping rank rows", who);
+    } else if (overlap(vu, vo)) {
+        return fail(DCP_ERR_ALIAS, "%s: out overlaps o (use DCP_INPLACE_RANK0 for in place)", who);
+    }
+    if (overlap(vu, vl)) return fail(DCP_ERR_ALIAS, "%s: out overlaps lse", who);
+    if (!vu.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out rows overlap one another", who);
+    if (return_lse) {
+        View vul = View(out_lse, 4).dim(G, ul_sg * 4).dim(B, ul_sb * 4).dim(Hc, ul_sh * 4);
+        if (overlap(vul, vo) || overlap(vul, vl) || overlap(vul, vu))
+            return fail(DCP_ERR_ALIAS, "%s: out_lse overlaps an input or out", who);
+        if (!vul.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out_lse entries overlap", who);
+    }
+    return run_merge(who, dtype, e, N, B, Hc, D, G, (const unsigned char*)o, o_sg * e, o_sn * e,
+                     o_sb * e, o_sh * e, lse, l_sg, l_sn, l_sb, l_sh, out, u_sg * e, u_sb * e,
+                     u_sh * e, out_lse, ul_sg, ul_sb, ul_sh, lse_base, return_lse, flags,
+                     vo.align(), vu.align(), inplace, (cudaStream_t)stream);
+}
+
+dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
+                                const void* recv, int64_t r_sg, int64_t r_sn, int64_t r_sb, int64_t r_sh,
+                                void* out, int64_t u_sg, int64_t u_sb, int64_t u_sh,
+                                float* out_lse, int64_t ul_sg, int64_t ul_sb, int64_t ul_sh,
+                                int lse_base, int return_lse, unsigned flags, void* stream) {
+    const char* who = "dcp_unpack_combine";
+    const int e = elem_size(dtype);
+    if (!e) return fail(DCP_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", who, dtype);
+    if (N < 1 || N > kMaxRanks || D < 1 || B < 0 || Hpr < 0 || G < 0)
+        return fail(DCP_ERR_INVALID_ARG, "%s: sizes N=%d B=%d Hpr=%d D=%d G=%d", who, N, B, Hpr, D, G);
+    if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)
+        return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
+    if (flags & ~(unsigned)DCP_SANITIZE_O)
+        return fail(DCP_ERR_INVALID_ARG, "%s: unsupported flags 0x%x", who, flags);
+    const int lpd = 4 / e;
+    if (D % lpd) return fail(DCP_ERR_MISALIGNED, "%s: D=%d is not a multiple of lpd=%d", who, D, lpd);
+    if (G == 0 || B == 0 || Hpr == 0) return ok();
+    if (!recv || !out || (return_lse && !out_lse))
+        return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (any_negative({r_sg, r_sn, r_sb, r_sh, u_sg, u_sb, u_sh}) ||
+        (return_lse && any_negative({ul_sg, ul_sb, ul_sh})))
+        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride", who);
+    if ((uintptr_t)out % e || (return_lse && (uintptr_t)out_lse % 4))
+        return fail(DCP_ERR_MISALIGNED, "%s: pointer not aligned to its element type", who);
+    const int64_t rb = (int64_t)D * e;
+    View vr = View(recv, rb + 4).dim(G, r_sg * e).dim(N, r_sn * e).dim(B, r_sb * e).dim(Hpr, r_sh * e);
+    if (vr.align() < 4)
+        return fail(DCP_ERR_MISALIGNED, "%s: receive rows must start on 4-byte boundaries", who);
+    View vu = View(out, rb).dim(G, u_sg * e).dim(B, u_sb * e).dim(Hpr, u_sh * e);
+    if (overlap(vu, vr)) return fail(DCP_ERR_ALIAS, "%s: out overlaps recv", who);
+    if (!vu.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out rows overlap one another", who);
+    if (return_lse) {
+        View vul = View(out_lse, 4).dim(G, ul_sg * 4).dim(B, ul_sb * 4).dim(Hpr, ul_sh * 4);
+        if (overlap(vul, vr) || overlap(vul, vu))
+            return fail(DCP_ERR_ALIAS, "%s: out_lse overlaps recv or out", who);
+        if (!vul.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out_lse entries overlap", who);
+    }
+    // The LSE of each row is the fp32 word right after its payload: the same
+    // rows seen as fp32 words, offset by D*e bytes.
+    const unsigned char* rbase = (const unsigned char*)recv;
+    const float* lse = (const float*)(rbase + rb);
+    return run_merge(who, dtype, e, N, B, Hpr, D, G, rbase, r_sg * e, r_sn * e, r_sb * e, r_sh * e,
+                     lse, r_sg * e / 4, r_sn * e / 4, r_sb * e / 4, r_sh * e / 4, out, u_sg * e,
+                     u_sb * e, u_sh * e, out_lse, ul_sg, ul_sb, ul_sh, lse_base, return_lse, flags,
+                     vr.align(), vu.align(), false, (cudaStream_t)stream);
+}
+
+}  // extern "C"

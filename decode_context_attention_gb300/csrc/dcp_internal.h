@@ -1,0 +1,63 @@
+// dcp_internal.h -- host-side launch interface between the C ABI (dcp_abi.cu)
+// and the kernels (dcp_pack.cu, dcp_combine_*.cu).  Not installed; the public
+// interface is include/dcp.h.
+//
+// All payload strides here are in BYTES and all LSE strides in fp32 WORDS; the
+// ABI layer converts the caller's element strides once, after validation.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dcp {
+
+constexpr int kThreads = 256;  // threads per CTA for every kernel here
+
+struct PackParams {
+    int N, B, H, D, G, H_pr;
+    int64_t rows;        // G * B * H source rows
+    int row_bytes;       // D * element size
+    int vb;              // vector width in bytes (16, 4 or 2)
+    int lpr;             // lanes cooperating on one row (power of two <= 32)
+    int copy_payload;    // 0: skip the payload (single-rank in-place combine)
+    int copy_lse;        // 0: skip the LSE words (single-rank combine without return_lse)
+    const unsigned char* o;
+    int64_t o_sg, o_sb, o_sh;
+    const float* lse;
+    int64_t l_sg, l_sb, l_sh;
+    unsigned char* dst_o;
+    int64_t do_sg, do_sn, do_sb, do_sh;
+    float* dst_lse;
+    int64_t dl_sg, dl_sn, dl_sb, dl_sh;
+};
+
+struct CombineParams {
+    int N, B, Hc, D, G;
+    int64_t rows;        // G * B * Hc output rows
+    int vec_per_row;     // D * element size / vector width
+    int lpr;             // lanes cooperating on one row (power of two <= 32)
+    int base2;           // LSE base: 0 = e, 1 = 2
+    int return_lse;
+    int sanitize;        // NaN/+-inf elements of O count as 0
+    const unsigned char* o;
+    int64_t o_sg, o_sn, o_sb, o_sh;
+    const float* lse;
+    int64_t l_sg, l_sn, l_sb, l_sh;
+    unsigned char* out;
+    int64_t u_sg, u_sb, u_sh;
+    float* out_lse;
+    int64_t ul_sg, ul_sb, ul_sh;
+};
+
+// Launchers return the launch's cudaGetLastError().
+cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
+cudaError_t launch_combine_f32(const CombineParams& p, int vb, cudaStream_t stream);
+cudaError_t launch_combine_f16(const CombineParams& p, int vb, cudaStream_t stream);
+cudaError_t launch_combine_bf16(const CombineParams& p, int vb, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+// Resident CTAs per SM of `kernel` at kThreads threads (cached per device and kernel).
+int ctas_per_sm(const void* kernel);
+
+}  // namespace dcp

@@ -1,0 +1,195 @@
+/*
+ * dcp.h -- C ABI of libdcp_gb300.so: the data-parallel hot path of decode
+ * context parallelism (DCP) on one GB300 (sm_103a).
+ *
+ * DCP splits a request's KV cache across the N ranks of a group; every rank
+ * returns a partial attention output O_r [B, H, D] and its log-sum-exp
+ * lse_r [B, H] (fp32), and the partials are merged with LSE weights.  This
+ * library implements the three steps of that merge:
+ *
+ *   dcp_pack_send       scatter O and LSE into a send layout (peer-major
+ *                       interleaved or peer-inside split), by strides alone;
+ *   dcp_lse_combine     the LSE-weighted combine over strided views;
+ *   dcp_unpack_combine  the combine reading interleaved [payload | LSE word]
+ *                       receive rows in one pass.
+ *
+ * The cross-rank exchange itself (NCCL all-to-all, MNNVL, all-gather /
+ * all-reduce) is not part of this library.  A group's N ranks can be held as
+ * one stacked tensor on one device; the "received" views then address the
+ * sender stack with swapped strides, or a relayout of it.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Pointers are DEVICE pointers on the current CUDA device.  The caller owns
+ *   every buffer.  The library allocates nothing, frees nothing, never
+ *   synchronises, and enqueues its kernels on `stream` (a cudaStream_t; NULL
+ *   means the legacy default stream).  Work is asynchronous: results are
+ *   valid once the stream reaches that point.
+ * - Strides are in ELEMENTS of the pointed-to type: payload elements (dtype)
+ *   for O / dst_o / out / recv, fp32 words for every LSE pointer.  Strides
+ *   must be >= 0.  The innermost (D) stride is always 1 and is not passed.
+ * - Sizes: N >= 1 and D >= 1.  B, H (or Hc, Hpr) and G may be 0, in which
+ *   case the call does nothing and returns DCP_OK.  N <= 4096.
+ * - G is a batch of independent groups (for example all N destination ranks,
+ *   or all N source ranks, of a group held on one device).
+ * - Validation happens on the host, before any launch; a failing call
+ *   launches nothing and returns a non-zero dcp_status_t.
+ *   dcp_last_error_message() then describes the failure (per host thread).
+ * - DCP_ERR_CUDA is returned when a launch fails (cudaGetLastError); the CUDA
+ *   error string is in dcp_last_error_message().
+ * - Outputs must not overlap inputs, except where an entry point says so;
+ *   the rows of one output must not overlap one another.
+ *
+ * Payload types: DCP_F32, DCP_F16, DCP_BF16.  LSE values are always fp32.
+ */
+#ifndef DCP_GB300_DCP_H_
+#define DCP_GB300_DCP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dcp_status {
+    DCP_OK = 0,
+    DCP_ERR_INVALID_ARG = 1,          /* bad size, NULL pointer, negative stride, bad flag */
+    DCP_ERR_UNSUPPORTED_DTYPE = 2,    /* dtype other than f32 / f16 / bf16 */
+    DCP_ERR_HEADS_NOT_DIVISIBLE = 3,  /* H % N != 0 in the pack */
+    DCP_ERR_MISALIGNED = 4,           /* D % lpd != 0, or a pointer/stride not aligned to its type */
+    DCP_ERR_ALIAS = 5,                /* an output overlaps an input or itself */
+    DCP_ERR_CUDA = 6                  /* a CUDA call failed; see dcp_last_error_message() */
+} dcp_status_t;
+
+enum { DCP_F32 = 0, DCP_F16 = 1, DCP_BF16 = 2 };
+enum { DCP_LSE_BASE_E = 0, DCP_LSE_BASE_2 = 1 };
+
+/* Flags of dcp_lse_combine / dcp_unpack_combine. */
+enum {
+    /* Replace NaN/+-inf elements of O by 0 before weighting (the ag_rs merge's
+     * nan_to_num_ on the partial output; sglang PR #34213 report,
+     * "关键源码片段", `cp_lse_ag_out_rs_mha`). */
+    DCP_SANITIZE_O = 1u,
+    /* dcp_lse_combine only: `out` IS the rank-0 slice of `o` (same pointer and
+     * the same G/B/H strides); each row's rank-0 partial is overwritten by the
+     * merged row after all N ranks of that row were read (sglang PR #34213
+     * report, "实现拆解" item 2). */
+    DCP_INPLACE_RANK0 = 2u
+};
+
+/*
+ * Payload elements one fp32 LSE word occupies in an interleaved row:
+ * 1 for DCP_F32, 2 for DCP_F16 and DCP_BF16, -1 for anything else.
+ * (vLLM PR #41160 report, "实现拆解" item 2, `_dcp_a2a_lse_pack_dim`:
+ * fp16 -> 2, fp32 -> 1, other types rejected; bf16 is the other 16-bit type.)
+ */
+int dcp_lse_pack_dim(int dtype);
+
+/* Static English text for a status code (never NULL). */
+const char* dcp_status_string(int status);
+
+/* Details of the last failing call made by this host thread ("" if none). */
+const char* dcp_last_error_message(void);
+
+/*
+ * dcp_pack_send -- the shared, stride-parameterised pack.
+ * (sglang PR #34651 report, "实现拆解" items 1-3 and "关键源码片段",
+ * `dcp_pack_a2a_send` / `_dcp_pack_a2a_send_kernel`; vLLM PR #41160 report,
+ * "实现拆解" item 1, `_dcp_a2a_pack_send_kernel`.)
+ *
+ * For each group g < G, token b < B and head h < H, with H_pr = H / N,
+ * peer p = h / H_pr and local head hl = h % H_pr:
+ *     dst_o  [g][p, b, hl, 0:D] = o  [g][b, h, 0:D]     (bit copy)
+ *     dst_lse[g][p, b, hl]      = lse[g][b, h]          (bit copy)
+ * and no other byte is written.
+ *
+ *   o        [G][B, H, D]       payload, strides (o_sg, o_sb, o_sh)
+ *   lse      [G][B, H]          fp32, strides (l_sg, l_sb, l_sh)
+ *   dst_o    [G][N, B, H_pr, D] payload, strides (do_sg, do_sn, do_sb, do_sh)
+ *   dst_lse  [G][N, B, H_pr]    fp32, strides (dl_sg, dl_sn, dl_sb, dl_sh)
+ *
+ * Peer-major interleaved send buffer [N, B, H_pr, D + lpd] (one flat buffer
+ * split by byte offset for a single all-to-all): dst_o = buffer with strides
+ * (B*H_pr*(D+lpd), H_pr*(D+lpd), D+lpd); dst_lse = (float*)buffer + D/lpd with
+ * the same strides divided by lpd.  Peer-inside split layout (O [B,H_pr,N,D],
+ * stats [B,H_pr,N,2]): dst_o = partial_o permuted to [N,B,H_pr,D], dst_lse =
+ * stats[..., 0] permuted to [N,B,H_pr]; stats slot 1 is never touched.
+ *
+ * dst_lse may lie inside dst_o's buffer only as in the interleaved layout:
+ * the same byte strides, starting at or after byte D*e of each row and ending
+ * before the next row.  Errors: DCP_ERR_HEADS_NOT_DIVISIBLE if H % N != 0;
+ * DCP_ERR_ALIAS for any other overlap; DCP_ERR_MISALIGNED for pointers not
+ * aligned to their element size.
+ */
+dcp_status_t dcp_pack_send(int dtype, int N, int B, int H, int D, int G,
+                           const void* o, int64_t o_sg, int64_t o_sb, int64_t o_sh,
+                           const float* lse, int64_t l_sg, int64_t l_sb, int64_t l_sh,
+                           void* dst_o, int64_t do_sg, int64_t do_sn, int64_t do_sb, int64_t do_sh,
+                           float* dst_lse, int64_t dl_sg, int64_t dl_sn, int64_t dl_sb, int64_t dl_sh,
+                           void* stream);
+
+/*
+ * dcp_lse_combine -- LSE-weighted merge of N rank partials over strided views.
+ * (sglang PR #34213 report, "关键源码片段", `cp_lse_ag_out_rs_mha`;
+ * sglang PR #34651 report, "实现拆解" item 3, `dcp_lse_combine_triton`
+ * reading the non-contiguous receive views; sglang PR #33926 report,
+ * "实现拆解" item 4 and "关联脉络" #34240: base-2 vs natural-log LSE.)
+ *
+ * For each row (g, b, h), over ranks r = 0..N-1, in the LSE base `lse_base`:
+ *     Gl   = logsumexp_r lse[g][r, b, h]
+ *            (any NaN -> NaN; else any +inf -> +inf; else all -inf -> -inf)
+ *     w_r  = base^(lse_r - Gl), replaced by 0 when NaN or +-inf
+ *     out[g][b, h, :] = sum_r w_r * O[g][r, b, h, :]   (fp32 accumulation,
+ *                        rounded once to the payload type)
+ *     out_lse[g][b, h] = Gl (same base as the input), when return_lse != 0.
+ * With DCP_SANITIZE_O, NaN/+-inf elements of O count as 0.  N == 1 returns
+ * the input unchanged (bit copy of O and LSE), as the single-rank early
+ * return of `cp_lse_ag_out_rs_mha` does.
+ *
+ *   o        [G][N, B, Hc, D] payload, strides (o_sg, o_sn, o_sb, o_sh)
+ *   lse      [G][N, B, Hc]    fp32, strides (l_sg, l_sn, l_sb, l_sh)
+ *   out      [G][B, Hc, D]    payload, strides (u_sg, u_sb, u_sh)
+ *   out_lse  [G][B, Hc]       fp32, strides (ul_sg, ul_sb, ul_sh); may be NULL
+ *                             when return_lse == 0
+ *
+ * flags: DCP_SANITIZE_O | DCP_INPLACE_RANK0.  With DCP_INPLACE_RANK0, `out`
+ * must equal `o` with u_sg == o_sg, u_sb == o_sb, u_sh == o_sh, and the rows
+ * of `o` must not overlap one another; the caller's rank-0 partial is dead
+ * after the call.  Per-rank head slices of the result (rank k keeps heads
+ * [k*Hc/N, (k+1)*Hc/N)) are plain views of `out` and `out_lse`.
+ */
+dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
+                             const void* o, int64_t o_sg, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                             const float* lse, int64_t l_sg, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                             void* out, int64_t u_sg, int64_t u_sb, int64_t u_sh,
+                             float* out_lse, int64_t ul_sg, int64_t ul_sb, int64_t ul_sh,
+                             int lse_base, int return_lse, unsigned flags, void* stream);
+
+/*
+ * dcp_unpack_combine -- the combine reading the interleaved receive buffer.
+ * (vLLM PR #41160 report, "实现拆解" item 1, `_dcp_a2a_unpack_combine_kernel`;
+ * sglang PR #34651 report, "实现拆解" item 2: one flat buffer split by byte
+ * offset, receive side unchanged.)
+ *
+ *   recv     [G][N, B, Hpr, D + lpd] payload, strides (r_sg, r_sn, r_sb, r_sh);
+ *            in each row the first D elements are rank r's partial O and the
+ *            fp32 word at word index D / lpd (bytes D*e .. D*e+3) is its LSE.
+ *   out      [G][B, Hpr, D]  payload, strides (u_sg, u_sb, u_sh)
+ *   out_lse  [G][B, Hpr]     fp32, strides (ul_sg, ul_sb, ul_sh); may be NULL
+ *                            when return_lse == 0
+ *
+ * Same arithmetic, flags (except DCP_INPLACE_RANK0, rejected) and N == 1 rule
+ * as dcp_lse_combine.  Errors: DCP_ERR_MISALIGNED if D % lpd != 0 or a row
+ * start is not 4-byte aligned; DCP_ERR_ALIAS if out / out_lse overlap recv.
+ */
+dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
+                                const void* recv, int64_t r_sg, int64_t r_sn, int64_t r_sb, int64_t r_sh,
+                                void* out, int64_t u_sg, int64_t u_sb, int64_t u_sh,
+                                float* out_lse, int64_t ul_sg, int64_t ul_sb, int64_t ul_sh,
+                                int lse_base, int return_lse, unsigned flags, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* DCP_GB300_DCP_H_ */

@@ -1,0 +1,125 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/dcp.h declares, and rejects bad arguments on the host before
+any CUDA call (each call below fails validation, so nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from decode_context_attention_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dcp.h")
+
+F32, F16, BF16 = 0, 1, 2
+# plausible but never dereferenced device addresses
+A = 0x10000000
+Bp = 0x20000000
+C = 0x30000000
+Dp = 0x40000000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dcp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_exactly_the_binding_exports():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_lse_pack_dim(lib):
+    assert binding.dcp_lse_pack_dim(F32) == 1
+    assert binding.dcp_lse_pack_dim(F16) == 2
+    assert binding.dcp_lse_pack_dim(BF16) == 2
+    assert binding.dcp_lse_pack_dim(7) == -1
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert binding.dcp_status_string(code)
+    assert binding.dcp_status_string(99) == "unknown status"
+
+
+def pack(dtype=F32, N=2, B=2, H=4, D=8, G=1, o=A, o_s=(64, 32, 8), lse=Bp, l_s=(8, 4, 1),
+         dst=C, d_s=(80, 40, 20, 10), dl=Dp, dl_s=(8, 4, 2, 1)):
+    return binding.dcp_pack_send(dtype, N, B, H, D, G, o, *o_s, lse, *l_s, dst, *d_s, dl, *dl_s, None)
+
+
+def test_pack_validation(lib):
+    assert pack(dtype=5) == 2
+    assert pack(N=0) == 1
+    assert pack(N=4097, H=4097) == 1
+    assert pack(D=0) == 1
+    assert pack(B=-1) == 1
+    assert pack(N=3) == 3                      # H % N != 0
+    assert "not a multiple" in binding.dcp_last_error_message()
+    assert pack(o=0) == 1                      # NULL
+    assert pack(o_s=(64, -32, 8)) == 1         # negative stride
+    assert pack(dtype=F16, o=A + 1) == 4       # misaligned payload pointer
+    assert pack(dl=Dp + 2) == 4                # misaligned LSE pointer
+    assert pack(dst=A + 16) == 5               # destination overlaps source
+    assert pack(d_s=(80, 40, 0, 10), B=2) == 5  # destination rows overlap one another
+    # LSE words inside the payload region of the destination rows
+    assert pack(dl=C + 4, dl_s=(80, 40, 20, 10)) == 5
+    # empty problems are a no-op that launches nothing
+    assert pack(B=0) == 0 and pack(G=0) == 0 and pack(H=0) == 0
+
+
+def combine(dtype=F32, N=2, B=2, Hc=4, D=8, G=1, o=A, o_s=(128, 64, 32, 8), lse=Bp,
+            l_s=(16, 8, 4, 1), out=C, u_s=(64, 32, 8), out_lse=Dp, ul_s=(8, 4, 1), base=0,
+            ret=1, flags=0):
+    return binding.dcp_lse_combine(dtype, N, B, Hc, D, G, o, *o_s, lse, *l_s, out, *u_s,
+                                   out_lse, *ul_s, base, ret, flags, None)
+
+
+def test_combine_validation(lib):
+    assert combine(dtype=9) == 2
+    assert combine(N=0) == 1
+    assert combine(base=3) == 1
+    assert combine(flags=8) == 1
+    assert combine(out=0) == 1
+    assert combine(out_lse=0) == 1               # return_lse needs out_lse
+    assert combine(out=C + 2) == 4               # f32 output needs 4-byte alignment
+    assert combine(out=A) == 5                   # overlaps o without the in-place flag
+    assert combine(out=Bp) == 5                  # overlaps lse
+    assert combine(out_lse=C) == 5               # out_lse overlaps out
+    assert combine(flags=2, out=C) == 1          # in-place output must be o's rank-0 slice
+    assert combine(flags=2, out=A, u_s=(128, 64, 16)) == 1  # ... with the same strides
+    assert combine(flags=2, out=A, u_s=(128, 32, 8), o_s=(128, 0, 32, 8)) == 5  # ranks overlap
+    assert combine(B=0) == 0 and combine(Hc=0) == 0 and combine(G=0) == 0
+
+
+def unpack(dtype=F16, N=2, B=2, Hpr=4, D=8, G=1, recv=A, r_s=(160, 80, 40, 10),
+           out=C, u_s=(64, 32, 8), out_lse=Dp, ul_s=(8, 4, 1), base=0, ret=1, flags=0):
+    return binding.dcp_unpack_combine(dtype, N, B, Hpr, D, G, recv, *r_s, out, *u_s,
+                                      out_lse, *ul_s, base, ret, flags, None)
+
+
+def test_unpack_validation(lib):
+    assert unpack(D=7) == 4                       # D % lpd != 0 (lpd = 2 for f16)
+    assert unpack(r_s=(160, 80, 40, 11)) == 4     # rows 22 bytes apart: not 4-byte aligned
+    assert unpack(recv=A + 2) == 4
+    assert unpack(flags=2) == 1                   # in-place is a dcp_lse_combine feature
+    assert unpack(out=A + 64) == 5                # out overlaps recv
+    assert unpack(B=0) == 0
+
+
+def test_binding_raises_with_message(lib):
+    with pytest.raises(binding.DcpError) as ei:
+        binding.check(pack(N=3), "dcp_pack_send")
+    assert ei.value.name == "DCP_ERR_HEADS_NOT_DIVISIBLE"
