@@ -7,8 +7,9 @@ partial outputs, base-2 LSE.  One step is the whole hot path for all 8 ranks
 held on one GPU: the peer-inside pack of every source rank (one launch, G = 8)
 followed by the LSE combine for every destination rank (one launch, G = 8)
 over the receive views; the all-to-all between them is a zero-copy view of
-the sender stack.  L2 is flushed (a 2x-L2 memset) before every kernel, outside
-the timed events, so every kernel reads its inputs from HBM.
+the sender stack.  L2 is flushed before every kernel (a 2x-L2 write, then a
+2x-L2 read so no dirty lines are left), outside the timed events, so every
+kernel reads its inputs from HBM.
 
 Also measured in the same run and reported under "secondary": the in-place
 sanitising combine of the cached-extend workload (N = 8, 16384 tokens, 96
@@ -162,14 +163,22 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class L2Flush:
+    """Evict L2 between timed launches: write one buffer of 2x L2, then read a
+    second one, so L2 ends up holding clean lines of neither the inputs nor the
+    flush (a write-only flush would leave dirty lines whose write-back the next
+    timed kernel would pay for)."""
+
     def __init__(self, device):
         import torch
 
         l2 = torch.cuda.get_device_properties(device).L2_cache_size
-        self.buf = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=device)
+        n = max(2 * l2, 64 << 20)
+        self.wbuf = torch.empty(n, dtype=torch.uint8, device=device)
+        self.rbuf = torch.zeros(n // 4, dtype=torch.float32, device=device)
 
     def __call__(self):
-        self.buf.zero_()
+        self.wbuf.zero_()
+        self.rbuf.amax()
 
 
 def time_sequence(launches, steps, warmup, flush, device):
@@ -403,7 +412,7 @@ def run_gpu(args):
     dom = max(range(len(kernels)), key=lambda j: kernels[j]["us_per_launch"])
 
     # --- e2e: host buffers in, host result out, through the public binding ------
-    e2e = run_e2e(mla, args, device)
+    e2e = None if args.no_e2e else run_e2e(mla, args, device)
 
     # --- secondary workloads (same run) ----------------------------------------
     secondary = []
@@ -444,7 +453,8 @@ def run_gpu(args):
         "config": {"workload": f"mla_decode N={w.N} B={w.B} H={w.H} D={w.D} bf16 base-2, "
                                "peer-inside pack + combine over strided recv views, all ranks on "
                                "one GPU", "calls_per_step_per_gpu": 1,
-                   "l2": "flushed (2x L2 memset) before every kernel, outside the timed events",
+                   "l2": "flushed before every kernel (2x-L2 write, then 2x-L2 read), outside "
+                         "the timed events",
                    "parallelism": f"{world} independent replica(s), no collective"},
         "roofline": {"bound": "hbm", "kernel": k["kernel"], "achieved": k["achieved_gbs"],
                      "peak": peak, "unit": "GB/s", "frac": k["frac_of_measured_hbm"],
@@ -564,6 +574,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -8,6 +8,7 @@
 
 #include <atomic>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <utility>
 
@@ -31,18 +32,22 @@ int device_sm_count() {
     return n;
 }
 
-int ctas_per_sm(const void* kernel) {
+int ctas_per_sm(const void* kernel, int threads, size_t smem) {
     static std::mutex mu;
-    static std::map<std::pair<int, const void*>, int> cache;
+    static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
     std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find({dev, kernel});
+    const auto key = std::make_tuple(dev, kernel, threads, smem);
+    auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+        n < 1)
         n = 1;
-    cache[{dev, kernel}] = n;
+    cache[key] = n;
     return n;
 }
 

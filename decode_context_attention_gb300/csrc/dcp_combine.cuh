@@ -1,8 +1,8 @@
-// dcp_combine.cuh -- the LSE-weighted merge kernel (templated over the payload
-// type, the vector width and the maximum rank count), included by one
-// translation unit per payload type.
+// dcp_combine.cuh -- the LSE-weighted merge kernels (templated over the payload
+// type, the vector width, the rank count and the O-sanitising flag), included
+// by one translation unit per payload type.
 //
-// What it computes, per output row (g, b, h), over ranks r < N (sglang PR
+// What they compute, per output row (g, b, h), over ranks r < N (sglang PR
 // #34213 report, "关键源码片段", `cp_lse_ag_out_rs_mha`; sglang PR #34651
 // report, "实现拆解" item 3, `dcp_lse_combine_triton`):
 //     Gl  = logsumexp_r lse_r   in base e or base 2 (sglang PR #33926 report,
@@ -20,16 +20,38 @@
 //    lane r of the group loads lse_r, and the max / NaN-inf class / sum of
 //    exponentials are reduced with xor shuffles inside the group, then each
 //    rank's weight is broadcast to the group with one shuffle;
-//  * each lane streams its slice of every rank's row with 16-byte loads when
-//    every row start is 16-byte aligned (4- or 2-byte otherwise), issuing all
-//    ranks' loads of a chunk before any arithmetic so 8-16 KiB per warp are in
-//    flight;
-//  * persistent grid: SM count x resident CTAs, grid-stride over rows.
+//  * payload is streamed with 16-byte vectors when every row start is 16-byte
+//    aligned (4- or 2-byte otherwise); 16-bit elements are widened two at a
+//    time and accumulated with paired fp32 FMAs (fma.rn.f32x2), about 1.5
+//    instructions per element, so the merge stays below the HBM time;
+//  * two variants keep bytes in flight: a register variant issues all ranks'
+//    loads of a chunk before the weights are reduced; a staged variant copies
+//    the next rows' rank stack into shared memory with cp.async, rows several
+//    deep, while it merges the current row;
+//  * persistent grid: SM count x resident CTAs, grid-stride over rows with
+//    division-free row cursors.
 #pragma once
 
 #include <math.h>
 
 #include "dcp_device.cuh"
+
+// Tuning knobs (compile-time): use the fixed-shape merge for the common row
+// lengths; use the cp.async-staged merge where it applies (off: measured
+// slower than the register variants on GB300), its pipeline depth (rows) and
+// warps per CTA.
+#ifndef DCP_COMBINE_FIXED
+#define DCP_COMBINE_FIXED 1
+#endif
+#ifndef DCP_COMBINE_STAGED
+#define DCP_COMBINE_STAGED 0
+#endif
+#ifndef DCP_STAGES
+#define DCP_STAGES 3
+#endif
+#ifndef DCP_STAGED_WARPS
+#define DCP_STAGED_WARPS 4
+#endif
 
 namespace dcp {
 
@@ -47,72 +69,64 @@ __device__ __forceinline__ float global_lse_from(unsigned cls, float m, float s,
     return m + lse_log(s, b2);
 }
 
-// Weights of ranks r < NRMAX (entries r >= N are 0) and the global LSE, for
-// the row whose rank-0 LSE is at `lrow` (rank stride `l_sn` words).
-template <int NRMAX>
-__device__ __forceinline__ void row_weights(const float* lrow, int64_t l_sn, int N,
-                                            const LaneGroup& lg, int lpr, bool b2,
-                                            float (&w)[NRMAX], float& Gl) {
-    if (N <= lpr) {
-        // warp-shuffle logsumexp: lane r holds lse_r
-        const float l = lg.jl < N ? __ldg(lrow + (int64_t)lg.jl * l_sn) : -INFINITY;
-        unsigned cls = isnan(l) ? kHasNaN : (l == INFINITY ? kHasPosInf : 0u);
-        float m = cls ? -INFINITY : l;
-        for (int off = lpr >> 1; off > 0; off >>= 1) {
-            m = fmaxf(m, __shfl_xor_sync(lg.mask, m, off, lpr));
-            cls |= __shfl_xor_sync(lg.mask, cls, off, lpr);
-        }
-        float wl = 0.f;
-        float s = 0.f;
-        if (cls == 0u && m != -INFINITY) {
-            const float el = lse_exp(l - m, b2);  // lanes with -inf (or no rank) hold 0
-            s = el;
-            for (int off = lpr >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(lg.mask, s, off, lpr);
-            wl = el / s;  // = base^(l - Gl) without the rounding of Gl
-        }
-        Gl = global_lse_from(cls, m, s, b2);
-#pragma unroll
-        for (int r = 0; r < NRMAX; ++r) w[r] = __shfl_sync(lg.mask, wl, r & (lpr - 1), lpr);
-#pragma unroll
-        for (int r = 0; r < NRMAX; ++r)
-            if (r >= N || r >= lpr) w[r] = 0.f;
-    } else {
-        // more ranks than lanes in the group: every lane reduces serially
-        float l[NRMAX];
-        unsigned cls = 0u;
-        float m = -INFINITY;
-#pragma unroll
-        for (int r = 0; r < NRMAX; ++r) {
-            l[r] = r < N ? __ldg(lrow + (int64_t)r * l_sn) : -INFINITY;
-            if (isnan(l[r])) cls |= kHasNaN;
-            else if (l[r] == INFINITY) cls |= kHasPosInf;
-            else m = fmaxf(m, l[r]);
-        }
-        float s = 0.f;
-#pragma unroll
-        for (int r = 0; r < NRMAX; ++r) w[r] = 0.f;
-        if (cls == 0u && m != -INFINITY) {
-#pragma unroll
-            for (int r = 0; r < NRMAX; ++r) {
-                w[r] = lse_exp(l[r] - m, b2);  // -inf and absent ranks give 0
-                s += w[r];
-            }
-            const float inv = 1.f / s;
-#pragma unroll
-            for (int r = 0; r < NRMAX; ++r) w[r] *= inv;
-        }
-        Gl = global_lse_from(cls, m, s, b2);
+// Shuffle logsumexp over a lane group: lane r holds lse_r (-inf for lanes
+// without a rank).  Returns this lane's weight; Gl gets the global LSE.
+__device__ __forceinline__ float group_weight(float l, const LaneGroup& lg, int lpr, bool b2, float& Gl) {
+    unsigned cls = isnan(l) ? kHasNaN : (l == INFINITY ? kHasPosInf : 0u);
+    float m = cls ? -INFINITY : l;
+    for (int off = lpr >> 1; off > 0; off >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(lg.mask, m, off, lpr));
+        cls |= __shfl_xor_sync(lg.mask, cls, off, lpr);
     }
+    float wl = 0.f, s = 0.f;
+    if (cls == 0u && m != -INFINITY) {
+        const float el = lse_exp(l - m, b2);  // lanes with -inf (or no rank) hold 0
+        s = el;
+        for (int off = lpr >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(lg.mask, s, off, lpr);
+        wl = el / s;
+    }
+    Gl = global_lse_from(cls, m, s, b2);
+    return wl;
 }
 
-// Ranks per load batch: all loads of a batch are issued before its arithmetic.
+// Weights of ranks r < NRMAX (0 for r >= N) when a lane group is narrower than
+// the rank count: every lane reduces serially.
 template <int NRMAX>
-struct RankChunk { static constexpr int value = NRMAX < 8 ? NRMAX : 8; };
+__device__ __forceinline__ void serial_weights(const float* lrow, int64_t l_sn, int N, bool b2,
+                                               float (&w)[NRMAX], float& Gl) {
+    float l[NRMAX];
+    unsigned cls = 0u;
+    float m = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < NRMAX; ++r) {
+        l[r] = r < N ? __ldg(lrow + (int64_t)r * l_sn) : -INFINITY;
+        if (isnan(l[r])) cls |= kHasNaN;
+        else if (l[r] == INFINITY) cls |= kHasPosInf;
+        else m = fmaxf(m, l[r]);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < NRMAX; ++r) w[r] = 0.f;
+    if (cls == 0u && m != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < NRMAX; ++r) {
+            w[r] = lse_exp(l[r] - m, b2);  // -inf and absent ranks give 0
+            s += w[r];
+        }
+        const float inv = 1.f / s;
+#pragma unroll
+        for (int r = 0; r < NRMAX; ++r) w[r] *= inv;
+    }
+    Gl = global_lse_from(cls, m, s, b2);
+}
 
-template <typename T, int VB, int NRMAX>
+// ---------------------------------------------------------------------------
+// Register variant.
+// ---------------------------------------------------------------------------
+template <typename T, int VB, int NRMAX, bool SAN>
 __global__ void __launch_bounds__(kThreads, 2) combine_kernel(const CombineParams p) {
     constexpr int EPV = VB / (int)sizeof(T);
-    constexpr int RC = RankChunk<NRMAX>::value;
+    constexpr int RC = NRMAX < 8 ? NRMAX : 8;  // ranks per load batch
     // vectors per lane per batch: at most ~64 registers of loaded payload and
     // 32 fp32 accumulators, so two CTAs fit on an SM without spilling
     constexpr int KU_LD = 64 / (RC * (VB / 4 > 0 ? VB / 4 : 1));
@@ -122,23 +136,24 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(const CombineParam
     using V = typename VecT<VB>::type;
 
     const LaneGroup lg = lane_group(p.lpr);
+    const int lpr = p.lpr;
     const bool b2 = p.base2 != 0;
     const int N = p.N;
     const int nv = p.vec_per_row;
-    for (int64_t row = lg.first; row < p.rows; row += lg.step) {
-        const int64_t h = row % p.Hc;
-        const int64_t t = row / p.Hc;
-        const int64_t b = t % p.B;
-        const int64_t g = t / p.B;
-
+    RowStep st;
+    st.set(lg.step, p.B, p.Hc);
+    RowCursor c;
+    c.set(lg.first, p.B, p.Hc);
+    for (int64_t row = lg.first; row < p.rows; row += lg.step, c.add(st.dg, st.db, st.dh, p.B, p.Hc)) {
+        const float* lrow = p.lse + c.g * p.l_sg + (int64_t)c.b * p.l_sb + (int64_t)c.h * p.l_sh;
+        const unsigned char* orow = p.o + c.g * p.o_sg + (int64_t)c.b * p.o_sb + (int64_t)c.h * p.o_sh;
+        unsigned char* urow = p.out + c.g * p.u_sg + (int64_t)c.b * p.u_sb + (int64_t)c.h * p.u_sh;
+        const bool shuffle = N <= lpr;
+        const float l = shuffle && lg.jl < N ? __ldg(lrow + (int64_t)lg.jl * p.l_sn) : -INFINITY;
         float w[NRMAX];
-        float Gl;
-        row_weights<NRMAX>(p.lse + g * p.l_sg + b * p.l_sb + h * p.l_sh, p.l_sn, N, lg, p.lpr, b2,
-                           w, Gl);
-
-        const unsigned char* orow = p.o + g * p.o_sg + b * p.o_sb + h * p.o_sh;
-        unsigned char* urow = p.out + g * p.u_sg + b * p.u_sb + h * p.u_sh;
-        for (int v0 = lg.jl; v0 < nv; v0 += p.lpr * KU) {
+        float Gl = 0.f;
+        // group-uniform chunk loop (every lane runs the same iterations)
+        for (int base = 0; base < nv; base += lpr * KU) {
             float acc[KU][EPV];
 #pragma unroll
             for (int k = 0; k < KU; ++k)
@@ -146,42 +161,140 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(const CombineParam
                 for (int i = 0; i < EPV; ++i) acc[k][i] = 0.f;
 #pragma unroll
             for (int r0 = 0; r0 < NRMAX; r0 += RC) {
+                if (r0 >= N) break;
                 V x[KU][RC];
 #pragma unroll
                 for (int k = 0; k < KU; ++k) {
-                    const int v = v0 + k * p.lpr;
+                    const int v = base + lg.jl + k * lpr;
 #pragma unroll
                     for (int j = 0; j < RC; ++j)
                         if (r0 + j < N && v < nv)
                             x[k][j] = ld_stream<VB>(orow + (int64_t)(r0 + j) * p.o_sn + (int64_t)v * VB);
                 }
+                if (r0 == 0 && base == 0) {
+                    // the weights are reduced while the first loads are in flight
+                    if (shuffle) {
+                        const float wl = group_weight(l, lg, lpr, b2, Gl);
 #pragma unroll
-                for (int k = 0; k < KU; ++k) {
-#pragma unroll
-                    for (int j = 0; j < RC; ++j) {
-                        if (r0 + j < N) {
-                            float f[EPV];
-                            unpack_vec<T, VB>(x[k][j], f);
-#pragma unroll
-                            for (int i = 0; i < EPV; ++i) {
-                                const float ov = (p.sanitize && !isfinite(f[i])) ? 0.f : f[i];
-                                acc[k][i] = fmaf(w[r0 + j], ov, acc[k][i]);
-                            }
-                        }
+                        for (int r = 0; r < NRMAX; ++r)
+                            w[r] = r < N ? __shfl_sync(lg.mask, wl, r & (lpr - 1), lpr) : 0.f;
+                    } else {
+                        serial_weights<NRMAX>(lrow, p.l_sn, N, b2, w, Gl);
                     }
                 }
+#pragma unroll
+                for (int k = 0; k < KU; ++k)
+#pragma unroll
+                    for (int j = 0; j < RC; ++j)
+                        if (r0 + j < N) fma_vec<T, VB, SAN>(acc[k], x[k][j], w[r0 + j]);
             }
 #pragma unroll
             for (int k = 0; k < KU; ++k) {
-                const int v = v0 + k * p.lpr;
-                if (v < nv) st_vec<VB>(urow + (int64_t)v * VB, pack_vec<T, VB>(acc[k]));
+                const int v = base + lg.jl + k * lpr;
+                if (v < nv) st_vec<VB>(urow + (int64_t)v * VB, round_vec<T, VB>(acc[k]));
             }
         }
-        if (p.return_lse && lg.jl == 0) p.out_lse[g * p.ul_sg + b * p.ul_sb + h * p.ul_sh] = Gl;
+        if (p.return_lse && lg.jl == 0) p.out_lse[c.g * p.ul_sg + (int64_t)c.b * p.ul_sb + (int64_t)c.h * p.ul_sh] = Gl;
     }
 }
 
-// Any N: weights are recomputed per batch of 8 ranks from a serial reduction.
+// ---------------------------------------------------------------------------
+// Fixed-shape variant for the common rows: LPR lanes per row and VPL vectors
+// per lane per rank are compile-time constants (row bytes = LPR * VPL * VB
+// exactly), so every load and store offset is an immediate, and the fp32
+// accumulators live as packed pairs for the whole row.  Needs N <= LPR (the
+// shuffle reduction) and N <= NR.
+// ---------------------------------------------------------------------------
+template <typename T, int VB, int NR, int LPR, int VPL, bool SAN>
+__global__ void __launch_bounds__(kThreads, 2) combine_fixed_kernel(const CombineParams p) {
+    constexpr int NP = VB / (int)sizeof(T) / 2;  // fp32 pairs per vector
+    // vectors per lane per rank loaded at once: <= 64 registers of payload
+    constexpr int WPV = VB / 4;
+    constexpr int VCH0 = 64 / (NR * WPV) > 0 ? 64 / (NR * WPV) : 1;
+    constexpr int VCH = VCH0 >= VPL ? VPL : VCH0;
+    static_assert(VPL % VCH == 0, "chunks must tile the row");
+    using V = typename VecT<VB>::type;
+
+    const int lane = threadIdx.x & 31;
+    LaneGroup lg;
+    lg.jl = lane & (LPR - 1);
+    lg.sub = lane / LPR;
+    lg.mask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lg.sub * LPR));
+    const int64_t wpc = blockDim.x / 32;
+    lg.first = ((int64_t)blockIdx.x * wpc + (threadIdx.x / 32)) * (32 / LPR) + lg.sub;
+    lg.step = (int64_t)gridDim.x * wpc * (32 / LPR);
+
+    const bool b2 = p.base2 != 0;
+    const int N = p.N;
+    RowStep st;
+    st.set(lg.step, p.B, p.Hc);
+    RowCursor c;
+    c.set(lg.first, p.B, p.Hc);
+    const int64_t lane_off = (int64_t)lg.jl * VB;
+    for (int64_t row = lg.first; row < p.rows; row += lg.step, c.add(st.dg, st.db, st.dh, p.B, p.Hc)) {
+        const float* lrow = p.lse + c.g * p.l_sg + (int64_t)c.b * p.l_sb + (int64_t)c.h * p.l_sh;
+        const unsigned char* orow =
+            p.o + c.g * p.o_sg + (int64_t)c.b * p.o_sb + (int64_t)c.h * p.o_sh + lane_off;
+        unsigned char* urow = p.out + c.g * p.u_sg + (int64_t)c.b * p.u_sb + (int64_t)c.h * p.u_sh + lane_off;
+        const float l = lg.jl < N ? __ldg(lrow + (int64_t)lg.jl * p.l_sn) : -INFINITY;
+        unsigned long long w2[NR];
+        float Gl = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < VPL; c0 += VCH) {
+            V x[NR][VCH];
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+                if (j < N) {
+                    const unsigned char* rp = orow + (int64_t)j * p.o_sn;
+#pragma unroll
+                    for (int q = 0; q < VCH; ++q) x[j][q] = ld_stream<VB>(rp + (c0 + q) * LPR * VB);
+                }
+            if (c0 == 0) {
+                // the weights are reduced while the first loads are in flight
+                const float wl = group_weight(l, lg, LPR, b2, Gl);
+#pragma unroll
+                for (int j = 0; j < NR; ++j) {
+                    const float wj = __shfl_sync(lg.mask, wl, j & (LPR - 1), LPR);
+                    w2[j] = pack2f(wj, wj);
+                }
+            }
+            unsigned long long acc[VCH][NP];
+#pragma unroll
+            for (int q = 0; q < VCH; ++q)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) acc[q][i] = 0ull;
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+                if (j < N)
+#pragma unroll
+                    for (int q = 0; q < VCH; ++q) fma_pairs<T, VB, SAN>(acc[q], x[j][q], w2[j]);
+#pragma unroll
+            for (int q = 0; q < VCH; ++q) st_vec<VB>(urow + (c0 + q) * LPR * VB, round_pairs<T, VB>(acc[q]));
+        }
+        if (p.return_lse && lg.jl == 0)
+            p.out_lse[c.g * p.ul_sg + (int64_t)c.b * p.ul_sb + (int64_t)c.h * p.ul_sh] = Gl;
+    }
+}
+
+// Fixed-shape kernel for (T, VB, NR) and this row length, or nullptr.
+template <typename T, int VB, int NR, bool SAN>
+const void* pick_fixed(int row_bytes, int& lpr) {
+    if constexpr (VB < 4 || (VB == 4 && sizeof(T) == 4)) {
+        return nullptr;  // one element per vector: no pairs
+    } else {
+        if (row_bytes == 8 * VB && NR <= 8) { lpr = 8; return (const void*)combine_fixed_kernel<T, VB, NR, 8, 1, SAN>; }
+        if (row_bytes == 16 * VB) { lpr = 16; return (const void*)combine_fixed_kernel<T, VB, NR, 16, 1, SAN>; }
+        if (row_bytes == 32 * VB) { lpr = 32; return (const void*)combine_fixed_kernel<T, VB, NR, 32, 1, SAN>; }
+        if (row_bytes == 64 * VB) { lpr = 32; return (const void*)combine_fixed_kernel<T, VB, NR, 32, 2, SAN>; }
+        if (row_bytes == 128 * VB) { lpr = 32; return (const void*)combine_fixed_kernel<T, VB, NR, 32, 4, SAN>; }
+        if (row_bytes == 256 * VB) { lpr = 32; return (const void*)combine_fixed_kernel<T, VB, NR, 32, 8, SAN>; }
+        return nullptr;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Any N (> 32): weights recomputed per batch of 8 ranks from a serial reduction.
+// ---------------------------------------------------------------------------
 template <typename T, int VB>
 __global__ void __launch_bounds__(kThreads, 2) combine_kernel_any_n(const CombineParams p) {
     constexpr int EPV = VB / (int)sizeof(T);
@@ -225,52 +338,221 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel_any_n(const Combin
                 for (int j = 0; j < RC; ++j) {
                     if (r0 + j < N) {
                         x[j] = ld_stream<VB>(orow + (int64_t)(r0 + j) * p.o_sn + (int64_t)v * VB);
-                        wr[j] = finite_g
-                                    ? lse_exp(__ldg(lrow + (int64_t)(r0 + j) * p.l_sn) - m, b2) * inv_s
-                                    : 0.f;
+                        wr[j] = finite_g ? lse_exp(__ldg(lrow + (int64_t)(r0 + j) * p.l_sn) - m, b2) * inv_s
+                                         : 0.f;
                     }
                 }
 #pragma unroll
                 for (int j = 0; j < RC; ++j) {
                     if (r0 + j < N) {
-                        float f[EPV];
-                        unpack_vec<T, VB>(x[j], f);
-#pragma unroll
-                        for (int i = 0; i < EPV; ++i) {
-                            const float ov = (p.sanitize && !isfinite(f[i])) ? 0.f : f[i];
-                            acc[i] = fmaf(wr[j], ov, acc[i]);
-                        }
+                        if (p.sanitize) fma_vec<T, VB, true>(acc, x[j], wr[j]);
+                        else fma_vec<T, VB, false>(acc, x[j], wr[j]);
                     }
                 }
             }
-            st_vec<VB>(urow + (int64_t)v * VB, pack_vec<T, VB>(acc));
+            st_vec<VB>(urow + (int64_t)v * VB, round_vec<T, VB>(acc));
         }
         if (p.return_lse && lg.jl == 0) p.out_lse[g * p.ul_sg + b * p.ul_sb + h * p.ul_sh] = Gl;
     }
 }
 
-template <typename T, int VB>
+// ---------------------------------------------------------------------------
+// Staged variant: every lane copies its 16-byte slices of the next rows' rank
+// stack into shared memory with cp.async, DCP_STAGES rows deep, while it
+// merges the current row.  Nothing in flight occupies registers.  Each lane
+// reads back only the slices it copied itself, so its own cp.async.wait_group
+// is the only synchronisation needed (no barrier, no spin loop).  The LSE
+// words of a row are loaded (lane r: rank r) when the row is issued and
+// reduced with shuffles when it is merged.
+// ---------------------------------------------------------------------------
+constexpr int kStagedWarps = DCP_STAGED_WARPS;
+constexpr int kStages = DCP_STAGES;
+static_assert(kStages == 2 || kStages == 3, "pipeline depth is 2 or 3 rows");
+
+template <int NR, int VPL>
+constexpr size_t staged_smem_bytes() {
+    return (size_t)kStagedWarps * kStages * NR * VPL * 32 * 16;
+}
+
+template <typename T, int NR, int VPL, bool SAN>
+__global__ void __launch_bounds__(kStagedWarps * 32) combine_staged_kernel(const CombineParams p) {
+    constexpr int VPR = NR * VPL;  // 16-byte slices per lane per row
+    constexpr int EPV = 16 / (int)sizeof(T);
+    extern __shared__ uint4 smem[];
+    const int lane = threadIdx.x & 31;
+    uint4* wbuf = smem + (size_t)(threadIdx.x >> 5) * kStages * VPR * 32;
+
+    const LaneGroup lg = lane_group(p.lpr);
+    const int N = p.N;
+    const int nv = p.vec_per_row;
+    const int lpr = p.lpr;
+    const bool b2 = p.base2 != 0;
+    RowStep st;
+    st.set(lg.step, p.B, p.Hc);
+    RowCursor icur, ccur;  // rows being issued / merged
+    icur.set(lg.first, p.B, p.Hc);
+    ccur = icur;
+    int64_t irow = lg.first;
+    float lq[kStages];
+
+    // issue the row at icur into stage `slot` (one commit group per row, empty
+    // past the end so group counting stays uniform)
+    auto issue = [&](int slot, float& lslot) {
+        if (irow < p.rows) {
+            const unsigned char* orow =
+                p.o + icur.g * p.o_sg + (int64_t)icur.b * p.o_sb + (int64_t)icur.h * p.o_sh;
+            uint4* sb = wbuf + slot * VPR * 32 + lane;
+#pragma unroll
+            for (int j = 0; j < NR; ++j) {
+                if (j < N) {
+#pragma unroll
+                    for (int q = 0; q < VPL; ++q) {
+                        const int v = lg.jl + q * lpr;
+                        if (v < nv)
+                            cp_async_16(sb + (j * VPL + q) * 32, orow + (int64_t)j * p.o_sn + (int64_t)v * 16);
+                    }
+                }
+            }
+            const float* lrow =
+                p.lse + icur.g * p.l_sg + (int64_t)icur.b * p.l_sb + (int64_t)icur.h * p.l_sh;
+            lslot = lg.jl < N ? __ldg(lrow + (int64_t)lg.jl * p.l_sn) : -INFINITY;
+        }
+        cp_async_commit();
+        irow += lg.step;
+        icur.add(st.dg, st.db, st.dh, p.B, p.Hc);
+    };
+
+    // merge the row at ccur from stage `slot`
+    auto merge = [&](int slot, float l) {
+        float Gl;
+        const float wl = group_weight(l, lg, lpr, b2, Gl);
+        float w[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) w[r] = __shfl_sync(lg.mask, wl, r & (lpr - 1), lpr);
+        const uint4* sb = wbuf + slot * VPR * 32 + lane;
+        unsigned char* urow = p.out + ccur.g * p.u_sg + (int64_t)ccur.b * p.u_sb + (int64_t)ccur.h * p.u_sh;
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+            const int v = lg.jl + q * lpr;
+            if (v < nv) {
+                float acc[EPV];
+#pragma unroll
+                for (int i = 0; i < EPV; ++i) acc[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < NR; ++j)
+                    if (j < N) fma_vec<T, 16, SAN>(acc, sb[(j * VPL + q) * 32], w[j]);
+                st_vec<16>(urow + (int64_t)v * 16, round_vec<T, 16>(acc));
+            }
+        }
+        if (p.return_lse && lg.jl == 0)
+            p.out_lse[ccur.g * p.ul_sg + (int64_t)ccur.b * p.ul_sb + (int64_t)ccur.h * p.ul_sh] = Gl;
+        ccur.add(st.dg, st.db, st.dh, p.B, p.Hc);
+    };
+
+    if constexpr (kStages == 3) {
+        issue(0, lq[0]);
+        issue(1, lq[1]);
+        for (int64_t row = lg.first; row < p.rows;) {
+            issue(2, lq[2]);
+            cp_async_wait<2>();
+            merge(0, lq[0]);
+            row += lg.step;
+            if (row >= p.rows) break;
+            issue(0, lq[0]);
+            cp_async_wait<2>();
+            merge(1, lq[1]);
+            row += lg.step;
+            if (row >= p.rows) break;
+            issue(1, lq[1]);
+            cp_async_wait<2>();
+            merge(2, lq[2]);
+            row += lg.step;
+        }
+    } else {
+        issue(0, lq[0]);
+        for (int64_t row = lg.first; row < p.rows;) {
+            issue(1, lq[1]);
+            cp_async_wait<1>();
+            merge(0, lq[0]);
+            row += lg.step;
+            if (row >= p.rows) break;
+            issue(0, lq[0]);
+            cp_async_wait<1>();
+            merge(1, lq[1]);
+            row += lg.step;
+        }
+    }
+    cp_async_wait<0>();
+}
+
+template <typename T, int NR, bool SAN>
+const void* pick_staged(int vpl, size_t& smem) {
+    if (vpl <= 1) {
+        smem = staged_smem_bytes<NR, 1>();
+        return (const void*)combine_staged_kernel<T, NR, 1, SAN>;
+    }
+    smem = staged_smem_bytes<NR, 2>();
+    return (const void*)combine_staged_kernel<T, NR, 2, SAN>;
+}
+
+template <typename T, int VB, bool SAN>
 cudaError_t launch_combine_vb(const CombineParams& p, cudaStream_t stream) {
-    const void* k;
-    if (p.N <= 2) k = (const void*)combine_kernel<T, VB, 2>;
-    else if (p.N <= 4) k = (const void*)combine_kernel<T, VB, 4>;
-    else if (p.N <= 8) k = (const void*)combine_kernel<T, VB, 8>;
-    else if (p.N <= 16) k = (const void*)combine_kernel<T, VB, 16>;
-    else if (p.N <= 32) k = (const void*)combine_kernel<T, VB, 32>;
-    else k = (const void*)combine_kernel_any_n<T, VB>;
-    const int rows_per_cta = (kThreads / 32) * (32 / p.lpr);
-    const int grid = persistent_grid(k, p.rows, rows_per_cta);
     void* args[] = {(void*)&p};
-    cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, stream);
-    return cudaGetLastError();
+#if DCP_COMBINE_FIXED
+    if (p.N <= 8) {
+        int lpr = 0;
+        const int rb = p.vec_per_row * VB;
+        const void* k = p.N <= 2 ? pick_fixed<T, VB, 2, SAN>(rb, lpr)
+                      : p.N <= 4 ? pick_fixed<T, VB, 4, SAN>(rb, lpr)
+                                 : pick_fixed<T, VB, 8, SAN>(rb, lpr);
+        if (k && p.N <= lpr) {
+            CombineParams q = p;
+            q.lpr = lpr;
+            void* qargs[] = {(void*)&q};
+            const int grid = persistent_grid(k, p.rows, (kThreads / 32) * (32 / lpr), kThreads, 0);
+            return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), qargs, 0, stream);
+        }
+    }
+#endif
+    const int rows_per_warp = 32 / p.lpr;
+    if constexpr (VB == 16 && DCP_COMBINE_STAGED) {
+        // staged when a lane's row holds <= 16 slices (<= 96 KiB of shared memory
+        // per CTA at 3 stages); longer rows keep enough bytes in flight from
+        // registers alone
+        const int vpl = (p.vec_per_row + p.lpr - 1) / p.lpr;
+        const int nr = p.N <= 2 ? 2 : p.N <= 4 ? 4 : 8;
+        if (p.N <= 8 && vpl <= 2 && nr * vpl <= 16) {
+            size_t smem = 0;
+            const void* k = p.N <= 2 ? pick_staged<T, 2, SAN>(vpl, smem)
+                          : p.N <= 4 ? pick_staged<T, 4, SAN>(vpl, smem)
+                                     : pick_staged<T, 8, SAN>(vpl, smem);
+            const int threads = kStagedWarps * 32;
+            const int grid = persistent_grid(k, p.rows, kStagedWarps * rows_per_warp, threads, smem);
+            return cudaLaunchKernel(k, dim3(grid), dim3(threads), args, smem, stream);
+        }
+    }
+    const void* k;
+    if (p.N <= 2) k = (const void*)combine_kernel<T, VB, 2, SAN>;
+    else if (p.N <= 4) k = (const void*)combine_kernel<T, VB, 4, SAN>;
+    else if (p.N <= 8) k = (const void*)combine_kernel<T, VB, 8, SAN>;
+    else if (p.N <= 16) k = (const void*)combine_kernel<T, VB, 16, SAN>;
+    else if (p.N <= 32) k = (const void*)combine_kernel<T, VB, 32, SAN>;
+    else k = (const void*)combine_kernel_any_n<T, VB>;
+    const int grid = persistent_grid(k, p.rows, (kThreads / 32) * rows_per_warp, kThreads, 0);
+    return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, stream);
+}
+
+template <typename T, int VB>
+cudaError_t launch_combine_san(const CombineParams& p, cudaStream_t stream) {
+    return p.sanitize ? launch_combine_vb<T, VB, true>(p, stream) : launch_combine_vb<T, VB, false>(p, stream);
 }
 
 template <typename T>
 cudaError_t launch_combine_t(const CombineParams& p, int vb, cudaStream_t stream) {
-    if (vb == 16) return launch_combine_vb<T, 16>(p, stream);
-    if (vb == 4) return launch_combine_vb<T, 4>(p, stream);
+    if (vb == 16) return launch_combine_san<T, 16>(p, stream);
+    if (vb == 4) return launch_combine_san<T, 4>(p, stream);
     if constexpr (sizeof(T) == 2) {
-        if (vb == 2) return launch_combine_vb<T, 2>(p, stream);
+        if (vb == 2) return launch_combine_san<T, 2>(p, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -69,6 +69,182 @@ __device__ __forceinline__ typename VecT<VB>::type pack_vec(const float (&f)[VB 
     return v;
 }
 
+// ---- paired fp32 arithmetic (sm_100+ fma.rn.f32x2: two IEEE fp32 FMAs,
+// each rounded to nearest, in one instruction) ---------------------------------
+__device__ __forceinline__ float2 ffma2(float w, float2 x, float2 acc) {
+    float2 d;
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %2};\n\t"
+        "mov.b64 b, {%3, %4};\n\t"
+        "mov.b64 c, {%5, %6};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(w), "f"(x.x), "f"(x.y), "f"(acc.x), "f"(acc.y));
+    return d;
+}
+
+__device__ __forceinline__ unsigned f32_to_pair(float2 f, __nv_bfloat16);
+__device__ __forceinline__ unsigned f32_to_pair(float2 f, __half);
+
+// fp32 pairs held in one 64-bit register (low half = first element), so the
+// paired FMA needs no repacking between iterations.
+__device__ __forceinline__ unsigned long long pack2(unsigned lo, unsigned hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ unsigned long long pack2f(float lo, float hi) {
+    return pack2(__float_as_uint(lo), __float_as_uint(hi));
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long r) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+// acc += w2 * x2, element-wise on two fp32 lanes (each an IEEE FMA, round to nearest)
+__device__ __forceinline__ void ffma2_acc(unsigned long long& acc, unsigned long long w2,
+                                          unsigned long long x2) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w2), "l"(x2));
+}
+
+// One 32-bit word of payload -> its fp32 pair.  bf16 widens by placing the
+// 16 bits in the upper half of an fp32; fp16 goes through the half2 convert.
+template <typename T>
+__device__ __forceinline__ unsigned long long word_to_pair(unsigned w);
+template <>
+__device__ __forceinline__ unsigned long long word_to_pair<__nv_bfloat16>(unsigned w) {
+    return pack2(w << 16, w & 0xffff0000u);
+}
+template <>
+__device__ __forceinline__ unsigned long long word_to_pair<__half>(unsigned w) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    const float2 f = __half22float2(h);
+    return pack2f(f.x, f.y);
+}
+__device__ __forceinline__ unsigned long long sanitize_pair(unsigned long long x2) {
+    float2 f = unpack2(x2);
+    f.x = isfinite(f.x) ? f.x : 0.f;
+    f.y = isfinite(f.y) ? f.y : 0.f;
+    return pack2f(f.x, f.y);
+}
+
+// acc[0..NP) += w2 * (payload vector x) for a VB-byte vector of T holding
+// 2*NP elements (VB = 16, or VB = 4 with a 16-bit T).
+template <typename T, int VB, bool SAN>
+__device__ __forceinline__ void fma_pairs(unsigned long long (&acc)[VB / sizeof(T) / 2],
+                                          const typename VecT<VB>::type& x, unsigned long long w2) {
+    constexpr int NP = VB / (int)sizeof(T) / 2;
+    unsigned wd[VB / 4];
+    memcpy(wd, &x, VB);
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        unsigned long long x2;
+        if constexpr (sizeof(T) == 4) x2 = pack2(wd[2 * k], wd[2 * k + 1]);
+        else x2 = word_to_pair<T>(wd[k]);
+        if (SAN) x2 = sanitize_pair(x2);
+        ffma2_acc(acc[k], w2, x2);
+    }
+}
+
+// Round NP fp32 pairs into one payload vector (round to nearest even).
+template <typename T, int VB>
+__device__ __forceinline__ typename VecT<VB>::type round_pairs(const unsigned long long (&acc)[VB / sizeof(T) / 2]) {
+    constexpr int NP = VB / (int)sizeof(T) / 2;
+    typename VecT<VB>::type v;
+    if constexpr (sizeof(T) == 4) {
+        memcpy(&v, acc, VB);
+    } else {
+        unsigned wd[VB / 4];
+#pragma unroll
+        for (int k = 0; k < NP; ++k) wd[k] = f32_to_pair(unpack2(acc[k]), T());
+        memcpy(&v, wd, VB);
+    }
+    return v;
+}
+
+// Two packed 16-bit payload elements (low half first) -> two floats.
+__device__ __forceinline__ float2 pair_to_f32(unsigned w, __nv_bfloat16) {
+    // a bf16 is the upper half of the fp32 with the same bits
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ float2 pair_to_f32(unsigned w, __half) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __half22float2(h);
+}
+// Two floats -> two packed 16-bit payload elements (round to nearest even).
+__device__ __forceinline__ unsigned f32_to_pair(float2 f, __nv_bfloat16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+    unsigned w;
+    memcpy(&w, &h, 4);
+    return w;
+}
+__device__ __forceinline__ unsigned f32_to_pair(float2 f, __half) {
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    unsigned w;
+    memcpy(&w, &h, 4);
+    return w;
+}
+
+__device__ __forceinline__ float zero_if_not_finite(float x) { return isfinite(x) ? x : 0.f; }
+
+// acc[0..EPV) += w * (payload vector x), EPV = VB / sizeof(T) elements; with
+// SAN, NaN/+-inf payload elements count as 0.
+template <typename T, int VB, bool SAN>
+__device__ __forceinline__ void fma_vec(float (&acc)[VB / sizeof(T)], const typename VecT<VB>::type& x,
+                                        float w) {
+    constexpr int EPV = VB / (int)sizeof(T);
+    if constexpr (sizeof(T) == 4) {
+        float f[EPV];
+        memcpy(f, &x, VB);
+#pragma unroll
+        for (int i = 0; i + 1 < EPV; i += 2) {
+            float2 xf = make_float2(f[i], f[i + 1]);
+            if (SAN) xf = make_float2(zero_if_not_finite(xf.x), zero_if_not_finite(xf.y));
+            const float2 r = ffma2(w, xf, make_float2(acc[i], acc[i + 1]));
+            acc[i] = r.x;
+            acc[i + 1] = r.y;
+        }
+        if constexpr (EPV % 2) acc[EPV - 1] = fmaf(w, SAN ? zero_if_not_finite(f[EPV - 1]) : f[EPV - 1], acc[EPV - 1]);
+    } else if constexpr (VB >= 4) {
+        unsigned wd[VB / 4];
+        memcpy(wd, &x, VB);
+#pragma unroll
+        for (int k = 0; k < VB / 4; ++k) {
+            float2 xf = pair_to_f32(wd[k], T());
+            if (SAN) xf = make_float2(zero_if_not_finite(xf.x), zero_if_not_finite(xf.y));
+            const float2 r = ffma2(w, xf, make_float2(acc[2 * k], acc[2 * k + 1]));
+            acc[2 * k] = r.x;
+            acc[2 * k + 1] = r.y;
+        }
+    } else {
+        T e;
+        memcpy(&e, &x, 2);
+        const float f = to_f32(e);
+        acc[0] = fmaf(w, SAN ? zero_if_not_finite(f) : f, acc[0]);
+    }
+}
+
+// Round EPV accumulators into one payload vector.
+template <typename T, int VB>
+__device__ __forceinline__ typename VecT<VB>::type round_vec(const float (&acc)[VB / sizeof(T)]) {
+    typename VecT<VB>::type v;
+    if constexpr (sizeof(T) == 4) {
+        memcpy(&v, acc, VB);
+    } else if constexpr (VB >= 4) {
+        unsigned wd[VB / 4];
+#pragma unroll
+        for (int k = 0; k < VB / 4; ++k) wd[k] = f32_to_pair(make_float2(acc[2 * k], acc[2 * k + 1]), T());
+        memcpy(&v, wd, VB);
+    } else {
+        const T e = from_f32<T>(acc[0]);
+        memcpy(&v, &e, 2);
+    }
+    return v;
+}
+
 // Lanes of a warp are split into groups of `lpr` consecutive lanes (a power of
 // two <= 32); each group owns one row at a time.
 struct LaneGroup {
@@ -93,11 +269,59 @@ __device__ __forceinline__ LaneGroup lane_group(int lpr) {
     return lg;
 }
 
+// (g, b, h) of row index r = (g * B + b) * H + h, advanced by a fixed number
+// of rows without any division (the step is decomposed once per thread).
+struct RowCursor {
+    int64_t g;
+    int b, h;
+    __device__ __forceinline__ void set(int64_t r, int B, int H) {
+        h = (int)(r % H);
+        const int64_t t = r / H;
+        b = (int)(t % B);
+        g = t / B;
+    }
+    // add (dg, db, dh) with carries; requires db < B and dh < H
+    __device__ __forceinline__ void add(int64_t dg, int db, int dh, int B, int H) {
+        h += dh;
+        int c = h >= H;
+        if (c) h -= H;
+        b += db + c;
+        c = b >= B;
+        if (c) b -= B;
+        g += dg + c;
+    }
+    __device__ __forceinline__ void next(int B, int H) { add(0, 0, 1, B, H); }
+};
+
+struct RowStep {
+    int64_t dg;
+    int db, dh;
+    __device__ __forceinline__ void set(int64_t step, int B, int H) {
+        dh = (int)(step % H);
+        const int64_t t = step / H;
+        db = (int)(t % B);
+        dg = t / B;
+    }
+};
+
+// cp.async (LDGSTS): 16-byte global -> shared copies that bypass L1 and hold
+// no registers while in flight; completion is tracked per thread in groups.
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // Grid for a grid-stride kernel: enough CTAs for every row, capped at the
 // number that are resident at once (SM count x CTAs per SM), so large inputs
 // run as one full wave of persistent CTAs.
-inline int persistent_grid(const void* kernel, int64_t rows, int rows_per_cta) {
-    const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(kernel);
+inline int persistent_grid(const void* kernel, int64_t rows, int rows_per_cta, int threads,
+                           size_t smem) {
+    const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(kernel, threads, smem);
     int64_t need = (rows + rows_per_cta - 1) / rows_per_cta;
     if (need < 1) need = 1;
     return (int)(need < cap ? need : cap);

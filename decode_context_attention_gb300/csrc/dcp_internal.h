@@ -57,7 +57,8 @@ cudaError_t launch_combine_bf16(const CombineParams& p, int vb, cudaStream_t str
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
-// Resident CTAs per SM of `kernel` at kThreads threads (cached per device and kernel).
-int ctas_per_sm(const void* kernel);
+// Resident CTAs per SM of `kernel` at `threads` threads and `smem` bytes of
+// dynamic shared memory (cached per device, kernel and shared-memory size).
+int ctas_per_sm(const void* kernel, int threads, size_t smem);
 
 }  // namespace dcp
