@@ -241,7 +241,7 @@ def csrc_digest() -> str:
 def ncu_traffic(kernel: str):
     """dram read+write bytes per launch from the committed ncu summary, if it was
     taken on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -286,13 +286,15 @@ def setup_mla_decode(device, seed_offset=0):
     }
 
 
-def setup_cached_extend(device):
+def setup_cached_extend(device, tokens=None):
     import torch
 
     from decode_context_attention_gb300 import binding
-    from decode_context_attention_gb300.workloads import WORKLOADS, generate
+    from decode_context_attention_gb300.workloads import WORKLOADS, generate, scaled
 
     w = WORKLOADS["cached_extend"]
+    if tokens:
+        w = scaled(w, B=tokens)
     d = generate(w, device)
     o, lse = d["o"], d["lse"]
     N, T, H, D = o.shape
@@ -402,6 +404,16 @@ def run_gpu(args):
     flush = L2Flush(device)
     clocks = ClockSampler(local)
     clocks.start()
+
+    if args.only:
+        # a short run of one workload (for profiler captures); prints nothing
+        wl = {"mla_decode": lambda: setup_mla_decode(device),
+              "sweep": lambda: setup_sweep_max(device),
+              "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens)}[args.only]()
+        time_sequence(wl["launches"], args.steps, args.warmup,
+                      None if args.only == "cached_extend" else flush, device)
+        clocks.stop()
+        return
 
     # --- headline: MLA decode merge, pack + combine, all 8 ranks ----------------
     mla = setup_mla_decode(device, seed_offset=rank)
@@ -575,6 +587,10 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["mla_decode", "sweep", "cached_extend"],
+                    help="run just this workload's launches (profiling); no JSON line")
+    ap.add_argument("--ext-tokens", type=int, default=None,
+                    help="tokens of the cached-extend workload under --only (default 16384)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -9,8 +9,8 @@
 //
 // Design: HBM copy.  A group of `lpr` lanes owns a batch of RB consecutive
 // source rows (consecutive heads of one token and peer) and issues the loads
-// of the whole batch before any store, so each warp keeps 8 vectors per lane
-// (4 KiB with 16-byte vectors) in flight.
+// of the whole batch before any store, so each warp keeps 4 KiB in flight
+// (8 vectors per lane of 16 bytes, or 32 of 4 bytes).
 // Vectors are as wide as every source and destination row start allows
 // (16 B for the peer-inside layout and contiguous sources; 4 B for the
 // interleaved rows, whose starts advance by D*e + 4 bytes).  Row indices are
@@ -23,12 +23,15 @@ namespace dcp {
 // LINEAR: the host guarantees that H_pr is a multiple of RB, so the RB rows of
 // a batch share (g, b, peer) and step by one head: their addresses are one
 // base plus k times the head stride.  Otherwise a batch is a single row.
-template <int VB, int VPL, bool LINEAR>
+// LPR > 0 fixes the lanes per row at compile time (rows of >= 2 vectors per
+// lane always use whole warps), making every vector offset an immediate.
+template <int VB, int VPL, bool LINEAR, int LPR>
 __global__ void __launch_bounds__(kThreads) pack_kernel(const PackParams p) {
-    constexpr int MAXV = 8;  // vectors held per lane per batch
+    constexpr int MAXV = VB == 16 ? 8 : 32;  // vectors held per lane per batch (<= 32 registers)
     constexpr int RB = LINEAR ? (MAXV / VPL > 0 ? MAXV / VPL : 1) : 1;  // rows per batch
     using V = typename VecT<VB>::type;
-    const LaneGroup lg = lane_group(p.lpr);
+    const int lpr = LPR > 0 ? LPR : p.lpr;
+    const LaneGroup lg = lane_group(lpr);
     const int nv = p.row_bytes / VB;
     const int64_t nbatch = (p.rows + RB - 1) / RB;
     RowCursor cur;
@@ -42,20 +45,20 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const PackParams p) {
         unsigned char* dst = p.dst_o + cur.g * p.do_sg + (int64_t)peer * p.do_sn +
                              (int64_t)cur.b * p.do_sb + (int64_t)hl * p.do_sh;
         if (p.copy_payload) {
-            for (int v0 = lg.jl; v0 < nv; v0 += p.lpr * VPL) {
+            for (int v0 = lg.jl; v0 < nv; v0 += lpr * VPL) {
                 V x[RB][VPL];
 #pragma unroll
                 for (int k = 0; k < RB; ++k)
 #pragma unroll
                     for (int j = 0; j < VPL; ++j) {
-                        const int v = v0 + j * p.lpr;
+                        const int v = v0 + j * lpr;
                         if (v < nv) x[k][j] = ld_stream<VB>(src + k * p.o_sh + (int64_t)v * VB);
                     }
 #pragma unroll
                 for (int k = 0; k < RB; ++k)
 #pragma unroll
                     for (int j = 0; j < VPL; ++j) {
-                        const int v = v0 + j * p.lpr;
+                        const int v = v0 + j * lpr;
                         if (v < nv) st_vec<VB>(dst + k * p.do_sh + (int64_t)v * VB, x[k][j]);
                     }
             }
@@ -74,10 +77,10 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const PackParams p) {
 
 template <int VB, bool LINEAR>
 static const void* pick_pack(int vpl) {
-    if (vpl <= 1) return (const void*)pack_kernel<VB, 1, LINEAR>;
-    if (vpl <= 2) return (const void*)pack_kernel<VB, 2, LINEAR>;
-    if (vpl <= 4) return (const void*)pack_kernel<VB, 4, LINEAR>;
-    return (const void*)pack_kernel<VB, 8, LINEAR>;
+    if (vpl <= 1) return (const void*)pack_kernel<VB, 1, LINEAR, 0>;
+    if (vpl <= 2) return (const void*)pack_kernel<VB, 2, LINEAR, 32>;
+    if (vpl <= 4) return (const void*)pack_kernel<VB, 4, LINEAR, 32>;
+    return (const void*)pack_kernel<VB, 8, LINEAR, 32>;
 }
 
 template <int VB>
@@ -89,7 +92,7 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
     const int nv = p.row_bytes / p.vb;
     const int vpl_need = (nv + p.lpr - 1) / p.lpr;
     const int vpl = vpl_need <= 1 ? 1 : vpl_need <= 2 ? 2 : vpl_need <= 4 ? 4 : 8;
-    const int rb_linear = 8 / vpl;
+    const int rb_linear = (p.vb == 16 ? 8 : 32) / vpl;
     const bool linear = p.H_pr % rb_linear == 0 && rb_linear <= p.lpr;
     const int rb = linear ? rb_linear : 1;
     const void* k;
