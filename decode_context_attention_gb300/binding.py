@@ -9,7 +9,9 @@ computed by the CUDA kernels behind the C ABI:
   addresses, sizes, element strides, a cudaStream_t handle).
 * ``pack_send`` / ``lse_combine`` / ``unpack_combine``: the same calls taking
   torch CUDA tensors (views allowed); strides are read from the tensors and the
-  kernels run on the current torch stream unless one is given.
+  kernels run on the current torch stream unless one is given.  Pinned host
+  tensors are accepted too: the kernels then stream them over the host link
+  (a pack that reads host inputs fuses the upload into the pack).
 
 There is no fallback: if the library is missing or a call fails, an exception
 is raised.
@@ -128,9 +130,12 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def _need_cuda(*ts):
+    """Operands must be reachable by the kernels: CUDA tensors, or page-locked
+    (pinned) host tensors, which the kernels read and write in place over the
+    host link.  Ordinary host tensors are refused (there is no CPU fallback)."""
     for t in ts:
-        if t is not None and not t.is_cuda:
-            raise ValueError("DCP kernels take CUDA tensors (no CPU fallback)")
+        if t is not None and not (t.is_cuda or t.is_pinned()):
+            raise ValueError("DCP kernels take CUDA tensors or pinned host tensors (no CPU fallback)")
 
 
 def _lead(t: torch.Tensor, nd: int) -> torch.Tensor:

@@ -316,15 +316,23 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Grid for a grid-stride kernel: enough CTAs for every row, capped at the
-// number that are resident at once (SM count x CTAs per SM), so large inputs
-// run as one full wave of persistent CTAs.
+// Grid for a grid-stride kernel.  persistent: enough CTAs for every row,
+// capped at the number resident at once (SM count x CTAs per SM), so large
+// inputs run as one full wave of persistent CTAs.  Otherwise one work item per
+// lane group: CTAs retire and are replaced at staggered times, which measured
+// faster for the pure-copy pack.
+inline int grid_for(const void* kernel, int64_t items, int items_per_cta, int threads, size_t smem,
+                    bool persistent) {
+    int64_t need = (items + items_per_cta - 1) / items_per_cta;
+    if (need < 1) need = 1;
+    if (need > 0x7fffffffll) need = 0x7fffffffll;
+    if (!persistent) return (int)need;
+    const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(kernel, threads, smem);
+    return (int)(need < cap ? need : cap);
+}
 inline int persistent_grid(const void* kernel, int64_t rows, int rows_per_cta, int threads,
                            size_t smem) {
-    const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(kernel, threads, smem);
-    int64_t need = (rows + rows_per_cta - 1) / rows_per_cta;
-    if (need < 1) need = 1;
-    return (int)(need < cap ? need : cap);
+    return grid_for(kernel, rows, rows_per_cta, threads, smem, true);
 }
 
 }  // namespace dcp

@@ -102,7 +102,7 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
     else return cudaErrorInvalidValue;
     const int batches_per_cta = (kThreads / 32) * (32 / p.lpr);
     const int64_t nbatch = (p.rows + rb - 1) / rb;
-    const int grid = persistent_grid(k, nbatch, batches_per_cta, kThreads, 0);
+    const int grid = grid_for(k, nbatch, batches_per_cta, kThreads, 0, false);
     void* args[] = {(void*)&p};
     return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, stream);
 }

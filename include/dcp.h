@@ -20,8 +20,10 @@
  *
  * Conventions for every entry point
  * ---------------------------------
- * - Pointers are DEVICE pointers on the current CUDA device.  The caller owns
- *   every buffer.  The library allocates nothing, frees nothing, never
+ * - Pointers are addresses the current CUDA device can dereference: device
+ *   memory, or page-locked host memory mapped at the same address (pinned
+ *   allocations under unified addressing), which the kernels then read or
+ *   write directly over the host link.  The caller owns every buffer.  The library allocates nothing, frees nothing, never
  *   synchronises, and enqueues its kernels on `stream` (a cudaStream_t; NULL
  *   means the legacy default stream).  Work is asynchronous: results are
  *   valid once the stream reaches that point.

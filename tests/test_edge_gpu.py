@@ -251,3 +251,32 @@ def test_errors_raise_through_the_binding():
     with pytest.raises(binding.DcpError):
         x = torch.randn((1, 2, 2, 2, 8), device=DEV)
         binding.lse_combine(x, torch.zeros((1, 2, 2, 2), device=DEV), x[:, 0])  # alias, no flag
+
+
+def test_pinned_host_operands_match_device_operands():
+    """Pinned host tensors as operands: the pack reads its inputs and the combine
+    writes its result over the host link; the bytes equal the device path's."""
+    N, B, H, D = 4, 6, 16, 128
+    H_pr = H // N
+    g = torch.Generator(device=DEV).manual_seed(9)
+    o = torch.randn((N, B, H, D), generator=g, device=DEV).to(torch.bfloat16)
+    lse = torch.empty((N, B, H), device=DEV).uniform_(0, 12, generator=g)
+    po, st = layouts.alloc_peer_inside(N, B, H_pr, N, D, torch.bfloat16, DEV)
+    po2, st2 = layouts.alloc_peer_inside(N, B, H_pr, N, D, torch.bfloat16, DEV)
+    binding.pack_send(o, lse, *layouts.peer_inside_send_views(po, st))
+    binding.pack_send(o.cpu().pin_memory(), lse.cpu().pin_memory(), *layouts.peer_inside_send_views(po2, st2))
+    torch.cuda.synchronize()
+    assert torch.equal(po.view(torch.int16), po2.view(torch.int16))
+    assert torch.equal(st[..., 0], st2[..., 0])
+    out = torch.empty((N, B, H_pr, D), dtype=torch.bfloat16, device=DEV)
+    out_lse = torch.empty((N, B, H_pr), device=DEV)
+    out_h = torch.empty((N, B, H_pr, D), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((N, B, H_pr)).pin_memory()
+    ro, rl = layouts.exchange_peer_inside(po, st)
+    binding.lse_combine(ro, rl, out, out_lse)
+    binding.lse_combine(ro, rl, out_h, lse_h)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu().view(torch.int16), out_h.view(torch.int16))
+    assert torch.equal(out_lse.cpu(), lse_h)
+    with pytest.raises(ValueError):
+        binding.lse_combine(ro, rl, torch.empty((N, B, H_pr, D), dtype=torch.bfloat16), None)
