@@ -207,3 +207,36 @@ def test_cached_extend_small_all_rows():
 def test_cached_extend_full_size_sampled():
     """16384 x 96 x 512 fp32 per rank, 8 ranks (24 GiB), the launch the benchmark times."""
     run_inplace(WORKLOADS["cached_extend"], sample=4096)
+
+
+def test_cached_extend_contiguous_head_slices_in_one_launch():
+    """The ag_rs merge's per-rank head slices (rank k keeps heads [k*H/N, (k+1)*H/N),
+    made contiguous) produced directly by the combine's store: the group axis
+    walks the slices, so one launch writes out[k] = merged heads of slice k as a
+    contiguous [T, H/N, D] block.  Compared with the oracle and, bit for bit,
+    with the slices of the in-place result."""
+    w = scaled(WORKLOADS["cached_extend"], B=40, seed=43)
+    d = generate(w, DEV)
+    o, lse = d["o"], d["lse"]                     # [N, T, H, D], [N, T, H]
+    N, T, H, D = o.shape
+    hs = H // N
+    o_np, l_np = to_np(o), to_np(lse)
+    o_k = o.view(N, T, N, hs, D).permute(2, 0, 1, 3, 4)     # [slice k][rank][T][hs][D]
+    l_k = lse.view(N, T, N, hs).permute(2, 0, 1, 3)
+    slices = torch.empty((N, T, hs, D), dtype=o.dtype, device=DEV)
+    slices_lse = torch.empty((N, T, hs), dtype=torch.float32, device=DEV)
+    binding.lse_combine(o_k, l_k, slices, slices_lse, base=w.base, sanitize=True)
+    want, want_lse = oracle.combine("f32", o_np[None], l_np[None], base=w.base, sanitize=True)
+    torch.cuda.synchronize()
+    want_k = want[0].reshape(T, N, hs, D).transpose(1, 0, 2, 3)
+    want_lk = want_lse[0].reshape(T, N, hs).transpose(1, 0, 2)
+    assert_merge_close(slices, want_k, "contiguous slices")
+    assert_lse_close(slices_lse, want_lk, "contiguous slice lse")
+    # the in-place merge, sliced afterwards, holds the same bytes
+    out_lse = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    binding.lse_combine(o, lse, o[0], out_lse, base=w.base, sanitize=True, inplace=True)
+    torch.cuda.synchronize()
+    for k in range(N):
+        assert torch.equal(slices[k].view(torch.int32), o[0][:, k * hs:(k + 1) * hs].contiguous().view(torch.int32))
+        assert torch.equal(slices_lse[k].view(torch.int32),
+                           out_lse[:, k * hs:(k + 1) * hs].contiguous().view(torch.int32))
