@@ -36,7 +36,8 @@ STATUS_NAMES = {0: "DCP_OK", 1: "DCP_ERR_INVALID_ARG", 2: "DCP_ERR_UNSUPPORTED_D
                 6: "DCP_ERR_CUDA"}
 # Every symbol include/dcp.h declares.
 EXPORTS = ("dcp_lse_pack_dim", "dcp_status_string", "dcp_last_error_message", "dcp_pack_send",
-           "dcp_lse_combine", "dcp_unpack_combine")
+           "dcp_lse_combine", "dcp_unpack_combine", "dcp_decode_attention_workspace_size",
+           "dcp_decode_attention")
 
 
 class DcpError(RuntimeError):
@@ -76,6 +77,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                         + [vp, i64, i64, i64, i64] + merge_tail)
         lib.dcp_unpack_combine.restype = i32
         lib.dcp_unpack_combine.argtypes = [i32] * 6 + [vp, i64, i64, i64, i64] + merge_tail
+        lib.dcp_decode_attention_workspace_size.restype = ctypes.c_size_t
+        lib.dcp_decode_attention_workspace_size.argtypes = [i32] * 6
+        lib.dcp_decode_attention.restype = i32
+        lib.dcp_decode_attention.argtypes = ([i32] * 6 + [vp, i64, i64] + [vp, i64, i64, i64, i64]
+                                             + [vp, i64, i64, i64, i64] + [vp, i32, ctypes.c_float, i32]
+                                             + [vp, i64, i64, i64] + [vp, i64, i64, i64]
+                                             + [i32, vp, ctypes.c_size_t, vp])
         _lib = lib
         return lib
 
@@ -106,6 +114,15 @@ def dcp_lse_combine(*args) -> int:
 
 def dcp_unpack_combine(*args) -> int:
     return load().dcp_unpack_combine(*args)
+
+
+def dcp_decode_attention_workspace_size(N: int, B: int, H: int, D: int, max_seq_len: int,
+                                        split_tokens: int) -> int:
+    return load().dcp_decode_attention_workspace_size(N, B, H, D, max_seq_len, split_tokens)
+
+
+def dcp_decode_attention(*args) -> int:
+    return load().dcp_decode_attention(*args)
 
 
 def check(status: int, where: str) -> None:
@@ -248,3 +265,43 @@ def lse_combine(o, lse, out, out_lse=None, base="e", sanitize=False, inplace=Fal
 
 def unpack_combine(recv, D, out, out_lse=None, base="e", sanitize=False, stream=None) -> None:
     prepare_unpack_combine(recv, D, out, out_lse, base, sanitize, stream)()
+
+
+def prepare_decode_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                             max_seq_len: int, o: torch.Tensor, lse: torch.Tensor, sm_scale: float,
+                             base: str = "e", split_tokens: int = 1024,
+                             workspace: torch.Tensor | None = None, stream=None) -> _Prepared:
+    """Each rank's decode attention over its round-robin share of the KV cache.
+
+    q [B,H,D]; k, v [N,B,Lc,Hkv,D] local caches (token i of rank r = global
+    token i*N + r); seq_lens [B] int32 global lengths; o [N,B,H,D], lse [N,B,H].
+    `workspace` (uint8, device) is needed when the local lengths span more than
+    one split; see workspace_bytes()."""
+    _need_cuda(q, k, v, seq_lens, o, lse, workspace)
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    for t in (q, k, v, o):
+        _inner_ok(t)
+    B, H, D = q.shape
+    N, _, _, Hkv, _ = k.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = (_dtype_code(q), N, B, H, Hkv, D,
+            q.data_ptr(), q.stride(0), q.stride(1),
+            k.data_ptr(), k.stride(0), k.stride(1), k.stride(2), k.stride(3),
+            v.data_ptr(), v.stride(0), v.stride(1), v.stride(2), v.stride(3),
+            seq_lens.data_ptr(), int(max_seq_len), float(sm_scale), int(split_tokens),
+            o.data_ptr(), o.stride(0), o.stride(1), o.stride(2),
+            lse.data_ptr(), lse.stride(0), lse.stride(1), lse.stride(2),
+            _base_code(base), None if workspace is None else workspace.data_ptr(), ws_bytes,
+            _stream_handle(stream))
+    return _Prepared("dcp_decode_attention", args, (q, k, v, seq_lens, o, lse, workspace))
+
+
+def decode_attention(q, k, v, seq_lens, max_seq_len, o, lse, sm_scale, base="e", split_tokens=1024,
+                     workspace=None, stream=None) -> None:
+    prepare_decode_attention(q, k, v, seq_lens, max_seq_len, o, lse, sm_scale, base, split_tokens,
+                             workspace, stream)()
+
+
+def workspace_bytes(N: int, B: int, H: int, D: int, max_seq_len: int, split_tokens: int) -> int:
+    return dcp_decode_attention_workspace_size(N, B, H, D, max_seq_len, split_tokens)

@@ -4,6 +4,7 @@
 // call launches nothing.
 #include <stdarg.h>
 #include <stdio.h>
+#include <math.h>
 #include <string.h>
 
 #include <atomic>
@@ -399,6 +400,101 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
                      lse, r_sg * e / 4, r_sn * e / 4, r_sb * e / 4, r_sh * e / 4, out, u_sg * e,
                      u_sb * e, u_sh * e, out_lse, ul_sg, ul_sb, ul_sh, lse_base, return_lse, flags,
                      vr.align(), vu.align(), false, (cudaStream_t)stream);
+}
+
+// ---- decode attention per rank ------------------------------------------
+
+static int attn_nsplit(int N, int max_seq_len, int split_tokens) {
+    const int64_t lloc = ((int64_t)max_seq_len + N - 1) / N;
+    const int64_t s = (lloc + split_tokens - 1) / split_tokens;
+    return s < 1 ? 1 : (int)s;
+}
+
+static size_t attn_workspace_bytes(int N, int B, int H, int D, int nsplit) {
+    if (nsplit <= 1) return 0;
+    const size_t rows = (size_t)N * B * H * nsplit;
+    return rows * (size_t)D * 4 + rows * 4;
+}
+
+size_t dcp_decode_attention_workspace_size(int N, int B, int H, int D, int max_seq_len, int split_tokens) {
+    if (N < 1 || B < 0 || H < 1 || D < 1 || max_seq_len < 0 || split_tokens < 1) return 0;
+    return attn_workspace_bytes(N, B, H, D, attn_nsplit(N, max_seq_len, split_tokens));
+}
+
+dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D,
+                                  const void* q, int64_t q_sb, int64_t q_sh,
+                                  const void* k, int64_t k_sn, int64_t k_sb, int64_t k_st, int64_t k_sh,
+                                  const void* v, int64_t v_sn, int64_t v_sb, int64_t v_st, int64_t v_sh,
+                                  const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                  void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                  float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                  int lse_base, void* workspace, size_t workspace_bytes, void* stream) {
+    const char* who = "dcp_decode_attention";
+    if (dtype != DCP_F16 && dtype != DCP_BF16)
+        return fail(DCP_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d (f16 or bf16 caches only)", who, dtype);
+    const int e = 2;
+    if (N < 1 || N > kMaxRanks || B < 0 || H < 1 || Hkv < 1 || max_seq_len < 0 || split_tokens < 1)
+        return fail(DCP_ERR_INVALID_ARG, "%s: sizes N=%d B=%d H=%d Hkv=%d max_seq_len=%d split_tokens=%d",
+                    who, N, B, H, Hkv, max_seq_len, split_tokens);
+    if (H % Hkv) return fail(DCP_ERR_HEADS_NOT_DIVISIBLE, "%s: H=%d is not a multiple of Hkv=%d", who, H, Hkv);
+    const int gq = H / Hkv;
+    if (gq != 1 && gq != 2 && gq != 4 && gq != 8)
+        return fail(DCP_ERR_INVALID_ARG, "%s: H/Hkv=%d (1, 2, 4 or 8 query heads per KV head)", who, gq);
+    if (D != 64 && D != 128 && D != 256) return fail(DCP_ERR_INVALID_ARG, "%s: D=%d (64, 128 or 256)", who, D);
+    if (!(sm_scale == sm_scale) || sm_scale == INFINITY || sm_scale == -INFINITY)
+        return fail(DCP_ERR_INVALID_ARG, "%s: sm_scale is not finite", who);
+    if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)
+        return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
+    if (B == 0) return ok();
+    const int nsplit = attn_nsplit(N, max_seq_len, split_tokens);
+    if ((int64_t)N * B * Hkv >= (1ll << 31) || nsplit > 65535)
+        return fail(DCP_ERR_INVALID_ARG, "%s: too many work items", who);
+    if (!q || !k || !v || !seq_lens || !o || !lse)
+        return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (any_negative({q_sb, q_sh, k_sn, k_sb, k_st, k_sh, v_sn, v_sb, v_st, v_sh, o_sn, o_sb, o_sh, l_sn, l_sb, l_sh}))
+        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride", who);
+    const int64_t rb = (int64_t)D * e;
+    const int64_t lcap = ((int64_t)max_seq_len + N - 1) / N;  // local cache capacity (tokens)
+    View vq = View(q, rb).dim(B, q_sb * e).dim(H, q_sh * e);
+    View vk = View(k, rb).dim(N, k_sn * e).dim(B, k_sb * e).dim(lcap, k_st * e).dim(Hkv, k_sh * e);
+    View vv = View(v, rb).dim(N, v_sn * e).dim(B, v_sb * e).dim(lcap, v_st * e).dim(Hkv, v_sh * e);
+    View vo = View(o, rb).dim(N, o_sn * e).dim(B, o_sb * e).dim(H, o_sh * e);
+    View vl = View(lse, 4).dim(N, l_sn * 4).dim(B, l_sb * 4).dim(H, l_sh * 4);
+    View vs = View(seq_lens, 4).dim(B, 4);
+    if (vq.align() < 16 || vk.align() < 16 || vv.align() < 16)
+        return fail(DCP_ERR_MISALIGNED, "%s: q, k and v rows must start on 16-byte boundaries", who);
+    if ((uintptr_t)o % e || (uintptr_t)lse % 4 || (uintptr_t)seq_lens % 4)
+        return fail(DCP_ERR_MISALIGNED, "%s: pointer not aligned to its element type", who);
+    for (const View* in : {&vq, &vk, &vv, &vs})
+        if (overlap(vo, *in) || overlap(vl, *in))
+            return fail(DCP_ERR_ALIAS, "%s: an output overlaps an input", who);
+    if (overlap(vo, vl) || !vo.rows_disjoint() || !vl.rows_disjoint())
+        return fail(DCP_ERR_ALIAS, "%s: outputs overlap", who);
+    const size_t need = attn_workspace_bytes(N, B, H, D, nsplit);
+    if (need) {
+        if (!workspace || workspace_bytes < need)
+            return fail(DCP_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed (%zu given)", who, need,
+                        workspace ? workspace_bytes : (size_t)0);
+        if ((uintptr_t)workspace % 16) return fail(DCP_ERR_MISALIGNED, "%s: workspace not 16-byte aligned", who);
+        View vw = View(workspace, (int64_t)need);
+        for (const View* other : {&vq, &vk, &vv, &vs, &vo, &vl})
+            if (overlap(vw, *other)) return fail(DCP_ERR_ALIAS, "%s: workspace overlaps an operand", who);
+    }
+    dcp::AttnParams p;
+    p.N = N; p.B = B; p.H = H; p.Hkv = Hkv; p.D = D;
+    p.max_seq_len = max_seq_len; p.split_tokens = split_tokens; p.nsplit = nsplit;
+    p.base2 = lse_base == DCP_LSE_BASE_2;
+    p.sm_scale = sm_scale;
+    p.q = (const unsigned char*)q; p.q_sb = q_sb * e; p.q_sh = q_sh * e;
+    p.k = (const unsigned char*)k; p.k_sn = k_sn * e; p.k_sb = k_sb * e; p.k_st = k_st * e; p.k_sh = k_sh * e;
+    p.v = (const unsigned char*)v; p.v_sn = v_sn * e; p.v_sb = v_sb * e; p.v_st = v_st * e; p.v_sh = v_sh * e;
+    p.seq_lens = seq_lens;
+    p.o = (unsigned char*)o; p.o_sn = o_sn * e; p.o_sb = o_sb * e; p.o_sh = o_sh * e;
+    p.lse = lse; p.l_sn = l_sn; p.l_sb = l_sb; p.l_sh = l_sh;
+    const size_t rows = (size_t)N * B * H * nsplit;
+    p.ws_o = need ? (float*)workspace : nullptr;
+    p.ws_lse = need ? (float*)workspace + rows * D : nullptr;
+    return launched(dcp::launch_decode_attention(p, dtype, (cudaStream_t)stream), who);
 }
 
 }  // extern "C"

@@ -49,7 +49,31 @@ struct CombineParams {
     int64_t ul_sg, ul_sb, ul_sh;
 };
 
+// Decode attention of every rank over its round-robin share of the KV cache.
+struct AttnParams {
+    int N, B, H, Hkv, D;
+    int max_seq_len;   // bound on seq_lens; the local caches hold ceil(max_seq_len / N) tokens
+    int split_tokens;  // local tokens per split
+    int nsplit;        // splits per (rank, request, KV head)
+    int base2;         // returned LSE base: 0 = e, 1 = 2
+    float sm_scale;
+    const unsigned char* q;
+    int64_t q_sb, q_sh;                 // bytes
+    const unsigned char* k;
+    int64_t k_sn, k_sb, k_st, k_sh;     // bytes
+    const unsigned char* v;
+    int64_t v_sn, v_sb, v_st, v_sh;     // bytes
+    const int* seq_lens;                // [B] global lengths
+    unsigned char* o;
+    int64_t o_sn, o_sb, o_sh;           // bytes
+    float* lse;
+    int64_t l_sn, l_sb, l_sh;           // fp32 words
+    float* ws_o;                        // [N*B*H*nsplit][D] partial outputs (nsplit > 1)
+    float* ws_lse;                      // [N*B*H*nsplit] partial base-2 LSEs
+};
+
 // Launchers return the launch's cudaGetLastError().
+cudaError_t launch_decode_attention(const AttnParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_combine_f32(const CombineParams& p, int vb, cudaStream_t stream);
 cudaError_t launch_combine_f16(const CombineParams& p, int vb, cudaStream_t stream);

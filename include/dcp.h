@@ -11,7 +11,9 @@
  *                       interleaved or peer-inside split), by strides alone;
  *   dcp_lse_combine     the LSE-weighted combine over strided views;
  *   dcp_unpack_combine  the combine reading interleaved [payload | LSE word]
- *                       receive rows in one pass.
+ *                       receive rows in one pass;
+ *   dcp_decode_attention  the step before the merge: each rank's decode
+ *                       attention over its round-robin share of the KV cache.
  *
  * The cross-rank exchange itself (NCCL all-to-all, MNNVL, all-gather /
  * all-reduce) is not part of this library.  A group's N ranks can be held as
@@ -47,6 +49,7 @@
 #ifndef DCP_GB300_DCP_H_
 #define DCP_GB300_DCP_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -189,6 +192,51 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
                                 void* out, int64_t u_sg, int64_t u_sb, int64_t u_sh,
                                 float* out_lse, int64_t ul_sg, int64_t ul_sb, int64_t ul_sh,
                                 int lse_base, int return_lse, unsigned flags, void* stream);
+
+/*
+ * dcp_decode_attention -- each DCP rank's single-token decode attention over
+ * the KV tokens it owns, producing the rank-local partials the merge takes.
+ * (sglang PR #33926 report, "实现拆解" items 3-4 and "关键源码片段": token t of a
+ * request lives on rank t % N, so rank r holds L / N tokens plus one when
+ * r < L % N (`get_dcp_lens`); each rank returns rank-local (out, lse); a rank
+ * owning no token of a request is the neutral (0, -inf) (`fixup_zero_kv_rows`);
+ * trtllm-gen's LSE is base 2, cute-dsl's natural log.)
+ *
+ * For rank r < N, request b < B, query head h < H (KV head h / (H / Hkv)),
+ * over the rank's local tokens i < L_r(b) = L_b / N + (r < L_b % N), with
+ * L_b = min(seq_lens[b], max_seq_len) and scores s_i = sm_scale <q, k_i>:
+ *     lse[r, b, h] = log sum_i exp(s_i)           (base e, or divided by ln 2)
+ *     o  [r, b, h] = sum_i exp(s_i - lse) v_i      (0 and -inf when L_r(b) = 0)
+ *
+ *   q        [B, H, D]              payload, strides (q_sb, q_sh)
+ *   k, v     [N][B, Lc, Hkv, D]     each rank's local cache, token i of rank r
+ *                                   being global token i*N + r; Lc =
+ *                                   ceil(max_seq_len / N); strides
+ *                                   (k_sn, k_sb, k_st, k_sh), same for v
+ *   seq_lens [B] int32 (device)     global lengths; values above max_seq_len
+ *                                   count as max_seq_len
+ *   o        [N, B, H, D]           payload, strides (o_sn, o_sb, o_sh)
+ *   lse      [N, B, H]              fp32, strides (l_sn, l_sb, l_sh)
+ *
+ * dtype: DCP_F16 or DCP_BF16 (q, k, v and o); D in {64, 128, 256}; H / Hkv in
+ * {1, 2, 4, 8}; q, k and v rows start on 16-byte boundaries.  Work is split
+ * into chunks of `split_tokens` local tokens; with more than one chunk the
+ * partial results go through `workspace` (caller-owned device memory, 16-byte
+ * aligned, at least dcp_decode_attention_workspace_size(...) bytes; NULL is
+ * fine when that size is 0).  Errors: DCP_ERR_HEADS_NOT_DIVISIBLE when
+ * H % Hkv != 0, DCP_ERR_INVALID_ARG for unsupported sizes or a too small
+ * workspace, DCP_ERR_MISALIGNED, DCP_ERR_ALIAS for overlapping operands.
+ */
+size_t dcp_decode_attention_workspace_size(int N, int B, int H, int D, int max_seq_len, int split_tokens);
+
+dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D,
+                                  const void* q, int64_t q_sb, int64_t q_sh,
+                                  const void* k, int64_t k_sn, int64_t k_sb, int64_t k_st, int64_t k_sh,
+                                  const void* v, int64_t v_sn, int64_t v_sb, int64_t v_st, int64_t v_sh,
+                                  const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                  void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                  float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                  int lse_base, void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

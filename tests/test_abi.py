@@ -123,3 +123,36 @@ def test_binding_raises_with_message(lib):
     with pytest.raises(binding.DcpError) as ei:
         binding.check(pack(N=3), "dcp_pack_send")
     assert ei.value.name == "DCP_ERR_HEADS_NOT_DIVISIBLE"
+
+
+def attn(dtype=BF16, N=2, B=2, H=4, Hkv=4, D=128, q=A, q_s=(512, 128), k=Bp, k_s=(8192, 4096, 512, 128),
+         v=C, v_s=(8192, 4096, 512, 128), seq=Dp, max_len=16, scale=0.1, split=4, o=0x50000000,
+         o_s=(1024, 512, 128), lse=0x60000000, l_s=(8, 4, 1), base=0, ws=0x70000000, ws_bytes=1 << 20):
+    return binding.dcp_decode_attention(dtype, N, B, H, Hkv, D, q, *q_s, k, *k_s, v, *v_s, seq, max_len,
+                                        scale, split, o, *o_s, lse, *l_s, base, ws, ws_bytes, None)
+
+
+def test_decode_attention_workspace_size(lib):
+    # one split: no workspace; else N*B*H*splits rows of D fp32 + one fp32 LSE each
+    assert binding.dcp_decode_attention_workspace_size(4, 3, 8, 128, 4000, 1000) == 0
+    assert binding.dcp_decode_attention_workspace_size(4, 3, 8, 128, 4001, 1000) == 4 * 3 * 8 * 2 * (128 + 1) * 4
+    assert binding.dcp_decode_attention_workspace_size(2, 1, 1, 64, 1000, 100) == 2 * 5 * 65 * 4
+    assert binding.dcp_decode_attention_workspace_size(0, 1, 1, 64, 10, 1) == 0
+
+
+def test_decode_attention_validation(lib):
+    assert attn(dtype=F32) == 2
+    assert attn(H=6, Hkv=4) == 3
+    assert attn(H=6, Hkv=2) == 1               # three query heads per KV head
+    assert attn(D=96) == 1
+    assert attn(split=0) == 1
+    assert attn(scale=float("nan")) == 1
+    assert attn(base=5) == 1
+    assert attn(q=A + 8) == 4                  # rows not on 16-byte boundaries
+    assert attn(k_s=(8192, 4096, 516, 128)) == 4
+    assert attn(seq=0) == 1
+    assert attn(ws_bytes=100) == 1             # 2 splits of 4 local tokens need a workspace
+    assert attn(ws=0) == 1
+    assert attn(o=A) == 5                      # output over q
+    assert attn(lse=0x50000000) == 5           # lse over o
+    assert attn(B=0) == 0

@@ -1,0 +1,176 @@
+"""GPU parity of each rank's decode attention over its round-robin share of the
+KV cache (the step that produces the merge's inputs), against the oracle's
+split attention, and the whole one-GPU DCP decode (attention per rank, pack,
+exchange view, combine) against unsplit attention.
+
+Attention tolerances (fp32 arithmetic over 16-bit inputs, written here): the
+payload output as for the merges (tests/parity.py); the LSE within
+2e-4 + 1e-5 |lse|: fp32 dot products of up to 256 terms whose magnitudes sum
+to ~sm_scale * D (about 1e-4 absolute at worst) plus the rounding of the
+log-sum-exp itself.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_context_attention_gb300 import binding, build, layouts
+
+from parity import assert_merge_close, to_f64, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    binding.load()
+    oracle.build()
+
+
+def local_caches(K, N):
+    """Global cache [B, L, Hkv, D] -> every rank's local cache [N, B, ceil(L/N), Hkv, D]
+    (token i of rank r is global token i*N + r; the tail is zero padding)."""
+    B, L, Hkv, D = K.shape
+    lc = (L + N - 1) // N
+    out = torch.zeros((N, B, lc, Hkv, D), dtype=K.dtype, device=K.device)
+    for r in range(N):
+        part = K[:, r::N]
+        out[r, :, :part.shape[1]] = part
+    return out
+
+
+def make_case(N, B, H, Hkv, D, lens, dtype, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    L = max(max(lens), 1)
+    q = torch.randn((B, H, D), generator=g, device=DEV).to(dtype)
+    K = torch.randn((B, L, Hkv, D), generator=g, device=DEV).to(dtype)
+    V = torch.randn((B, L, Hkv, D), generator=g, device=DEV).to(dtype)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    return q, K, V, seq, L
+
+
+def run_attention(q, K, V, seq, L, N, scale, base, split):
+    B, H, D = q.shape
+    Hkv = K.shape[2]
+    k, v = local_caches(K, N), local_caches(V, N)
+    o = torch.empty((N, B, H, D), dtype=q.dtype, device=DEV)
+    lse = torch.empty((N, B, H), dtype=torch.float32, device=DEV)
+    nbytes = binding.workspace_bytes(N, B, H, D, L, split)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=DEV) if nbytes else None
+    binding.decode_attention(q, k, v, seq, L, o, lse, scale, base=base, split_tokens=split, workspace=ws)
+    return o, lse
+
+
+def oracle_partials(q, K, V, lens, N, scale, base):
+    B, H, D = q.shape
+    Hkv = K.shape[2]
+    gq = H // Hkv
+    qn, Kn, Vn = to_f64(q), to_f64(K), to_f64(V)
+    want = np.zeros((N, B, H, D))
+    want_lse = np.zeros((N, B, H))
+    for b in range(B):
+        for h in range(H):
+            O, l = oracle.split_attention(qn[b, h], Kn[b, :lens[b], h // gq], Vn[b, :lens[b], h // gq], N,
+                                          scale, base=base)
+            want[:, b, h], want_lse[:, b, h] = O, l
+    return want, want_lse
+
+
+def assert_attn_lse(got, want, what="lse"):
+    g = to_f64(got).reshape(want.shape)
+    ninf = want == -np.inf
+    assert np.array_equal(g == -np.inf, ninf), f"{what}: empty-rank positions differ"
+    d = np.abs(g[~ninf] - want[~ninf])
+    bad = d > 2e-4 + 1e-5 * np.abs(want[~ninf])
+    assert not bad.any(), f"{what}: {int(bad.sum())} values off, max {d.max():.3e}"
+
+
+CASES = [
+    # N, B, H, Hkv, D, lengths, dtype, base, split_tokens
+    (4, 3, 4, 4, 128, [0, 1, 3, 4, 5, 200, 1111], torch.bfloat16, "e", 16),
+    (4, 3, 4, 4, 128, [0, 1, 3, 4, 5, 200, 1111], torch.bfloat16, "2", 4096),
+    (2, 2, 8, 2, 64, [7, 64, 129, 300], torch.float16, "e", 32),
+    (8, 2, 4, 1, 256, [3, 9, 17, 500], torch.bfloat16, "2", 40),
+    (3, 2, 16, 2, 128, [1, 2, 1000], torch.float16, "2", 100),
+    (1, 2, 2, 2, 128, [0, 1, 77], torch.bfloat16, "e", 8),
+]
+
+
+@pytest.mark.parametrize("N,B,H,Hkv,D,lens,dtype,base,split", CASES)
+def test_rank_partials_match_oracle(N, B, H, Hkv, D, lens, dtype, base, split):
+    B = len(lens)
+    q, K, V, seq, L = make_case(N, B, H, Hkv, D, lens, dtype, seed=N * 100 + D)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_attention(q, K, V, seq, L, N, scale, base, split)
+    want, want_lse = oracle_partials(q, K, V, lens, N, scale, base)
+    torch.cuda.synchronize()
+    assert_merge_close(o, want, "rank partial O")
+    assert_attn_lse(lse, want_lse)
+
+
+def test_lengths_above_the_bound_are_clamped():
+    N, D = 2, 64
+    q, K, V, seq, L = make_case(N, 2, 2, 2, D, [10, 30], torch.bfloat16, seed=5)
+    seq_big = torch.tensor([10, 10_000], dtype=torch.int32, device=DEV)
+    o, lse = run_attention(q, K, V, seq_big, 30, N, 0.125, "e", 8)
+    want, want_lse = oracle_partials(q, K, V, [10, 30], N, 0.125, "e")
+    torch.cuda.synchronize()
+    assert_merge_close(o, want)
+    assert_attn_lse(lse, want_lse)
+
+
+@pytest.mark.parametrize("base", ["e", "2"])
+def test_whole_dcp_decode_equals_unsplit_attention(base):
+    """Attention per rank -> peer-inside pack -> exchange view -> combine, all on
+    one GPU, equals single-query softmax attention over the whole sequence."""
+    N, H, Hkv, D = 4, 16, 4, 128
+    lens = [1, 3, 57, 640, 2049, 4]
+    B = len(lens)
+    q, K, V, seq, L = make_case(N, B, H, Hkv, D, lens, torch.bfloat16, seed=77)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_attention(q, K, V, seq, L, N, scale, base, 256)       # [N,B,H,D], [N,B,H]
+    H_pr = H // N
+    partial_o, stats = layouts.alloc_peer_inside(N, B, H_pr, N, D, torch.bfloat16, DEV)
+    binding.pack_send(o, lse, *layouts.peer_inside_send_views(partial_o, stats))
+    ro, rl = layouts.exchange_peer_inside(partial_o, stats)
+    out = torch.empty((N, B, H_pr, D), dtype=torch.bfloat16, device=DEV)
+    out_lse = torch.empty((N, B, H_pr), dtype=torch.float32, device=DEV)
+    binding.lse_combine(ro, rl, out, out_lse, base=base)
+    torch.cuda.synchronize()
+    # destination d holds heads [d*H_pr, (d+1)*H_pr)
+    got = out.permute(1, 0, 2, 3).reshape(B, H, D)
+    got_lse = out_lse.permute(1, 0, 2).reshape(B, H)
+    qn, Kn, Vn = to_f64(q), to_f64(K), to_f64(V)
+    want = np.zeros((B, H, D))
+    want_lse = np.zeros((B, H))
+    for b in range(B):
+        for h in range(H):
+            s = (Kn[b, :lens[b], h // (H // Hkv)] @ qn[b, h]) * scale
+            m = s.max()
+            p = np.exp(s - m)
+            want[b, h] = (p / p.sum()) @ Vn[b, :lens[b], h // (H // Hkv)]
+            want_lse[b, h] = (m + math.log(p.sum())) / (math.log(2.0) if base == "2" else 1.0)
+    # the merge itself, exactly as the oracle merges the GPU's own bf16 partials
+    po_np = to_np(partial_o)
+    st_np = stats.cpu().numpy()
+    m_want, m_want_lse = oracle.combine("bf16", po_np.transpose(3, 0, 1, 2, 4), st_np[..., 0].transpose(3, 0, 1, 2),
+                                        base=base)
+    assert_merge_close(out, m_want, "merge of the GPU partials")
+    # against unsplit attention: the pipeline rounds twice (each rank's partial
+    # to bf16, then the merged row), so per element |d| <= 2^-8 (|want| +
+    # sum_r w_r |O_r|) + 1e-5, with w_r and O_r the oracle's per-rank values
+    parts, plse = oracle_partials(q, K, V, lens, N, scale, "e")
+    with np.errstate(invalid="ignore"):
+        gl = np.logaddexp.reduce(plse, axis=0)
+        w = np.nan_to_num(np.exp(plse - gl[None]), nan=0.0)
+    spread = (w[..., None] * np.abs(parts)).sum(axis=0)
+    d = np.abs(to_f64(got) - want)
+    bound = 2.0 ** -8 * (np.abs(want) + spread) + 1e-5
+    assert (d <= bound).all(), f"merged attention: worst excess {(d - bound).max():.3e}"
+    assert d.max() / np.abs(want).max() <= 2e-2
+    assert_attn_lse(got_lse, want_lse, "merged lse")
