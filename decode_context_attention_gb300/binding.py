@@ -37,7 +37,7 @@ STATUS_NAMES = {0: "DCP_OK", 1: "DCP_ERR_INVALID_ARG", 2: "DCP_ERR_UNSUPPORTED_D
 # Every symbol include/dcp.h declares.
 EXPORTS = ("dcp_lse_pack_dim", "dcp_status_string", "dcp_last_error_message", "dcp_pack_send",
            "dcp_lse_combine", "dcp_unpack_combine", "dcp_decode_attention_workspace_size",
-           "dcp_decode_attention")
+           "dcp_decode_attention", "dcp_decode_attention_noalloc")
 
 
 class DcpError(RuntimeError):
@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                              + [vp, i64, i64, i64, i64] + [vp, i32, ctypes.c_float, i32]
                                              + [vp, i64, i64, i64] + [vp, i64, i64, i64]
                                              + [i32, vp, ctypes.c_size_t, vp])
+        lib.dcp_decode_attention_noalloc.restype = i32
+        lib.dcp_decode_attention_noalloc.argtypes = lib.dcp_decode_attention.argtypes[:-3] + [vp]
         _lib = lib
         return lib
 

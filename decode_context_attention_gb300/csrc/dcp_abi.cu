@@ -174,6 +174,11 @@ constexpr int kMaxRanks = 4096;
 
 }  // namespace
 
+namespace dcp {
+// Lets other translation units report a failure through dcp_last_error_message().
+dcp_status_t set_error(dcp_status_t s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace dcp
+
 extern "C" {
 
 int dcp_lse_pack_dim(int dtype) {

@@ -28,6 +28,9 @@
 //    merges the splits with the LSE rule of the combine (empty splits and
 //    empty ranks are the neutral (0, -inf) and drop out exactly).
 #include <math.h>
+#include <stdio.h>
+
+#include <mutex>
 
 #include "dcp_device.cuh"
 
@@ -267,3 +270,70 @@ cudaError_t launch_decode_attention(const AttnParams& p, int dtype, cudaStream_t
 }
 
 }  // namespace dcp
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory.  Some callers
+// of this library may not call cudaMalloc (or any allocator) at the point
+// where they run the attention: code that runs inside a memory pool whose
+// size is fixed up front, an inference server that forbids allocation on its
+// serving path, or a host runtime that has no allocator of its own to hand.
+// For them the scratch the split path needs lives in this file-scope device
+// array instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB, reserved on every device that loads this code
+static __device__ __align__(256) float g_attn_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};  // device address of g_attn_scratch, per device
+
+}  // namespace
+
+extern "C" dcp_status_t dcp_decode_attention_noalloc(
+    int dtype, int N, int B, int H, int Hkv, int D, const void* q, int64_t q_sb, int64_t q_sh,
+    const void* k, int64_t k_sn, int64_t k_sb, int64_t k_st, int64_t k_sh, const void* v, int64_t v_sn,
+    int64_t v_sb, int64_t v_st, int64_t v_sh, const int* seq_lens, int max_seq_len, float sm_scale,
+    int split_tokens, void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh, float* lse, int64_t l_sn,
+    int64_t l_sb, int64_t l_sh, int lse_base, void* stream) {
+    const size_t need = dcp_decode_attention_workspace_size(N, B, H, D, max_seq_len, split_tokens);
+    if (need > kNoAllocScratchBytes) {
+        char msg[256];
+        snprintf(msg, sizeof(msg),
+                 "dcp_decode_attention_noalloc: these sizes need %zu bytes of scratch, the built-in "
+                 "scratch holds %zu (use fewer splits, i.e. a larger split_tokens, or "
+                 "dcp_decode_attention with a workspace)",
+                 need, kNoAllocScratchBytes);
+        return dcp::set_error(DCP_ERR_INVALID_ARG, msg);
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "dcp_decode_attention_noalloc: no usable current device (%s)",
+                 cudaGetErrorString(e));
+        return dcp::set_error(DCP_ERR_CUDA, msg);
+    }
+    void* scratch = nullptr;
+    {
+        // first call on this device: look up the array's device address once,
+        // with this device current
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_ptr[dev]) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_attn_scratch);
+            if (e != cudaSuccess) {
+                char msg[256];
+                snprintf(msg, sizeof(msg), "dcp_decode_attention_noalloc: cudaGetSymbolAddress failed: %s",
+                         cudaGetErrorString(e));
+                return dcp::set_error(DCP_ERR_CUDA, msg);
+            }
+            g_scratch_ptr[dev] = ptr;
+        }
+        scratch = g_scratch_ptr[dev];
+    }
+    return dcp_decode_attention(dtype, N, B, H, Hkv, D, q, q_sb, q_sh, k, k_sn, k_sb, k_st, k_sh, v, v_sn,
+                                v_sb, v_st, v_sh, seq_lens, max_seq_len, sm_scale, split_tokens, o, o_sn,
+                                o_sb, o_sh, lse, l_sn, l_sb, l_sh, lse_base, scratch, kNoAllocScratchBytes,
+                                stream);
+}

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "dcp.h"
+
 namespace dcp {
 
 constexpr int kThreads = 256;  // threads per CTA for every kernel here
@@ -71,6 +73,9 @@ struct AttnParams {
     float* ws_o;                        // [N*B*H*nsplit][D] partial outputs (nsplit > 1)
     float* ws_lse;                      // [N*B*H*nsplit] partial base-2 LSEs
 };
+
+// Records `msg` as this host thread's dcp_last_error_message() and returns s.
+dcp_status_t set_error(dcp_status_t s, const char* msg);
 
 // Launchers return the launch's cudaGetLastError().
 cudaError_t launch_decode_attention(const AttnParams& p, int dtype, cudaStream_t stream);

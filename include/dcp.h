@@ -238,6 +238,36 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
                                   float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
                                   int lse_base, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * dcp_decode_attention_noalloc -- dcp_decode_attention for callers that may
+ * not allocate device memory where they run it (a fixed-size memory pool set
+ * up front, a serving loop that forbids allocation, a host runtime with no
+ * allocator to hand), so cannot provide a workspace.  The pages have no
+ * counterpart; this is a convenience of this library.
+ *
+ * Same arguments, result and errors as dcp_decode_attention, without the
+ * workspace: the split partials live in a 16 MiB scratch array built into the
+ * library, which every device that loads the library's attention code holds
+ * until the process exits.  Sizes whose scratch
+ * (dcp_decode_attention_workspace_size) exceeds 16 MiB are rejected with
+ * DCP_ERR_INVALID_ARG and a message giving both sizes; use a larger
+ * split_tokens or dcp_decode_attention with a workspace instead.  The call
+ * allocates nothing.  Its first call on a device looks up the scratch
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls share the one
+ * array and every call writes each scratch entry before reading it (nothing
+ * needs to start at zero), so calls whose work overlaps on the GPU (other
+ * streams, other threads) race on the scratch: serialise them.
+ */
+dcp_status_t dcp_decode_attention_noalloc(int dtype, int N, int B, int H, int Hkv, int D,
+                                          const void* q, int64_t q_sb, int64_t q_sh,
+                                          const void* k, int64_t k_sn, int64_t k_sb, int64_t k_st, int64_t k_sh,
+                                          const void* v, int64_t v_sn, int64_t v_sb, int64_t v_st, int64_t v_sh,
+                                          const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                          void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                          float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                          int lse_base, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif
