@@ -13,8 +13,10 @@ kernel reads its inputs from HBM.
 
 Also measured in the same run and reported under "secondary": the in-place
 sanitising combine of the cached-extend workload (N = 8, 16384 tokens, 96
-heads, D = 512, fp32; 29 GB per call) and the largest long-context sweep
-point through the fused unpack+combine (N = 8, B = 256, H = 64, D = 512, fp16).
+heads, D = 512, fp32; 29 GB per call), the largest long-context sweep point
+through the fused unpack+combine (N = 8, B = 256, H = 64, D = 512, fp16), and
+the decode attention that produces the merge's inputs (N = 4 ranks, B = 64
+requests, H = 32, D = 128, bf16, lengths up to 16384; ~9 GB of K/V).
 
 `--impl reference` times the fp64 CPU oracle instead, on a bounded sample of
 the same workload, and reports it in the same unit.
@@ -306,6 +308,34 @@ def setup_cached_extend(device, tokens=None):
             "bytes": [bytes_merge(1, N, T, H, D, 4)]}
 
 
+def setup_decode_attention(device, split_tokens=1024):
+    import math
+
+    import torch
+
+    from decode_context_attention_gb300 import binding
+    from decode_context_attention_gb300.workloads import generate_attention
+
+    a = generate_attention(device=device)
+    c = a["cfg"]
+    N, B, H, Hkv, D = c["N"], c["B"], c["H"], c["Hkv"], c["D"]
+    o = torch.empty((N, B, H, D), dtype=a["q"].dtype, device=device)
+    lse = torch.empty((N, B, H), dtype=torch.float32, device=device)
+    nbytes = binding.workspace_bytes(N, B, H, D, a["max_len"], split_tokens)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
+    call = binding.prepare_decode_attention(a["q"], a["k"], a["v"], a["seq_lens"], a["max_len"], o, lse,
+                                            1.0 / math.sqrt(D), base=c["base"], split_tokens=split_tokens,
+                                            workspace=ws)
+    tokens = int(a["seq_lens"].sum().item())
+    e = a["q"].element_size()
+    # K and V rows of every owned token, each rank's read of q, O and LSE written
+    algo = 2 * tokens * Hkv * D * e + N * B * H * D * e + N * B * H * D * e + N * B * H * 4
+    return {"launches": [call], "keep": (a, o, lse, ws), "tokens": tokens, "workspace_bytes": nbytes,
+            "names": [f"dcp_decode_attention (N={N} B={B} H={H} Hkv={Hkv} D={D} bf16, "
+                      f"{tokens} KV tokens, splits of {split_tokens})"],
+            "bytes": [algo]}
+
+
 def setup_sweep_max(device):
     import torch
 
@@ -409,6 +439,7 @@ def run_gpu(args):
         # a short run of one workload (for profiler captures); prints nothing
         wl = {"mla_decode": lambda: setup_mla_decode(device),
               "sweep": lambda: setup_sweep_max(device),
+              "decode_attention": lambda: setup_decode_attention(device),
               "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens)}[args.only]()
         time_sequence(wl["launches"], args.steps, args.warmup,
                       None if args.only == "cached_extend" else flush, device)
@@ -435,6 +466,13 @@ def run_gpu(args):
                           "kernels": [kernel_record(n, p, b, peak)
                                       for n, p, b in zip(sw["names"], p2, sw["bytes"])]})
         del sw
+        at = setup_decode_attention(device)
+        p4, _ = time_sequence(at["launches"], max(10, args.steps // 20), 3, flush, device)
+        secondary.append({"workload": "mha_decode_attention (the step before the merge)",
+                          "workspace_bytes": at["workspace_bytes"],
+                          "kernels": [kernel_record(at["names"][0], p4[0], at["bytes"][0], peak)]})
+        del at
+        torch.cuda.empty_cache()
         ce = setup_cached_extend(device)
         p3, _ = time_sequence(ce["launches"], args.ext_steps, 3, None, device)
         secondary.append({"workload": "cached_extend N=8 T=16384 H=96 D=512 fp32",
@@ -593,7 +631,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["mla_decode", "sweep", "cached_extend"],
+    ap.add_argument("--only", choices=["mla_decode", "sweep", "cached_extend", "decode_attention"],
                     help="run just this workload's launches (profiling); no JSON line")
     ap.add_argument("--ext-tokens", type=int, default=None,
                     help="tokens of the cached-extend workload under --only (default 16384)")

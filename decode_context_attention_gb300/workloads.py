@@ -27,6 +27,12 @@ cached-extend cases; no model weights or datasets are involved):
                  the LSE, drawn uniformly with replacement, are set to NaN, +inf
                  or -inf with equal odds.  In-place combine + head slices.
 
+  mha_decode_attention  the step before the merge: N=4 ranks, B=64 requests,
+                 H=32 query heads over 32 KV heads, D=128, bf16; request lengths
+                 ~ U(1, 16384); every rank's local K/V cache holds its
+                 round-robin share (local token i of rank r = global token
+                 i*N + r), values ~ N(0,1); queries ~ N(0,1).
+
 An empty (rank, token) pair is the pages' neutral state for a rank that owns
 no KV slice of that request: O = 0, LSE = -inf (sglang PR #33926 report,
 "实现拆解" item 3, `fixup_zero_kv_rows`).  KV ownership is per token, so the
@@ -158,3 +164,28 @@ def generate(w: Workload, device="cuda", seed: int | None = None) -> dict:
     if bool(empty.any()):
         _empty_pairs(empty, o, lse)
     return {"o": o, "lse": lse, "empty": empty}
+
+
+ATTENTION = {"mha_decode_attention": dict(N=4, B=64, H=32, Hkv=32, D=128, dtype="bf16", max_len=16384,
+                                          base="e", seed=5)}
+
+
+def generate_attention(name="mha_decode_attention", device="cuda", seed=None, **override) -> dict:
+    """Draw a decode-attention workload: q [B,H,D], each rank's local caches
+    k, v [N,B,Lc,Hkv,D] (Lc = ceil(max_len / N); entries past a rank's local
+    length are never read), seq_lens [B] int32 global lengths in [1, max_len]."""
+    c = dict(ATTENTION[name], **override)
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(c["seed"] if seed is None else seed)
+    N, B, H, Hkv, D, L = c["N"], c["B"], c["H"], c["Hkv"], c["D"], c["max_len"]
+    dt = TORCH_DTYPES[c["dtype"]]
+    lc = (L + N - 1) // N
+    q = torch.empty((B, H, D), dtype=dt, device=device).normal_(generator=g)
+    k = torch.empty((N, B, lc, Hkv, D), dtype=dt, device=device)
+    v = torch.empty((N, B, lc, Hkv, D), dtype=dt, device=device)
+    for r in range(N):
+        k[r].normal_(generator=g)
+        v[r].normal_(generator=g)
+    seq = torch.randint(1, L + 1, (B,), generator=g, device=device, dtype=torch.int64).to(torch.int32)
+    return {"q": q, "k": k, "v": v, "seq_lens": seq, "max_len": L, "cfg": c}

@@ -174,3 +174,40 @@ def test_whole_dcp_decode_equals_unsplit_attention(base):
     assert (d <= bound).all(), f"merged attention: worst excess {(d - bound).max():.3e}"
     assert d.max() / np.abs(want).max() <= 2e-2
     assert_attn_lse(got_lse, want_lse, "merged lse")
+
+
+def test_decode_attention_workload_full_size_sampled():
+    """The benchmark's workload (N=4, B=64, H=32, D=128, lengths up to 16384) in
+    its launch configuration (splits of 1024 local tokens): sampled (request,
+    head) rows of every rank against the oracle."""
+    from decode_context_attention_gb300.workloads import generate_attention
+
+    a = generate_attention(device=DEV)
+    c = a["cfg"]
+    N, B, H, Hkv, D = c["N"], c["B"], c["H"], c["Hkv"], c["D"]
+    scale = 1.0 / math.sqrt(D)
+    o = torch.empty((N, B, H, D), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((N, B, H), dtype=torch.float32, device=DEV)
+    nbytes = binding.workspace_bytes(N, B, H, D, a["max_len"], 1024)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    binding.decode_attention(a["q"], a["k"], a["v"], a["seq_lens"], a["max_len"], o, lse, scale,
+                             base=c["base"], split_tokens=1024, workspace=ws)
+    torch.cuda.synchronize()
+    lens = a["seq_lens"].cpu().tolist()
+    rng = np.random.default_rng(3)
+    picks = [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 24), rng.integers(0, H, 24))]
+    picks += [(int(np.argmax(lens)), 0), (int(np.argmin(lens)), H - 1)]
+    for b, h in picks:
+        L = lens[b]
+        hk = h // (H // Hkv)
+        # rebuild the global sequence: global token t = local token t // N of rank t % N
+        kg = torch.stack([a["k"][t % N, b, t // N, hk] for t in range(L)]) if L < 64 else None
+        if kg is None:
+            idx = torch.arange(L, device=DEV)
+            kg = a["k"][idx % N, b, idx // N, hk]
+            vg = a["v"][idx % N, b, idx // N, hk]
+        else:
+            vg = torch.stack([a["v"][t % N, b, t // N, hk] for t in range(L)])
+        O, l = oracle.split_attention(to_f64(a["q"][b, h]), to_f64(kg), to_f64(vg), N, scale, base=c["base"])
+        assert_merge_close(o[:, b, h], O, f"row b={b} h={h}")
+        assert_attn_lse(lse[:, b, h], l, f"lse b={b} h={h}")
