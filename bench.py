@@ -24,7 +24,6 @@ the same workload, and reports it in the same unit.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -232,11 +231,20 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def csrc_digest() -> str:
+# The source files that define each profiled kernel's code: a counter taken on
+# a kernel stays valid while these files are unchanged.
+KERNEL_SOURCES = {
+    "pack_kernel": ("dcp_pack.cu", "dcp_device.cuh"),
+    "combine_kernel": ("dcp_combine.cuh", "dcp_combine_bf16.cu", "dcp_device.cuh"),
+    "decode_partial_kernel": ("dcp_attention.cu", "dcp_device.cuh"),
+}
+
+
+def csrc_digest(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "decode_context_attention_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "decode_context_attention_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -249,7 +257,7 @@ def ncu_traffic(kernel: str):
     with open(p) as f:
         d = json.load(f)
     ent = d.get("kernels", {}).get(kernel)
-    if not ent or ent.get("csrc_digest") != csrc_digest():
+    if not ent or kernel not in KERNEL_SOURCES or ent.get("csrc_digest") != csrc_digest(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -308,7 +316,7 @@ def setup_cached_extend(device, tokens=None):
             "bytes": [bytes_merge(1, N, T, H, D, 4)]}
 
 
-def setup_decode_attention(device, split_tokens=1024):
+def setup_decode_attention(device, split_tokens=1024, batch=None):
     import math
 
     import torch
@@ -316,7 +324,7 @@ def setup_decode_attention(device, split_tokens=1024):
     from decode_context_attention_gb300 import binding
     from decode_context_attention_gb300.workloads import generate_attention
 
-    a = generate_attention(device=device)
+    a = generate_attention(device=device, **({"B": batch} if batch else {}))
     c = a["cfg"]
     N, B, H, Hkv, D = c["N"], c["B"], c["H"], c["Hkv"], c["D"]
     o = torch.empty((N, B, H, D), dtype=a["q"].dtype, device=device)
@@ -399,6 +407,60 @@ def oracle_one_eighth(w, o0, l0, po, st, rows=None):
     return (B / w.B) / w.N
 
 
+def time_oracle_attention(at, budget_s: float):
+    """Oracle µs per decode-attention call: sampled (request, head) rows of the
+    workload through oracle.split_attention (every rank at once), scaled by the
+    KV tokens of the whole call."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    a = at["keep"][0]
+    c = a["cfg"]
+    N, H, Hkv, D = c["N"], c["H"], c["Hkv"], c["D"]
+    lens = a["seq_lens"].cpu().tolist()
+    rng = np.random.default_rng(0)
+    done_tokens, t_used, n = 0, 0.0, 0
+    while t_used < budget_s and n < 64:
+        b, h = int(rng.integers(len(lens))), int(rng.integers(H))
+        L = lens[b]
+        idx = torch.arange(L, device=a["k"].device)
+        hk = h // (H // Hkv)
+        kg = a["k"][idx % N, b, idx // N, hk].double().cpu().numpy()
+        vg = a["v"][idx % N, b, idx // N, hk].double().cpu().numpy()
+        q = a["q"][b, h].double().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.split_attention(q, kg, vg, N, 1.0 / D ** 0.5, base=c["base"])
+        t_used += time.perf_counter() - t0
+        done_tokens += L
+        n += 1
+    total = at["tokens"] * H  # every (token, query head) pair of the call
+    return t_used / max(done_tokens, 1) * total * 1e6, t_used, n
+
+
+def time_oracle_cached_extend(budget_s: float):
+    """Oracle µs per cached-extend call from a small all-rows sample (the same
+    recipe at 64 tokens), scaled by the row count."""
+    import torch
+
+    import oracle
+    from decode_context_attention_gb300.workloads import WORKLOADS, generate, scaled
+
+    w = WORKLOADS["cached_extend"]
+    small = scaled(w, B=64)
+    d = generate(small, "cpu")
+    o, l = d["o"].numpy(), d["lse"].numpy()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.combine("f32", o[None], l[None], base=w.base, sanitize=True)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return el / n * (w.B / small.B) * 1e6, el, n
+
+
 def time_oracle(mla, budget_s: float):
     """Oracle µs per full call, extrapolated from repeated 1/8-call samples."""
     w, o0, l0, po, st = oracle_sample_inputs(mla)
@@ -439,7 +501,7 @@ def run_gpu(args):
         # a short run of one workload (for profiler captures); prints nothing
         wl = {"mla_decode": lambda: setup_mla_decode(device),
               "sweep": lambda: setup_sweep_max(device),
-              "decode_attention": lambda: setup_decode_attention(device),
+              "decode_attention": lambda: setup_decode_attention(device, batch=args.att_batch),
               "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens)}[args.only]()
         time_sequence(wl["launches"], args.steps, args.warmup,
                       None if args.only == "cached_extend" else flush, device)
@@ -468,16 +530,26 @@ def run_gpu(args):
         del sw
         at = setup_decode_attention(device)
         p4, _ = time_sequence(at["launches"], max(10, args.steps // 20), 3, flush, device)
-        secondary.append({"workload": "mha_decode_attention (the step before the merge)",
-                          "workspace_bytes": at["workspace_bytes"],
-                          "kernels": [kernel_record(at["names"][0], p4[0], at["bytes"][0], peak)]})
+        rec = {"workload": "mha_decode_attention (the step before the merge)",
+               "workspace_bytes": at["workspace_bytes"],
+               "kernels": [kernel_record(at["names"][0], p4[0], at["bytes"][0], peak)]}
+        if rank == 0 and not args.no_cpu_baseline:
+            us, el, n = time_oracle_attention(at, min(5.0, args.cpu_budget))
+            rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": 1,
+                                 "sample": f"{n} sampled (request, head) rows, {el:.1f} s, scaled by KV tokens"}
+        secondary.append(rec)
         del at
         torch.cuda.empty_cache()
         ce = setup_cached_extend(device)
         p3, _ = time_sequence(ce["launches"], args.ext_steps, 3, None, device)
-        secondary.append({"workload": "cached_extend N=8 T=16384 H=96 D=512 fp32",
-                          "inputs_vs_l2": "24 GiB stack, far larger than L2 (no flush)",
-                          "kernels": [kernel_record(ce["names"][0], p3[0], ce["bytes"][0], peak)]})
+        rec = {"workload": "cached_extend N=8 T=16384 H=96 D=512 fp32",
+               "inputs_vs_l2": "24 GiB stack, far larger than L2 (no flush)",
+               "kernels": [kernel_record(ce["names"][0], p3[0], ce["bytes"][0], peak)]}
+        if rank == 0 and not args.no_cpu_baseline:
+            us, el, n = time_oracle_cached_extend(min(5.0, args.cpu_budget))
+            rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": 1,
+                                 "sample": f"{n} x all rows of the 64-token case, {el:.1f} s, scaled by rows"}
+        secondary.append(rec)
         del ce
         torch.cuda.empty_cache()
     clk = clocks.stop()
@@ -633,6 +705,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=["mla_decode", "sweep", "cached_extend", "decode_attention"],
                     help="run just this workload's launches (profiling); no JSON line")
+    ap.add_argument("--att-batch", type=int, default=None,
+                    help="requests of the decode-attention workload under --only (default 64)")
     ap.add_argument("--ext-tokens", type=int, default=None,
                     help="tokens of the cached-extend workload under --only (default 16384)")
     args = ap.parse_args()
