@@ -10,7 +10,8 @@ numpy arrays.
 Every operand is a numpy array *view*; its strides (in bytes) are turned into
 element strides for the C code, so strided and interleaved layouts are
 described exactly as the pages describe them (a payload view plus an fp32
-word view of the same buffer).  bf16 arrays are carried as ``uint16``.
+word view of the same buffer).  bf16 arrays are carried as ``uint16`` and
+fp8 (e4m3) arrays as ``uint8``.
 
 Pins: ``tests/test_oracle.py`` checks every function here against what the
 pages and mathematics fix (identity at N=1, neutral empty ranks, shift
@@ -32,7 +33,7 @@ _SRC = os.path.join(_HERE, "dcp_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
-DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3, "fp8": 4}
 BASES = {"e": 0, "2": 1}
 SANITIZE_O = 1
 
@@ -96,7 +97,8 @@ def _ptr(a: np.ndarray) -> int:
 
 
 def _check_payload(a: np.ndarray, dtype: str) -> None:
-    want = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "f64": np.float64}[dtype]
+    want = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "f64": np.float64,
+            "fp8": np.uint8}[dtype]
     if a.dtype != want:
         raise TypeError(f"{dtype} payload must be a numpy {np.dtype(want)} array, got {a.dtype}")
     if a.shape and a.shape[-1] > 1 and a.strides[-1] != a.itemsize:

@@ -49,7 +49,10 @@
  * Conventions: all strides are in elements of the pointed-to type (payload
  * elements for O, fp32 words for LSE); the innermost (D) stride is 1.
  * dtype codes: 0 = fp32, 1 = fp16, 2 = bf16, 3 = fp64 (fp64 payloads exist only
- * so that the self-checks can run the merge without input rounding).
+ * so that the self-checks can run the merge without input rounding), 4 = fp8
+ * e4m3.  fp8 payloads extend the pages: vLLM PR #41160 report, "风险与影响",
+ * notes that the LSE pack dimension rejects fp8 (ValueError); here an fp32
+ * LSE word occupies four one-byte elements (lpd = 4).
  * base codes: 0 = e, 1 = 2.
  */
 #include <math.h>
@@ -60,6 +63,7 @@
 #define ORACLE_F16 1
 #define ORACLE_BF16 2
 #define ORACLE_F64 3
+#define ORACLE_FP8 4
 #define ORACLE_BASE_E 0
 #define ORACLE_BASE_2 1
 #define ORACLE_SANITIZE_O 1u
@@ -68,7 +72,7 @@
 static double ln2(void) { return log(2.0); }
 
 static int elem_bytes(int dtype) {
-    return dtype == ORACLE_F64 ? 8 : dtype == ORACLE_F32 ? 4 : 2;
+    return dtype == ORACLE_F64 ? 8 : dtype == ORACLE_F32 ? 4 : dtype == ORACLE_FP8 ? 1 : 2;
 }
 
 /* ---- element decoding (IEEE binary16 / bfloat16 / binary32 -> double) ---- */
@@ -84,6 +88,23 @@ static double decode_f16(uint16_t h) {
         v = man ? NAN : INFINITY;
     } else {
         v = ldexp((double)(man + 1024), ex - 25); /* (1.man) * 2^(ex-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* fp8 e4m3 ("fn" variant: no infinities): 1 sign, 4 exponent bits (bias 7),
+ * 3 mantissa bits; exponent and mantissa all ones is NaN. */
+static double decode_fp8_e4m3(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int ex = (b >> 3) & 0xf;
+    int man = b & 0x7;
+    double v;
+    if (ex == 15 && man == 7) {
+        v = NAN;
+    } else if (ex == 0) {
+        v = ldexp((double)man, -9); /* subnormal: man * 2^-9 */
+    } else {
+        v = ldexp((double)(man + 8), ex - 10); /* (1.man) * 2^(ex-7) */
     }
     return sign ? -v : v;
 }
@@ -107,6 +128,7 @@ static double load_elem(const void* base, int dtype, int64_t idx) {
         memcpy(&f, p, 4);
         return (double)f;
     }
+    if (dtype == ORACLE_FP8) return decode_fp8_e4m3(*p);
     uint16_t h;
     memcpy(&h, p, 2);
     return dtype == ORACLE_F16 ? decode_f16(h) : decode_bf16(h);
@@ -122,6 +144,7 @@ double oracle_decode_elem(int dtype, const void* base, int64_t idx) {
 int oracle_lse_pack_dim(int dtype) {
     if (dtype == ORACLE_F32) return 1;
     if (dtype == ORACLE_F16 || dtype == ORACLE_BF16) return 2;
+    if (dtype == ORACLE_FP8) return 4; /* extension: four one-byte elements per word */
     return -1;
 }
 

@@ -29,6 +29,8 @@ def rand_bits(rng, shape, dtype):
     """Random payload bit patterns (any bits, NaN payloads included)."""
     if dtype == "f32":
         return rng.integers(0, 2**32, size=shape, dtype=np.uint32).view(np.float32)
+    if dtype == "fp8":
+        return rng.integers(0, 2**8, size=shape, dtype=np.uint8)
     bits = rng.integers(0, 2**16, size=shape, dtype=np.uint16)
     return bits.view(np.float16) if dtype == "f16" else bits
 
@@ -61,13 +63,26 @@ def test_bf16_decoder_matches_torch_on_every_bit_pattern():
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
 
 
+def test_fp8_e4m3_decoder_matches_torch_on_every_bit_pattern():
+    bits = np.arange(256, dtype=np.uint32).astype(np.uint8)
+    got = oracle.decode("fp8", bits)
+    want = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(want)
+    assert nan.sum() == 2  # 0x7f and 0xff; e4m3fn has no infinities
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
 def test_lse_pack_dim():
-    # vLLM #41160, "实现拆解" item 2: fp16 -> 2, fp32 -> 1, anything else rejected;
-    # bf16 is the other 16-bit output type and takes 2 as well.
+    # vLLM #41160, "实现拆解" item 2: fp16 -> 2, fp32 -> 1; bf16 is the other
+    # 16-bit output type and takes 2 as well.  The page notes that fp8 is
+    # rejected there; this library extends it: an fp32 word is four fp8 elements.
     assert oracle.lse_pack_dim("f32") == 1
     assert oracle.lse_pack_dim("f16") == 2
     assert oracle.lse_pack_dim("bf16") == 2
-    assert oracle.lse_pack_dim("fp8") == -1
+    assert oracle.lse_pack_dim("fp8") == 4
+    assert oracle.lse_pack_dim("int4") == -1
 
 
 # --------------------------------------------------------------------------
@@ -95,7 +110,7 @@ def test_pack_peer_inside_matches_page_layout(sentinel):
         assert np.array_equal(stats[..., 1], np.full_like(stats[..., 1], sentinel))
 
 
-@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "fp8"])
 @pytest.mark.parametrize("pad", [0, 3])
 def test_pack_peer_major_interleaved_bytes(dtype, pad):
     """sglang #34651 "实现拆解" item 2 / vLLM #41160: send buffer [N,B,Hpr,D+lpd];
@@ -103,8 +118,8 @@ def test_pack_peer_major_interleaved_bytes(dtype, pad):
     elements per row, the padding must keep its sentinel bytes."""
     rng = np.random.default_rng(2)
     lpd = oracle.lse_pack_dim(dtype)
-    e = 4 if dtype == "f32" else 2
-    for N, B, H, D in [(2, 4, 16, 128), (4, 3, 8, 6), (1, 2, 4, 8), (8, 2, 8, 64)]:
+    e = {"f32": 4, "fp8": 1}.get(dtype, 2)
+    for N, B, H, D in [(2, 4, 16, 128), (4, 3, 8, 12), (1, 2, 4, 8), (8, 2, 8, 64)]:
         Hpr = H // N
         out = rand_bits(rng, (B, H, D), dtype)
         lse = rand_bits(rng, (B, H), "f32")
@@ -413,7 +428,7 @@ def test_merged_split_attention_equals_unsplit_attention(base):
 # fused unpack + combine over the interleaved receive rows
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "fp8"])
 def test_unpack_combine_equals_combine_on_separated_views(dtype):
     rng = np.random.default_rng(14)
     lpd = oracle.lse_pack_dim(dtype)
@@ -421,6 +436,9 @@ def test_unpack_combine_equals_combine_on_separated_views(dtype):
     if dtype == "bf16":
         vals = torch.randn(G, N, B, Hpr, D, dtype=torch.bfloat16)
         payload = vals.view(torch.int16).numpy().view(np.uint16)
+    elif dtype == "fp8":
+        vals = torch.randn(G, N, B, Hpr, D).to(torch.float8_e4m3fn)
+        payload = vals.view(torch.uint8).numpy()
     else:
         payload = rng.standard_normal((G, N, B, Hpr, D)).astype(np.float16 if dtype == "f16" else np.float32)
     lse = rng.uniform(-3, 9, size=(G, N, B, Hpr)).astype(np.float32)
