@@ -14,7 +14,9 @@ kernel reads its inputs from HBM.
 Also measured in the same run and reported under "secondary": the in-place
 sanitising combine of the cached-extend workload (N = 8, 16384 tokens, 96
 heads, D = 512, fp32; 29 GB per call), the largest long-context sweep point
-through the fused unpack+combine (N = 8, B = 256, H = 64, D = 512, fp16), and
+through the fused unpack+combine (N = 8, B = 256, H = 64, D = 512, fp16), the
+MLA decode shape with fp8 e4m3 payloads through the interleaved pack (lpd = 4)
+and the fused unpack+combine, and
 the decode attention that produces the merge's inputs (N = 4 ranks, B = 64
 requests, H = 32, D = 128, bf16, lengths up to 16384; ~9 GB of K/V).
 
@@ -345,13 +347,27 @@ def setup_decode_attention(device, split_tokens=1024, batch=None):
 
 
 def setup_sweep_max(device):
-    import torch
-
-    from decode_context_attention_gb300 import binding, layouts
-    from decode_context_attention_gb300.workloads import generate, sweep_points
+    from decode_context_attention_gb300.workloads import sweep_points
 
     w = [p for p in sweep_points() if p.layout == "peer_major" and p.N == 8 and p.B == 256
          and p.D == 512][0]
+    return setup_peer_major(w, device)
+
+
+def setup_mla_fp8(device):
+    from decode_context_attention_gb300.workloads import WORKLOADS
+
+    return setup_peer_major(WORKLOADS["mla_decode_fp8"], device)
+
+
+def setup_peer_major(w, device):
+    """Interleaved pack of every source rank, then the fused unpack+combine of
+    every destination over the exchanged rows (a view of the send stack)."""
+    import torch
+
+    from decode_context_attention_gb300 import binding, layouts
+    from decode_context_attention_gb300.workloads import generate
+
     d = generate(w, device)
     S, B, H, D = d["o"].shape
     N, H_pr = w.N, w.H_pr
@@ -364,9 +380,9 @@ def setup_sweep_max(device):
     pack = binding.prepare_pack_send(d["o"], d["lse"], pay, words)
     fused = binding.prepare_unpack_combine(recv, D, out, out_lse, base=w.base)
     e = d["o"].element_size()
-    return {"w": w, "launches": [pack, fused], "keep": (d, send, out, out_lse),
-            "names": ["dcp_pack_send (peer-major interleaved, G=8)",
-                      "dcp_unpack_combine (interleaved recv, G=8)"],
+    return {"w": w, "launches": [pack, fused], "keep": (d, send, out, out_lse), "d": d, "send": send,
+            "names": [f"dcp_pack_send (peer-major interleaved, G={S})",
+                      f"dcp_unpack_combine (interleaved recv, G={N})"],
             "bytes": [bytes_pack(S, B, H, D, e), bytes_merge(N, S, B, H_pr, D, e)]}
 
 
@@ -461,6 +477,45 @@ def time_oracle_cached_extend(budget_s: float):
     return el / n * (w.B / small.B) * 1e6, el, n
 
 
+def host_payload(t):
+    """Contiguous host copy of a payload tensor in the oracle's representation."""
+    import numpy as np
+    import torch
+
+    t = t.detach().contiguous().cpu()
+    if t.element_size() == 1:
+        return t.view(torch.uint8).numpy()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def time_oracle_peer_major(pm, budget_s: float):
+    """Oracle µs per call of a peer-major workload: one source's interleaved
+    pack and one destination's fused unpack+combine (1/N of a call each),
+    repeated, scaled to a whole call."""
+    import numpy as np
+
+    import oracle
+
+    w = pm["w"]
+    o0 = host_payload(pm["d"]["o"][0])
+    l0 = pm["d"]["lse"][0].cpu().numpy()
+    recv0 = host_payload(pm["send"][:, 0])          # destination 0's rows from every source
+    N, B, H_pr, D = w.N, w.B, w.H_pr, w.D
+    lpd = 4 // pm["d"]["o"].element_size()
+    dst = np.empty((1, N, B, H_pr, D + lpd), dtype=o0.dtype)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.pack(w.dtype, N, o0[None], l0[None], dst[..., :D], dst.view(np.float32)[..., D // lpd])
+        oracle.unpack_combine(w.dtype, recv0[None], D, base=w.base)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return el / (n / N) * 1e6, el, n
+
+
 def time_oracle(mla, budget_s: float):
     """Oracle µs per full call, extrapolated from repeated 1/8-call samples."""
     w, o0, l0, po, st = oracle_sample_inputs(mla)
@@ -501,6 +556,7 @@ def run_gpu(args):
         # a short run of one workload (for profiler captures); prints nothing
         wl = {"mla_decode": lambda: setup_mla_decode(device),
               "sweep": lambda: setup_sweep_max(device),
+              "mla_decode_fp8": lambda: setup_mla_fp8(device),
               "decode_attention": lambda: setup_decode_attention(device, batch=args.att_batch),
               "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens)}[args.only]()
         time_sequence(wl["launches"], args.steps, args.warmup,
@@ -522,12 +578,21 @@ def run_gpu(args):
     # --- secondary workloads (same run) ----------------------------------------
     secondary = []
     if not args.no_secondary:
-        sw = setup_sweep_max(device)
-        p2, _ = time_sequence(sw["launches"], max(20, args.steps // 10), args.warmup, flush, device)
-        secondary.append({"workload": sw["w"].name,
-                          "kernels": [kernel_record(n, p, b, peak)
-                                      for n, p, b in zip(sw["names"], p2, sw["bytes"])]})
-        del sw
+        for setup in (setup_sweep_max, setup_mla_fp8):
+            sw = setup(device)
+            p2, _ = time_sequence(sw["launches"], max(20, args.steps // 10), args.warmup, flush, device)
+            w2 = sw["w"]
+            rec = {"workload": f"{w2.name} N={w2.N} B={w2.B} H={w2.H} D={w2.D} {w2.dtype} base-{w2.base}, "
+                               "peer-major pack + fused unpack+combine",
+                   "kernels": [kernel_record(n, p, b, peak)
+                               for n, p, b in zip(sw["names"], p2, sw["bytes"])]}
+            if rank == 0 and not args.no_cpu_baseline:
+                us, el, n = time_oracle_peer_major(sw, min(5.0, args.cpu_budget))
+                rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": 1,
+                                     "sample": f"{n} x (one source's pack + one destination's "
+                                               f"unpack+combine = 1/{w2.N} of a call), {el:.1f} s"}
+            secondary.append(rec)
+            del sw
         at = setup_decode_attention(device)
         p4, _ = time_sequence(at["launches"], max(10, args.steps // 20), 3, flush, device)
         rec = {"workload": "mha_decode_attention (the step before the merge)",
@@ -703,7 +768,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["mla_decode", "sweep", "cached_extend", "decode_attention"],
+    ap.add_argument("--only", choices=["mla_decode", "sweep", "mla_decode_fp8", "cached_extend",
+                                       "decode_attention"],
                     help="run just this workload's launches (profiling); no JSON line")
     ap.add_argument("--att-batch", type=int, default=None,
                     help="requests of the decode-attention workload under --only (default 64)")

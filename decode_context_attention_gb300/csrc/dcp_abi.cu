@@ -76,6 +76,7 @@ int elem_size(int dtype) {
         case DCP_F32: return 4;
         case DCP_F16:
         case DCP_BF16: return 2;
+        case DCP_FP8_E4M3: return 1;
         default: return 0;
     }
 }
@@ -158,6 +159,12 @@ int pick_vb(int row_bytes, int align_a, int align_b, int e) {
     return e == 2 ? 2 : 4;
 }
 
+// fp8 rows are moved in 4- or 16-byte vectors only: the row length and every
+// row start must be multiples of 4 bytes (one e4m3 element is one byte).
+bool fp8_rows_ok(int e, int D, int align_a, int align_b) {
+    return e != 1 || (D % 4 == 0 && align_a >= 4 && align_b >= 4);
+}
+
 int lanes_per_row(int vectors) {
     int l = 1;
     while (l < vectors && l < 32) l <<= 1;
@@ -190,7 +197,7 @@ const char* dcp_status_string(int status) {
     switch (status) {
         case DCP_OK: return "success";
         case DCP_ERR_INVALID_ARG: return "invalid argument";
-        case DCP_ERR_UNSUPPORTED_DTYPE: return "unsupported payload dtype (f32, f16 and bf16 only)";
+        case DCP_ERR_UNSUPPORTED_DTYPE: return "unsupported payload dtype (f32, f16, bf16 and fp8 e4m3 only)";
         case DCP_ERR_HEADS_NOT_DIVISIBLE: return "number of heads is not a multiple of the rank count";
         case DCP_ERR_MISALIGNED: return "misaligned pointer, stride or head dim";
         case DCP_ERR_ALIAS: return "an output overlaps an input or itself";
@@ -229,6 +236,8 @@ dcp_status_t dcp_pack_send(int dtype, int N, int B, int H, int D, int G,
     View vdl = View(dst_lse, 4).dim(G, dl_sg * 4).dim(N, dl_sn * 4).dim(B, dl_sb * 4).dim(H_pr, dl_sh * 4);
     if (overlap(vdo, vo) || overlap(vdo, vl) || overlap(vdl, vo) || overlap(vdl, vl))
         return fail(DCP_ERR_ALIAS, "dcp_pack_send: destination overlaps the source");
+    if (!fp8_rows_ok(e, D, vo.align(), vdo.align()))
+        return fail(DCP_ERR_MISALIGNED, "dcp_pack_send: fp8 rows need D %% 4 == 0 and 4-byte aligned row starts");
     if (!vdo.rows_disjoint() || !vdl.rows_disjoint())
         return fail(DCP_ERR_ALIAS, "dcp_pack_send: destination rows overlap one another");
     if (overlap(vdo, vdl)) {
@@ -303,7 +312,8 @@ static dcp_status_t run_merge(const char* who, int dtype, int e, int N, int B, i
     switch (dtype) {
         case DCP_F32: err = dcp::launch_combine_f32(p, vb, stream); break;
         case DCP_F16: err = dcp::launch_combine_f16(p, vb, stream); break;
-        default: err = dcp::launch_combine_bf16(p, vb, stream); break;
+        case DCP_BF16: err = dcp::launch_combine_bf16(p, vb, stream); break;
+        default: err = dcp::launch_combine_fp8(p, vb, stream); break;
     }
     return launched(err, who);
 }
@@ -346,6 +356,8 @@ dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
     } else if (overlap(vu, vo)) {
         return fail(DCP_ERR_ALIAS, "%s: out overlaps o (use DCP_INPLACE_RANK0 for in place)", who);
     }
+    if (!fp8_rows_ok(e, D, vo.align(), vu.align()))
+        return fail(DCP_ERR_MISALIGNED, "%s: fp8 rows need D %% 4 == 0 and 4-byte aligned row starts", who);
     if (overlap(vu, vl)) return fail(DCP_ERR_ALIAS, "%s: out overlaps lse", who);
     if (!vu.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out rows overlap one another", who);
     if (return_lse) {
@@ -389,6 +401,8 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
     if (vr.align() < 4)
         return fail(DCP_ERR_MISALIGNED, "%s: receive rows must start on 4-byte boundaries", who);
     View vu = View(out, rb).dim(G, u_sg * e).dim(B, u_sb * e).dim(Hpr, u_sh * e);
+    if (!fp8_rows_ok(e, D, vr.align(), vu.align()))
+        return fail(DCP_ERR_MISALIGNED, "%s: fp8 rows need 4-byte aligned row starts", who);
     if (overlap(vu, vr)) return fail(DCP_ERR_ALIAS, "%s: out overlaps recv", who);
     if (!vu.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out rows overlap one another", who);
     if (return_lse) {

@@ -37,11 +37,15 @@
 #include "dcp_device.cuh"
 
 // Tuning knobs (compile-time): use the fixed-shape merge for the common row
+// lengths; use the shifted-chunk merge for 4-byte-aligned rows of those
 // lengths; use the cp.async-staged merge where it applies (off: measured
 // slower than the register variants on GB300), its pipeline depth (rows) and
 // warps per CTA.
 #ifndef DCP_COMBINE_FIXED
 #define DCP_COMBINE_FIXED 1
+#endif
+#ifndef DCP_COMBINE_SHIFTED
+#define DCP_COMBINE_SHIFTED 1
 #endif
 #ifndef DCP_COMBINE_STAGED
 #define DCP_COMBINE_STAGED 0
@@ -209,8 +213,11 @@ template <typename T, int VB, int NR, int LPR, int VPL, bool SAN>
 __global__ void __launch_bounds__(kThreads, 2) combine_fixed_kernel(const CombineParams p) {
     constexpr int NP = VB / (int)sizeof(T) / 2;  // fp32 pairs per vector
     // vectors per lane per rank loaded at once: <= 64 registers of payload
+    // and <= 64 registers of packed fp32 accumulators
     constexpr int WPV = VB / 4;
-    constexpr int VCH0 = 64 / (NR * WPV) > 0 ? 64 / (NR * WPV) : 1;
+    constexpr int VCH_LD = 64 / (NR * WPV) > 0 ? 64 / (NR * WPV) : 1;
+    constexpr int VCH_ACC = 32 / NP > 0 ? 32 / NP : 1;
+    constexpr int VCH0 = VCH_LD < VCH_ACC ? VCH_LD : VCH_ACC;
     constexpr int VCH = VCH0 >= VPL ? VPL : VCH0;
     static_assert(VPL % VCH == 0, "chunks must tile the row");
     using V = typename VecT<VB>::type;
@@ -276,12 +283,144 @@ __global__ void __launch_bounds__(kThreads, 2) combine_fixed_kernel(const Combin
     }
 }
 
+// ---------------------------------------------------------------------------
+// Shifted-chunk variant for payload rows that start on a 4-byte but not a
+// 16-byte boundary (the interleaved receive rows, D*e + 4 bytes apart) when
+// every rank's row of an output row has the same misalignment (rank stride a
+// multiple of 16 bytes).  The lanes read the 16-byte-aligned chunks that cover
+// the row -- the same chunk positions in every rank, so word k of a chunk is
+// the same payload word in all of them -- merge them word by word and store
+// each word at its place in the (4-byte-aligned) output row.  Chunk 0 starts
+// up to 12 bytes before the row (those words are read, never used or
+// written); the up to 3 payload words past the last whole chunk are merged by
+// the first lanes from 4-byte loads.  Reads stay inside the aligned 16-byte
+// granules that hold the row, so they never leave its pages.
+// ---------------------------------------------------------------------------
+template <typename T, int NR, int LPR, int VPL, bool SAN>
+__global__ void __launch_bounds__(kThreads, 2) combine_shifted_kernel(const CombineParams p) {
+    constexpr int NP = 16 / (int)sizeof(T) / 2;  // fp32 pairs per chunk
+    constexpr int EPW = 4 / (int)sizeof(T);      // elements per word
+    constexpr int RB = LPR * VPL * 16;           // payload bytes of a row
+    constexpr int VCH_LD = 64 / (NR * 4) > 0 ? 64 / (NR * 4) : 1;
+    constexpr int VCH_ACC = 32 / NP > 0 ? 32 / NP : 1;
+    constexpr int VCH0 = VCH_LD < VCH_ACC ? VCH_LD : VCH_ACC;
+    constexpr int VCH = VCH0 >= VPL ? VPL : VCH0;
+    static_assert(VPL % VCH == 0, "chunks must tile the row");
+
+    const int lane = threadIdx.x & 31;
+    LaneGroup lg;
+    lg.jl = lane & (LPR - 1);
+    lg.sub = lane / LPR;
+    lg.mask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lg.sub * LPR));
+    const int64_t wpc = blockDim.x / 32;
+    lg.first = ((int64_t)blockIdx.x * wpc + (threadIdx.x / 32)) * (32 / LPR) + lg.sub;
+    lg.step = (int64_t)gridDim.x * wpc * (32 / LPR);
+
+    const bool b2 = p.base2 != 0;
+    const int N = p.N;
+    RowStep st;
+    st.set(lg.step, p.B, p.Hc);
+    RowCursor c;
+    c.set(lg.first, p.B, p.Hc);
+    for (int64_t row = lg.first; row < p.rows; row += lg.step, c.add(st.dg, st.db, st.dh, p.B, p.Hc)) {
+        const float* lrow = p.lse + c.g * p.l_sg + (int64_t)c.b * p.l_sb + (int64_t)c.h * p.l_sh;
+        const unsigned char* o0 = p.o + c.g * p.o_sg + (int64_t)c.b * p.o_sb + (int64_t)c.h * p.o_sh;
+        unsigned char* urow = p.out + c.g * p.u_sg + (int64_t)c.b * p.u_sb + (int64_t)c.h * p.u_sh;
+        const int skip = (int)((uintptr_t)o0 & 15u) >> 2;   // words of chunk 0 before the row
+        const unsigned char* oal = o0 - 4 * skip + lg.jl * 16;
+        const float l = lg.jl < N ? __ldg(lrow + (int64_t)lg.jl * p.l_sn) : -INFINITY;
+        // payload words past the last whole chunk: lanes 0 .. skip-1, one word each
+        const bool tail = lg.jl < skip;
+        unsigned xt[NR];
+#pragma unroll
+        for (int j = 0; j < NR; ++j)
+            if (j < N && tail) xt[j] = ld_stream<4>(o0 + (RB - 4 * skip) + 4 * lg.jl + (int64_t)j * p.o_sn);
+        unsigned long long w2[NR];
+        float Gl = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < VPL; c0 += VCH) {
+            uint4 x[NR][VCH];
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+                if (j < N) {
+                    const unsigned char* rp = oal + (int64_t)j * p.o_sn;
+#pragma unroll
+                    for (int q = 0; q < VCH; ++q) x[j][q] = ld_stream<16>(rp + (c0 + q) * LPR * 16);
+                }
+            if (c0 == 0) {
+                const float wl = group_weight(l, lg, LPR, b2, Gl);
+#pragma unroll
+                for (int j = 0; j < NR; ++j) {
+                    const float wj = __shfl_sync(lg.mask, wl, j & (LPR - 1), LPR);
+                    w2[j] = pack2f(wj, wj);
+                }
+            }
+            unsigned long long acc[VCH][NP];
+#pragma unroll
+            for (int q = 0; q < VCH; ++q)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) acc[q][i] = 0ull;
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+                if (j < N)
+#pragma unroll
+                    for (int q = 0; q < VCH; ++q) fma_pairs<T, 16, SAN>(acc[q], x[j][q], w2[j]);
+#pragma unroll
+            for (int q = 0; q < VCH; ++q) {
+                const uint4 v = round_pairs<T, 16>(acc[q]);
+                const unsigned wd[4] = {v.x, v.y, v.z, v.w};
+                const int p0 = ((c0 + q) * LPR + lg.jl) * 4 - skip;   // output word of wd[0]
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (p0 + k >= 0) st_vec<4>(urow + 4 * (p0 + k), wd[k]);
+            }
+        }
+        if (tail) {
+            float at[EPW];
+#pragma unroll
+            for (int i = 0; i < EPW; ++i) at[i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+                if (j < N) fma_vec<T, 4, SAN>(at, xt[j], unpack2(w2[j]).x);
+            st_vec<4>(urow + (RB - 4 * skip) + 4 * lg.jl, round_vec<T, 4>(at));
+        }
+        if (p.return_lse && lg.jl == 0)
+            p.out_lse[c.g * p.ul_sg + (int64_t)c.b * p.ul_sb + (int64_t)c.h * p.ul_sh] = Gl;
+    }
+}
+
+// Shifted-chunk kernel for (T, NR) and this row length, or nullptr.
+// Not for fp8: its rows are half as long in bytes, and the word-wise stores
+// and the per-word tail cost more than the 4-byte loads they replace
+// (measured 25.5 vs 22.1 us for the fp8 MLA-decode unpack+combine).
+template <typename T, int NR, bool SAN>
+const void* pick_shifted(int row_bytes, int& lpr) {
+    if constexpr (sizeof(T) == 1) {
+        return nullptr;
+    } else {
+        if (row_bytes == 128 && NR <= 8) { lpr = 8; return (const void*)combine_shifted_kernel<T, NR, 8, 1, SAN>; }
+        if (row_bytes == 256) { lpr = 16; return (const void*)combine_shifted_kernel<T, NR, 16, 1, SAN>; }
+        if (row_bytes == 512) { lpr = 32; return (const void*)combine_shifted_kernel<T, NR, 32, 1, SAN>; }
+        if (row_bytes == 1024) { lpr = 32; return (const void*)combine_shifted_kernel<T, NR, 32, 2, SAN>; }
+        if (row_bytes == 2048) { lpr = 32; return (const void*)combine_shifted_kernel<T, NR, 32, 4, SAN>; }
+        return nullptr;
+    }
+}
+
 // Fixed-shape kernel for (T, VB, NR) and this row length, or nullptr.
 template <typename T, int VB, int NR, bool SAN>
 const void* pick_fixed(int row_bytes, int& lpr) {
     if constexpr (VB < 4 || (VB == 4 && sizeof(T) == 4)) {
         return nullptr;  // one element per vector: no pairs
     } else {
+        if constexpr (sizeof(T) == 1) {
+            // fp8 rows of 256 / 512 bytes: 32 bytes per lane and rank (as a
+            // 16-bit row of the same D gets), so 4 or 2 rows share a warp and
+            // twice the bytes are in flight per lane than at one vector
+            constexpr int V32 = 32 / VB;
+            if (row_bytes == 8 * 32 && NR <= 8) { lpr = 8; return (const void*)combine_fixed_kernel<T, VB, NR, 8, V32, SAN>; }
+            if (row_bytes == 16 * 32) { lpr = 16; return (const void*)combine_fixed_kernel<T, VB, NR, 16, V32, SAN>; }
+        }
         if (row_bytes == 8 * VB && NR <= 8) { lpr = 8; return (const void*)combine_fixed_kernel<T, VB, NR, 8, 1, SAN>; }
         if (row_bytes == 16 * VB) { lpr = 16; return (const void*)combine_fixed_kernel<T, VB, NR, 16, 1, SAN>; }
         if (row_bytes == 32 * VB) { lpr = 32; return (const void*)combine_fixed_kernel<T, VB, NR, 32, 1, SAN>; }
@@ -499,6 +638,23 @@ template <typename T, int VB, bool SAN>
 cudaError_t launch_combine_vb(const CombineParams& p, cudaStream_t stream) {
     void* args[] = {(void*)&p};
 #if DCP_COMBINE_FIXED
+    if constexpr (VB == 4 && DCP_COMBINE_SHIFTED) {
+        // 4-byte-aligned rows whose ranks share one misalignment: 16-byte chunks
+        const int rb = p.vec_per_row * VB;
+        if (p.N <= 8 && p.o_sn % 16 == 0 && p.out != (unsigned char*)p.o) {
+            int lpr = 0;
+            const void* k = p.N <= 2 ? pick_shifted<T, 2, SAN>(rb, lpr)
+                          : p.N <= 4 ? pick_shifted<T, 4, SAN>(rb, lpr)
+                                     : pick_shifted<T, 8, SAN>(rb, lpr);
+            if (k && p.N <= lpr) {
+                CombineParams q = p;
+                q.lpr = lpr;
+                void* qargs[] = {(void*)&q};
+                const int grid = persistent_grid(k, p.rows, (kThreads / 32) * (32 / lpr), kThreads, 0);
+                return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), qargs, 0, stream);
+            }
+        }
+    }
     if (p.N <= 8) {
         int lpr = 0;
         const int rb = p.vec_per_row * VB;

@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -130,8 +131,22 @@ __device__ __forceinline__ unsigned long long sanitize_pair(unsigned long long x
     return pack2f(f.x, f.y);
 }
 
+// Two fp8 e4m3 elements (16 bits, low byte first) <-> an fp32 pair.  Widening
+// goes through the hardware e4m3x2 -> f16x2 convert (exact); narrowing
+// rounds to nearest and saturates to the largest finite e4m3 (448).
+__device__ __forceinline__ unsigned long long fp8x2_to_pair(unsigned v) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+    __half2 h;
+    memcpy(&h, &hr, 4);
+    const float2 f = __half22float2(h);
+    return pack2f(f.x, f.y);
+}
+__device__ __forceinline__ unsigned pair_to_fp8x2(float2 f) {
+    return (unsigned)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+}
+
 // acc[0..NP) += w2 * (payload vector x) for a VB-byte vector of T holding
-// 2*NP elements (VB = 16, or VB = 4 with a 16-bit T).
+// 2*NP elements (VB = 16, or VB = 4 with a 16-bit or 8-bit T).
 template <typename T, int VB, bool SAN>
 __device__ __forceinline__ void fma_pairs(unsigned long long (&acc)[VB / sizeof(T) / 2],
                                           const typename VecT<VB>::type& x, unsigned long long w2) {
@@ -142,6 +157,7 @@ __device__ __forceinline__ void fma_pairs(unsigned long long (&acc)[VB / sizeof(
     for (int k = 0; k < NP; ++k) {
         unsigned long long x2;
         if constexpr (sizeof(T) == 4) x2 = pack2(wd[2 * k], wd[2 * k + 1]);
+        else if constexpr (sizeof(T) == 1) x2 = fp8x2_to_pair(wd[k >> 1] >> (16 * (k & 1)));
         else x2 = word_to_pair<T>(wd[k]);
         if (SAN) x2 = sanitize_pair(x2);
         ffma2_acc(acc[k], w2, x2);
@@ -155,6 +171,12 @@ __device__ __forceinline__ typename VecT<VB>::type round_pairs(const unsigned lo
     typename VecT<VB>::type v;
     if constexpr (sizeof(T) == 4) {
         memcpy(&v, acc, VB);
+    } else if constexpr (sizeof(T) == 1) {
+        unsigned wd[VB / 4];
+#pragma unroll
+        for (int k = 0; k < VB / 4; ++k)
+            wd[k] = pair_to_fp8x2(unpack2(acc[2 * k])) | (pair_to_fp8x2(unpack2(acc[2 * k + 1])) << 16);
+        memcpy(&v, wd, VB);
     } else {
         unsigned wd[VB / 4];
 #pragma unroll
@@ -208,6 +230,17 @@ __device__ __forceinline__ void fma_vec(float (&acc)[VB / sizeof(T)], const type
             acc[i + 1] = r.y;
         }
         if constexpr (EPV % 2) acc[EPV - 1] = fmaf(w, SAN ? zero_if_not_finite(f[EPV - 1]) : f[EPV - 1], acc[EPV - 1]);
+    } else if constexpr (sizeof(T) == 1) {
+        unsigned wd[VB / 4];
+        memcpy(wd, &x, VB);
+#pragma unroll
+        for (int k = 0; k < EPV / 2; ++k) {
+            float2 xf = unpack2(fp8x2_to_pair(wd[k >> 1] >> (16 * (k & 1))));
+            if (SAN) xf = make_float2(zero_if_not_finite(xf.x), zero_if_not_finite(xf.y));
+            const float2 r = ffma2(w, xf, make_float2(acc[2 * k], acc[2 * k + 1]));
+            acc[2 * k] = r.x;
+            acc[2 * k + 1] = r.y;
+        }
     } else if constexpr (VB >= 4) {
         unsigned wd[VB / 4];
         memcpy(wd, &x, VB);
@@ -233,6 +266,13 @@ __device__ __forceinline__ typename VecT<VB>::type round_vec(const float (&acc)[
     typename VecT<VB>::type v;
     if constexpr (sizeof(T) == 4) {
         memcpy(&v, acc, VB);
+    } else if constexpr (sizeof(T) == 1) {
+        unsigned wd[VB / 4];
+#pragma unroll
+        for (int k = 0; k < VB / 4; ++k)
+            wd[k] = pair_to_fp8x2(make_float2(acc[4 * k], acc[4 * k + 1])) |
+                    (pair_to_fp8x2(make_float2(acc[4 * k + 2], acc[4 * k + 3])) << 16);
+        memcpy(&v, wd, VB);
     } else if constexpr (VB >= 4) {
         unsigned wd[VB / 4];
 #pragma unroll

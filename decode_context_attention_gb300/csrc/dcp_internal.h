@@ -83,6 +83,7 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_combine_f32(const CombineParams& p, int vb, cudaStream_t stream);
 cudaError_t launch_combine_f16(const CombineParams& p, int vb, cudaStream_t stream);
 cudaError_t launch_combine_bf16(const CombineParams& p, int vb, cudaStream_t stream);
+cudaError_t launch_combine_fp8(const CombineParams& p, int vb, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -27,11 +27,11 @@ import torch
 
 
 def lse_pack_dim(dtype: torch.dtype) -> int:
-    """Payload elements one fp32 word occupies: 1 for fp32, 2 for 16-bit types."""
-    e = torch.empty((), dtype=dtype).element_size()
-    if e not in (2, 4):
+    """Payload elements one fp32 word occupies: 1 for fp32, 2 for 16-bit types,
+    4 for fp8 e4m3."""
+    if dtype not in (torch.float32, torch.float16, torch.bfloat16, torch.float8_e4m3fn):
         raise ValueError(f"no interleaved layout for {dtype}")
-    return 4 // e
+    return 4 // torch.empty((), dtype=dtype).element_size()
 
 
 # ---- peer-major interleaved ----------------------------------------------------

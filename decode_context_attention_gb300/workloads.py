@@ -22,6 +22,10 @@ cached-extend cases; no model weights or datasets are involved):
                  base-e LSE l_r = c + s*u_r with c ~ U(0,12), s ~ U(0,40) per
                  (token, head) and u_r ~ U(0,1) per rank (max - min up to 40);
                  both pack layouts (48 points).
+  mla_decode_fp8 the MLA decode shape (N=8, B=128, H=128, D=512) with fp8 e4m3
+                 O (N(0,1) drawn in fp32, rounded to e4m3), LSE ~ U(0,20) base 2,
+                 peer-major interleaved rows (lpd = 4).  Pack + fused
+                 unpack+combine.
   cached_extend  N=8, T=16384, H=96, D=512, fp32 O ~ N(0,1) (3 GiB per rank),
                  LSE ~ U(0,15) base e; round(1e-4 * numel) positions of O and of
                  the LSE, drawn uniformly with replacement, are set to NaN, +inf
@@ -44,7 +48,8 @@ from dataclasses import dataclass, replace
 
 import torch
 
-TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+                "fp8": torch.float8_e4m3fn}
 
 
 @dataclass(frozen=True)
@@ -54,7 +59,7 @@ class Workload:
     B: int          # tokens (decode batch, or cached-extend tokens T)
     H: int          # query heads
     D: int          # head dim of O (v_head_dim or kv_lora_rank)
-    dtype: str      # payload type of O: "f32" | "f16" | "bf16"
+    dtype: str      # payload type of O: "f32" | "f16" | "bf16" | "fp8"
     base: str       # LSE base: "e" | "2"
     layout: str     # "peer_major" | "peer_inside" | "inplace"
     kind: str       # value recipe, one of the module docstring's workloads
@@ -69,6 +74,7 @@ WORKLOADS = {
     "tiny": Workload("tiny", 2, 4, 16, 128, "f32", "e", "peer_major", "tiny", 0),
     "mha_decode": Workload("mha_decode", 4, 64, 32, 128, "bf16", "e", "peer_major", "mha_decode", 1),
     "mla_decode": Workload("mla_decode", 8, 128, 128, 512, "bf16", "2", "peer_inside", "mla_decode", 2),
+    "mla_decode_fp8": Workload("mla_decode_fp8", 8, 128, 128, 512, "fp8", "2", "peer_major", "mla_decode", 6),
     "cached_extend": Workload("cached_extend", 8, 16384, 96, 512, "f32", "e", "inplace",
                               "cached_extend", 4),
 }
@@ -100,14 +106,17 @@ def _uniform(shape, lo, hi, g, device):
 def _normal_payload(N, B, H, D, dtype, g, device):
     o = torch.empty((N, B, H, D), dtype=TORCH_DTYPES[dtype], device=device)
     for r in range(N):  # one rank at a time keeps the fp32 temporaries small
-        o[r].normal_(generator=g)
+        if o.element_size() == 1:   # fp8: draw in fp32, round once
+            o[r].copy_(torch.empty((B, H, D), device=device).normal_(generator=g))
+        else:
+            o[r].normal_(generator=g)
     return o
 
 
 def _empty_pairs(mask_nb, o, lse):
     """Apply the neutral (O = 0, LSE = -inf) state to the (rank, token) pairs in mask_nb."""
     idx = mask_nb.nonzero(as_tuple=True)
-    o[idx] = 0
+    o.view(torch.uint8)[idx] = 0    # all-zero bytes are +0 in every payload type
     lse[idx] = float("-inf")
 
 

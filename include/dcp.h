@@ -44,7 +44,19 @@
  * - Outputs must not overlap inputs, except where an entry point says so;
  *   the rows of one output must not overlap one another.
  *
- * Payload types: DCP_F32, DCP_F16, DCP_BF16.  LSE values are always fp32.
+ * Payload types: DCP_F32, DCP_F16, DCP_BF16 and DCP_FP8_E4M3.  LSE values
+ * are always fp32.  Merges accumulate in fp32 whatever the payload type and
+ * round once into the output type.
+ *
+ * DCP_FP8_E4M3 is the OCP e4m3 "fn" byte format (bias 7, no infinities,
+ * S.1111.111 is NaN, largest finite 448).  Its rows are moved in 4- or 16-byte
+ * vectors, so with fp8 payloads D must be a multiple of 4 and every payload
+ * row must start on a 4-byte boundary (DCP_ERR_MISALIGNED otherwise).  Merged
+ * fp8 outputs are rounded to nearest-even, saturating at +-448; NaN stays NaN.
+ * The pages leave fp8 to future work (vLLM PR #41160 report, risk list: the
+ * LSE pack-dim helper rejects fp8 with a ValueError; sglang PR #34213 report,
+ * risk list: the fp32-word reinterpretation needs re-reading once fp8 is
+ * added); the byte layout here is the same rule carried to a 1-byte element.
  */
 #ifndef DCP_GB300_DCP_H_
 #define DCP_GB300_DCP_H_
@@ -59,14 +71,15 @@ extern "C" {
 typedef enum dcp_status {
     DCP_OK = 0,
     DCP_ERR_INVALID_ARG = 1,          /* bad size, NULL pointer, negative stride, bad flag */
-    DCP_ERR_UNSUPPORTED_DTYPE = 2,    /* dtype other than f32 / f16 / bf16 */
+    DCP_ERR_UNSUPPORTED_DTYPE = 2,    /* dtype other than f32 / f16 / bf16 / fp8 e4m3 */
     DCP_ERR_HEADS_NOT_DIVISIBLE = 3,  /* H % N != 0 in the pack */
-    DCP_ERR_MISALIGNED = 4,           /* D % lpd != 0, or a pointer/stride not aligned to its type */
+    DCP_ERR_MISALIGNED = 4,           /* D % lpd != 0, a pointer/stride not aligned to its type,
+                                         or fp8 rows not on 4-byte boundaries */
     DCP_ERR_ALIAS = 5,                /* an output overlaps an input or itself */
     DCP_ERR_CUDA = 6                  /* a CUDA call failed; see dcp_last_error_message() */
 } dcp_status_t;
 
-enum { DCP_F32 = 0, DCP_F16 = 1, DCP_BF16 = 2 };
+enum { DCP_F32 = 0, DCP_F16 = 1, DCP_BF16 = 2, DCP_FP8_E4M3 = 3 };
 enum { DCP_LSE_BASE_E = 0, DCP_LSE_BASE_2 = 1 };
 
 /* Flags of dcp_lse_combine / dcp_unpack_combine. */
@@ -84,9 +97,11 @@ enum {
 
 /*
  * Payload elements one fp32 LSE word occupies in an interleaved row:
- * 1 for DCP_F32, 2 for DCP_F16 and DCP_BF16, -1 for anything else.
- * (vLLM PR #41160 report, "实现拆解" item 2, `_dcp_a2a_lse_pack_dim`:
- * fp16 -> 2, fp32 -> 1, other types rejected; bf16 is the other 16-bit type.)
+ * 1 for DCP_F32, 2 for DCP_F16 and DCP_BF16, 4 for DCP_FP8_E4M3, -1 for
+ * anything else.  (vLLM PR #41160 report, "实现拆解" item 2,
+ * `_dcp_a2a_lse_pack_dim`: fp16 -> 2, fp32 -> 1, other types rejected; bf16
+ * is the other 16-bit type, and fp8 -- which that helper still rejects -- is
+ * given the same 4-bytes-per-word rule.)
  */
 int dcp_lse_pack_dim(int dtype);
 

@@ -10,6 +10,12 @@ Tolerances (written here once, used by every merge comparison):
     <= 2^-9 for bf16, 2^-12 for fp16, doubled for margin) plus fp32
     accumulation error (<= 1e-5 absolute at these magnitudes):
         bf16: |d| <= 4e-3 |oracle| + 1e-5      fp16: |d| <= 5e-4 |oracle| + 1e-5
+  * fp8 e4m3 payload: one round-to-nearest into e4m3 of the fp32 sum, so
+    every element lies within half an e4m3 ulp of the oracle value (ulp =
+    2^(floor(log2|x|) - 3) for |x| >= 2^-6, 2^-9 below), plus the fp32
+    accumulation slack 1e-5 (1 + |oracle|).  The 2e-2 norm-wise bound stated
+    for 16-bit payloads is not applied: one e4m3 rounding alone can reach
+    2^-4 relative.
   * Non-finite oracle values (NaN, +-inf) must be matched exactly by class.
 """
 from __future__ import annotations
@@ -17,16 +23,21 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-NP_PAYLOAD = {torch.float32: np.float32, torch.float16: np.float16, torch.bfloat16: np.uint16}
-ORACLE_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+NP_PAYLOAD = {torch.float32: np.float32, torch.float16: np.float16, torch.bfloat16: np.uint16,
+              torch.float8_e4m3fn: np.uint8}
+ORACLE_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
+             torch.float8_e4m3fn: "fp8"}
 ELEM_REL = {torch.float32: 0.0, torch.float16: 5e-4, torch.bfloat16: 4e-3}
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
-    """Contiguous host copy with the oracle's payload representation (bf16 as uint16)."""
+    """Contiguous host copy with the oracle's payload representation (bf16 as
+    uint16, fp8 as uint8)."""
     t = t.detach().contiguous().cpu()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
     return t.numpy()
 
 
@@ -55,6 +66,13 @@ def _class_mask(want: np.ndarray, got: np.ndarray, what: str) -> np.ndarray:
     return ~(nan_w | inf_w)
 
 
+def e4m3_ulp(a: np.ndarray) -> np.ndarray:
+    """Spacing of e4m3 values around |a|: 2^(e - 3) in the binade [2^e, 2^(e+1)),
+    2^-9 among the subnormals (|a| < 2^-6)."""
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    return np.exp2(e - 3)
+
+
 def assert_merge_close(got: torch.Tensor, want: np.ndarray, what: str = "out") -> dict:
     """Compare a merged payload tensor with the oracle's fp64 result."""
     dt = got.dtype
@@ -65,6 +83,11 @@ def assert_merge_close(got: torch.Tensor, want: np.ndarray, what: str = "out") -
     stats = {"max_abs": float(d.max(initial=0.0)), "n": int(fin.sum())}
     if dt == torch.float32:
         assert stats["max_abs"] <= 1e-5, f"{what}: max abs error {stats['max_abs']:.3e} > 1e-5"
+    elif dt == torch.float8_e4m3fn:
+        bound = 0.5 * e4m3_ulp(w) + 1e-5 * (1.0 + w)
+        bad = d > bound
+        assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond half an e4m3 ulp, "
+                               f"worst excess {float((d - bound).max()):.3e}")
     else:
         scale = max(float(w.max(initial=0.0)), 1e-30)
         stats["rel"] = stats["max_abs"] / scale

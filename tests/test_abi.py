@@ -12,7 +12,7 @@ from decode_context_attention_gb300 import binding, build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "dcp.h")
 
-F32, F16, BF16 = 0, 1, 2
+F32, F16, BF16, FP8 = 0, 1, 2, 3
 # plausible but never dereferenced device addresses
 A = 0x10000000
 Bp = 0x20000000
@@ -46,6 +46,7 @@ def test_lse_pack_dim(lib):
     assert binding.dcp_lse_pack_dim(F32) == 1
     assert binding.dcp_lse_pack_dim(F16) == 2
     assert binding.dcp_lse_pack_dim(BF16) == 2
+    assert binding.dcp_lse_pack_dim(FP8) == 4
     assert binding.dcp_lse_pack_dim(7) == -1
 
 
@@ -119,6 +120,19 @@ def test_unpack_validation(lib):
     assert unpack(B=0) == 0
 
 
+def test_fp8_rows_need_four_byte_granularity(lib):
+    # one e4m3 element is one byte: D % 4 == 0 and 4-byte aligned row starts
+    assert pack(dtype=FP8, D=6, o_s=(48, 24, 6)) == 4
+    assert pack(dtype=FP8) == 4                              # dst rows 10 bytes apart
+    assert pack(dtype=FP8, o=A + 2, d_s=(96, 48, 24, 12)) == 4
+    assert "fp8" in binding.dcp_last_error_message()
+    assert combine(dtype=FP8, D=6, o_s=(96, 48, 24, 6), u_s=(48, 24, 6)) == 4
+    assert combine(dtype=FP8, out=C + 2) == 4
+    assert unpack(dtype=FP8, D=6) == 4                       # D % lpd (lpd = 4)
+    assert unpack(dtype=FP8, r_s=(192, 96, 48, 12), out=C + 1) == 4
+    assert unpack(dtype=FP8, r_s=(160, 80, 40, 10)) == 4     # receive rows off the grid
+
+
 def test_binding_raises_with_message(lib):
     with pytest.raises(binding.DcpError) as ei:
         binding.check(pack(N=3), "dcp_pack_send")
@@ -142,6 +156,7 @@ def test_decode_attention_workspace_size(lib):
 
 def test_decode_attention_validation(lib):
     assert attn(dtype=F32) == 2
+    assert attn(dtype=FP8) == 2
     assert attn(H=6, Hkv=4) == 3
     assert attn(H=6, Hkv=2) == 1               # three query heads per KV head
     assert attn(D=96) == 1

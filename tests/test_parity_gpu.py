@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle, on
-the seeded workloads (tiny, MHA decode, MLA decode, the long-context sweep,
-cached extend), element by element.
+the seeded workloads (tiny, MHA decode, MLA decode in bf16 and fp8, the
+long-context sweep, cached extend), element by element.
 
 Pack / layout outputs: bit-exact over the WHOLE destination allocation (which
 starts filled with the same sentinel bytes on both sides, so a stray write
@@ -93,6 +93,15 @@ def test_mha_decode_strided_combine_on_interleaved_views():
     run_peer_major(WORKLOADS["mha_decode"], fused=False, materialize=False)
 
 
+@pytest.mark.parametrize("materialize", [False, True])
+def test_mla_decode_fp8_pack_and_fused_unpack_combine(materialize):
+    run_peer_major(WORKLOADS["mla_decode_fp8"], fused=True, materialize=materialize)
+
+
+def test_mla_decode_fp8_strided_combine_on_interleaved_views():
+    run_peer_major(WORKLOADS["mla_decode_fp8"], fused=False, materialize=False)
+
+
 # ---------------------------------------------------------------------------
 # peer-inside split: pack + combine over the strided receive views
 # ---------------------------------------------------------------------------
@@ -134,6 +143,12 @@ def run_peer_inside(w, materialize: bool, stats_fill: float = -7777.0):
 @pytest.mark.parametrize("materialize", [False, True])
 def test_mla_decode_peer_inside_pack_and_strided_combine(materialize):
     run_peer_inside(WORKLOADS["mla_decode"], materialize=materialize)
+
+
+@pytest.mark.parametrize("materialize", [False, True])
+def test_mla_decode_fp8_peer_inside_pack_and_strided_combine(materialize):
+    run_peer_inside(scaled(WORKLOADS["mla_decode_fp8"], B=32, layout="peer_inside", seed=61),
+                    materialize=materialize)
 
 
 def test_page_peer_inside_shapes_with_zero_stats():
