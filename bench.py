@@ -11,14 +11,21 @@ the sender stack.  L2 is flushed before every kernel (a 2x-L2 write, then a
 2x-L2 read so no dirty lines are left), outside the timed events, so every
 kernel reads its inputs from HBM.
 
-Also measured in the same run and reported under "secondary": the in-place
-sanitising combine of the cached-extend workload (N = 8, 16384 tokens, 96
-heads, D = 512, fp32; 29 GB per call), the largest long-context sweep point
-through the fused unpack+combine (N = 8, B = 256, H = 64, D = 512, fp16), the
-MLA decode shape with fp8 e4m3 payloads through the interleaved pack (lpd = 4)
-and the fused unpack+combine, and
-the decode attention that produces the merge's inputs (N = 4 ranks, B = 64
-requests, H = 32, D = 128, bf16, lengths up to 16384; ~9 GB of K/V).
+Also measured in the same run and reported under "secondary":
+  * one rank's own calls of the headline workload (G = 1: the pack of one
+    source, the combine of one destination);
+  * the two-collective layout at the largest long-context sweep point (N = 8,
+    B = 256, H = 64, D = 512, fp16): O and LSE packed into separate buffers,
+    combine without a returned LSE;
+  * the same sweep point through the interleaved pack and the fused
+    unpack+combine;
+  * the MLA decode shape with fp8 e4m3 payloads through the interleaved pack
+    (lpd = 4) and the fused unpack+combine;
+  * the decode attention that produces the merge's inputs (N = 4 ranks,
+    B = 64 requests, H = 32, D = 128, bf16, lengths up to 16384; ~9 GB of K/V);
+  * the cached-extend workload (N = 8, 16384 tokens, 96 heads, D = 512, fp32;
+    29 GB per call): the combine writing the per-rank head slices
+    contiguously, then the in-place sanitising combine.
 
 `--impl reference` times the fp64 CPU oracle instead, on a bounded sample of
 the same workload, and reports it in the same unit.
@@ -224,6 +231,31 @@ def kernel_record(name, ms_list, nbytes, peak_gbs):
             "frac_of_measured_hbm": round(gbs / peak_gbs, 4)}
 
 
+def theoretical_hbm_gbs(gpu_index: int):
+    """Nominal DRAM bandwidth from the driver's read-only queries: 2 transfers
+    per memory clock x bus width.  None where NVML is not available."""
+    import ctypes
+
+    try:
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if nvml.nvmlInit_v2() != 0:
+            return None
+        try:
+            dev = ctypes.c_void_p()
+            if nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(dev)) != 0:
+                return None
+            mhz, bits = ctypes.c_uint(), ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(dev, ctypes.c_int(2), ctypes.byref(mhz)) != 0:  # memory clock
+                return None
+            if nvml.nvmlDeviceGetMemoryBusWidth(dev, ctypes.byref(bits)) != 0:
+                return None
+            return round(2 * mhz.value * 1e6 * bits.value / 8 / 1e9, 1)
+        finally:
+            nvml.nvmlShutdown()
+    except (OSError, AttributeError):
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -298,7 +330,7 @@ def setup_mla_decode(device, seed_offset=0):
     }
 
 
-def setup_cached_extend(device, tokens=None):
+def setup_cached_extend(device, tokens=None, slices=False):
     import torch
 
     from decode_context_attention_gb300 import binding
@@ -313,9 +345,22 @@ def setup_cached_extend(device, tokens=None):
     out_lse = torch.empty((T, H), dtype=torch.float32, device=device)
     comb = binding.prepare_lse_combine(o, lse, o[0], out_lse, base=w.base, sanitize=True,
                                        inplace=True)
-    return {"w": w, "launches": [comb], "keep": (o, lse, out_lse),
-            "names": ["dcp_lse_combine (in place, sanitise, fp32)"],
-            "bytes": [bytes_merge(1, N, T, H, D, 4)]}
+    if not slices:
+        return {"w": w, "launches": [comb], "keep": (o, lse, out_lse),
+                "names": ["dcp_lse_combine (in place, sanitise, fp32)"],
+                "bytes": [bytes_merge(1, N, T, H, D, 4)]}
+    # the per-rank head slices [k*H/N, (k+1)*H/N) written contiguously by the
+    # combine itself (group axis = slice), from the same inputs
+    hs = H // N
+    o_k = o.view(N, T, N, hs, D).permute(2, 0, 1, 3, 4)
+    l_k = lse.view(N, T, N, hs).permute(2, 0, 1, 3)
+    sl = torch.empty((N, T, hs, D), dtype=o.dtype, device=device)
+    sl_lse = torch.empty((N, T, hs), dtype=torch.float32, device=device)
+    slc = binding.prepare_lse_combine(o_k, l_k, sl, sl_lse, base=w.base, sanitize=True)
+    return {"w": w, "launches": [slc, comb], "keep": (o, lse, out_lse, sl, sl_lse),
+            "names": ["dcp_lse_combine (contiguous head slices, sanitise, fp32)",
+                      "dcp_lse_combine (in place, sanitise, fp32)"],
+            "bytes": [bytes_merge(1, N, T, H, D, 4)] * 2}
 
 
 def setup_decode_attention(device, split_tokens=1024, batch=None):
@@ -358,6 +403,60 @@ def setup_mla_fp8(device):
     from decode_context_attention_gb300.workloads import WORKLOADS
 
     return setup_peer_major(WORKLOADS["mla_decode_fp8"], device)
+
+
+def setup_two_collective(device):
+    """The legacy two-collective layout at the largest sweep point: O and LSE
+    packed into separate peer-major buffers (one all-to-all each), then the
+    combine over the exchanged views without a returned LSE."""
+    import torch
+
+    from decode_context_attention_gb300 import binding
+    from decode_context_attention_gb300.workloads import generate, sweep_points
+
+    w = [p for p in sweep_points() if p.layout == "peer_major" and p.N == 8 and p.B == 256
+         and p.D == 512][0]
+    d = generate(w, device)
+    S, B, H, D = d["o"].shape
+    N, H_pr = w.N, w.H_pr
+    send_o = torch.empty((S, N, B, H_pr, D), dtype=d["o"].dtype, device=device)
+    send_l = torch.empty((S, N, B, H_pr), dtype=torch.float32, device=device)
+    out = torch.empty((N, B, H_pr, D), dtype=d["o"].dtype, device=device)
+    pack = binding.prepare_pack_send(d["o"], d["lse"], send_o, send_l)
+    comb = binding.prepare_lse_combine(send_o.transpose(0, 1), send_l.transpose(0, 1), out, None,
+                                       base=w.base)
+    e = d["o"].element_size()
+    return {"w": w, "launches": [pack, comb], "keep": (d, send_o, send_l, out),
+            "names": [f"dcp_pack_send (separate O and LSE buffers, G={S})",
+                      f"dcp_lse_combine (separate recv views, no returned LSE, G={N})"],
+            "bytes": [bytes_pack(S, B, H, D, e), bytes_merge(N, S, B, H_pr, D, e, return_lse=False)]}
+
+
+def setup_per_rank(device):
+    """One rank's own calls of the MLA decode merge (G = 1): the pack of source
+    0 and the combine of destination 0."""
+    import torch
+
+    from decode_context_attention_gb300 import binding, layouts
+    from decode_context_attention_gb300.workloads import WORKLOADS, generate
+
+    w = WORKLOADS["mla_decode"]
+    d = generate(w, device)
+    S, B, H, D = d["o"].shape
+    N, H_pr = w.N, w.H_pr
+    partial_o, stats = layouts.alloc_peer_inside(S, B, H_pr, N, D, d["o"].dtype, device)
+    dst_o, dst_lse = layouts.peer_inside_send_views(partial_o, stats)
+    ro, rl = layouts.exchange_peer_inside(partial_o, stats)
+    binding.pack_send(d["o"], d["lse"], dst_o, dst_lse)
+    out = torch.empty((1, B, H_pr, D), dtype=d["o"].dtype, device=device)
+    out_lse = torch.empty((1, B, H_pr), dtype=torch.float32, device=device)
+    pack = binding.prepare_pack_send(d["o"][:1], d["lse"][:1], dst_o[:1], dst_lse[:1])
+    comb = binding.prepare_lse_combine(ro[:1], rl[:1], out, out_lse, base=w.base)
+    e = d["o"].element_size()
+    return {"w": w, "launches": [pack, comb], "keep": (d, partial_o, stats, out, out_lse),
+            "names": ["dcp_pack_send (peer-inside, one source rank, G=1)",
+                      "dcp_lse_combine (one destination rank, G=1)"],
+            "bytes": [bytes_pack(1, B, H, D, e), bytes_merge(1, N, B, H_pr, D, e)]}
 
 
 def setup_peer_major(w, device):
@@ -558,6 +657,8 @@ def run_gpu(args):
               "sweep": lambda: setup_sweep_max(device),
               "mla_decode_fp8": lambda: setup_mla_fp8(device),
               "decode_attention": lambda: setup_decode_attention(device, batch=args.att_batch),
+              "two_collective": lambda: setup_two_collective(device),
+              "per_rank": lambda: setup_per_rank(device),
               "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens)}[args.only]()
         time_sequence(wl["launches"], args.steps, args.warmup,
                       None if args.only == "cached_extend" else flush, device)
@@ -578,6 +679,21 @@ def run_gpu(args):
     # --- secondary workloads (same run) ----------------------------------------
     secondary = []
     if not args.no_secondary:
+        gm, gmed = time_graph_step(mla, max(50, args.steps // 4), args.warmup, flush, device)
+        secondary.append({"workload": "mla_decode headline step captured as one CUDA graph (pack + combine), "
+                                      "L2 flushed before each replay only",
+                          "us_per_step": round(gm, 3), "us_median": round(gmed, 3),
+                          "gpu_launches_per_step": 2})
+        for setup, what in ((setup_per_rank, "per-rank calls (G=1) of the headline workload"),
+                            (setup_two_collective, "two-collective layout: separate O and LSE buffers")):
+            sw = setup(device)
+            p2, _ = time_sequence(sw["launches"], max(20, args.steps // 10), args.warmup, flush, device)
+            w2 = sw["w"]
+            secondary.append({"workload": f"{w2.name} N={w2.N} B={w2.B} H={w2.H} D={w2.D} {w2.dtype} "
+                                          f"base-{w2.base}, {what}",
+                              "kernels": [kernel_record(n, p, b, peak)
+                                          for n, p, b in zip(sw["names"], p2, sw["bytes"])]})
+            del sw
         for setup in (setup_sweep_max, setup_mla_fp8):
             sw = setup(device)
             p2, _ = time_sequence(sw["launches"], max(20, args.steps // 10), args.warmup, flush, device)
@@ -605,11 +721,11 @@ def run_gpu(args):
         secondary.append(rec)
         del at
         torch.cuda.empty_cache()
-        ce = setup_cached_extend(device)
+        ce = setup_cached_extend(device, slices=True)
         p3, _ = time_sequence(ce["launches"], args.ext_steps, 3, None, device)
         rec = {"workload": "cached_extend N=8 T=16384 H=96 D=512 fp32",
                "inputs_vs_l2": "24 GiB stack, far larger than L2 (no flush)",
-               "kernels": [kernel_record(ce["names"][0], p3[0], ce["bytes"][0], peak)]}
+               "kernels": [kernel_record(n, p, b, peak) for n, p, b in zip(ce["names"], p3, ce["bytes"])]}
         if rank == 0 and not args.no_cpu_baseline:
             us, el, n = time_oracle_cached_extend(min(5.0, args.cpu_budget))
             rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": 1,
@@ -646,6 +762,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": k["kernel"], "achieved": k["achieved_gbs"],
                      "peak": peak, "unit": "GB/s", "frac": k["frac_of_measured_hbm"],
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "peak_theoretical_gbs": theoretical_hbm_gbs(local),
                      "traffic": traffic, "algorithmic_bytes": k["algorithmic_bytes"]},
         "kernels": kernels,
         "secondary": secondary,
@@ -656,6 +773,35 @@ def run_gpu(args):
         "wall_s_timed_region": round(wall, 3),
     }
     print(json.dumps(line), flush=True)
+
+
+def time_graph_step(mla, steps, warmup, flush, device):
+    """The headline step (pack + combine) captured once as a CUDA graph and
+    replayed; L2 is flushed before each replay only, so the combine may find
+    the tail of the freshly written send buffer still in L2, as in a real
+    back-to-back step.  Returns (mean, median) µs per step."""
+    import torch
+
+    from decode_context_attention_gb300 import binding, layouts
+
+    d, w = mla["d"], mla["w"]
+    dst_o, dst_lse = layouts.peer_inside_send_views(mla["partial_o"], mla["stats"])
+    ro, rl = layouts.exchange_peer_inside(mla["partial_o"], mla["stats"])
+
+    def step():
+        binding.pack_send(d["o"], d["lse"], dst_o, dst_lse)
+        binding.lse_combine(ro, rl, mla["out"], mla["out_lse"], base=w.base)
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream(device).wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    per, _ = time_sequence([g.replay], steps, warmup, flush, device)
+    return statistics.fmean(per[0]) * 1e3, statistics.median(per[0]) * 1e3
 
 
 def run_e2e(mla, args, device):
@@ -768,8 +914,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["mla_decode", "sweep", "mla_decode_fp8", "cached_extend",
-                                       "decode_attention"],
+    ap.add_argument("--only", choices=["mla_decode", "sweep", "mla_decode_fp8", "two_collective", "per_rank",
+                                       "cached_extend", "decode_attention"],
                     help="run just this workload's launches (profiling); no JSON line")
     ap.add_argument("--att-batch", type=int, default=None,
                     help="requests of the decode-attention workload under --only (default 64)")

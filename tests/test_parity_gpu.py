@@ -171,6 +171,33 @@ def test_sweep_point(w):
         run_peer_inside(w, materialize=False)
 
 
+@pytest.mark.parametrize("N,B,D", [(2, 8, 128), (8, 256, 512)])
+def test_two_collective_layout(N, B, D):
+    """The legacy layout: O and LSE packed into separate peer-major buffers (one
+    all-to-all each), then the combine over the exchanged views without a
+    returned LSE.  The sweep recipe; the second case is its largest point."""
+    w = [p for p in sweep_points() if p.layout == "peer_major" and p.N == N and p.B == B and p.D == D][0]
+    d = generate(w, DEV)
+    o, lse = d["o"], d["lse"]
+    S, _, H, _ = o.shape
+    H_pr, dt = w.H_pr, o.dtype
+    send_o = sentinel_like((S, N, B, H_pr, D), dt, DEV)
+    send_l = sentinel_like((S, N, B, H_pr), torch.float32, DEV)
+    binding.pack_send(o, lse, send_o, send_l)
+    so_np = np_sentinel((S, N, B, H_pr, D), NP_PAYLOAD[dt])
+    sl_np = np_sentinel((S, N, B, H_pr), np.float32)
+    oracle.pack(ORACLE_DT[dt], N, to_np(o), to_np(lse), so_np, sl_np)
+    torch.cuda.synchronize()
+    assert_bytes_equal(send_o, so_np, "separate O send buffer")
+    assert_bytes_equal(send_l, sl_np, "separate LSE send buffer")
+    out = torch.empty((N, B, H_pr, D), dtype=dt, device=DEV)
+    binding.lse_combine(send_o.transpose(0, 1), send_l.transpose(0, 1), out, None, base=w.base)
+    want, _ = oracle.combine(ORACLE_DT[dt], so_np.transpose(1, 0, 2, 3, 4), sl_np.transpose(1, 0, 2, 3),
+                             base=w.base)
+    torch.cuda.synchronize()
+    assert_merge_close(out, want, f"{w.name} two-collective out")
+
+
 # ---------------------------------------------------------------------------
 # cached extend: in-place sanitising combine + head slices
 # ---------------------------------------------------------------------------
