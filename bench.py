@@ -446,14 +446,17 @@ def setup_per_rank(device):
     N, H_pr = w.N, w.H_pr
     partial_o, stats = layouts.alloc_peer_inside(S, B, H_pr, N, D, d["o"].dtype, device)
     dst_o, dst_lse = layouts.peer_inside_send_views(partial_o, stats)
-    ro, rl = layouts.exchange_peer_inside(partial_o, stats)
     binding.pack_send(d["o"], d["lse"], dst_o, dst_lse)
+    # destination 0 merges its own receive buffer, as a real all-to-all leaves
+    # it: o_out [B, H_pr, N, D] and stats [B, H_pr, N, 2], contiguous
+    ro, rl = layouts.materialize_peer_inside(partial_o, stats)
+    ro, rl = ro[:1].clone(), rl[:1]
     out = torch.empty((1, B, H_pr, D), dtype=d["o"].dtype, device=device)
     out_lse = torch.empty((1, B, H_pr), dtype=torch.float32, device=device)
     pack = binding.prepare_pack_send(d["o"][:1], d["lse"][:1], dst_o[:1], dst_lse[:1])
-    comb = binding.prepare_lse_combine(ro[:1], rl[:1], out, out_lse, base=w.base)
+    comb = binding.prepare_lse_combine(ro, rl, out, out_lse, base=w.base)
     e = d["o"].element_size()
-    return {"w": w, "launches": [pack, comb], "keep": (d, partial_o, stats, out, out_lse),
+    return {"w": w, "launches": [pack, comb], "keep": (d, partial_o, stats, ro, rl, out, out_lse),
             "names": ["dcp_pack_send (peer-inside, one source rank, G=1)",
                       "dcp_lse_combine (one destination rank, G=1)"],
             "bytes": [bytes_pack(1, B, H, D, e), bytes_merge(1, N, B, H_pr, D, e)]}

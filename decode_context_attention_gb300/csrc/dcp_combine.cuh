@@ -392,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 2) combine_shifted_kernel(const Comb
 // Shifted-chunk kernel for (T, NR) and this row length, or nullptr.
 // Not for fp8: its rows are half as long in bytes, and the word-wise stores
 // and the per-word tail cost more than the 4-byte loads they replace
-// (measured 25.5 vs 22.1 us for the fp8 MLA-decode unpack+combine).
+// (fp8 MLA-decode unpack+combine: 25.7 us with 16 lanes x 2 chunks per row,
+// 26.7 us with 32 lanes x 1 chunk, against 22.0 us for the 4-byte path).
 template <typename T, int NR, bool SAN>
 const void* pick_shifted(int row_bytes, int& lpr) {
     if constexpr (sizeof(T) == 1) {
