@@ -17,7 +17,8 @@ Pins: ``tests/test_oracle.py`` checks every function here against what the
 pages and mathematics fix (identity at N=1, neutral empty ranks, shift
 invariance, base-2/base-e agreement, closed forms, brute-force split
 attention equal to unsplit attention, round-robin partition invariants,
-numpy's own fp16/bf16 decoding and index maps).
+numpy's own fp16/bf16 decoding and index maps); ``tests/test_oracle_mutants.py``
+shows that 24 planted slips in ``dcp_oracle.c`` each make one of those pins fail.
 """
 from __future__ import annotations
 
@@ -59,7 +60,10 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # DCP_ORACLE_LIB points the oracle at another build of dcp_oracle.c:
+        # the planted-mistake test (tests/test_oracle_mutants.py) runs the
+        # pins against deliberately broken copies this way.
+        lib = ctypes.CDLL(os.environ.get("DCP_ORACLE_LIB") or build())
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         lib.oracle_pack.restype = i32
         lib.oracle_pack.argtypes = ([i32] * 6 + [vp, i64, i64, i64] + [vp, i64, i64, i64]
