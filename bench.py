@@ -363,7 +363,7 @@ def setup_cached_extend(device, tokens=None, slices=False):
             "bytes": [bytes_merge(1, N, T, H, D, 4)] * 2}
 
 
-def setup_decode_attention(device, split_tokens=1024, batch=None):
+def setup_decode_attention(device, split_tokens=1024, batch=None, name="mha_decode_attention"):
     import math
 
     import torch
@@ -371,7 +371,7 @@ def setup_decode_attention(device, split_tokens=1024, batch=None):
     from decode_context_attention_gb300 import binding
     from decode_context_attention_gb300.workloads import generate_attention
 
-    a = generate_attention(device=device, **({"B": batch} if batch else {}))
+    a = generate_attention(name, device=device, **({"B": batch} if batch else {}))
     c = a["cfg"]
     N, B, H, Hkv, D = c["N"], c["B"], c["H"], c["Hkv"], c["D"]
     o = torch.empty((N, B, H, D), dtype=a["q"].dtype, device=device)
@@ -386,6 +386,7 @@ def setup_decode_attention(device, split_tokens=1024, batch=None):
     # K and V rows of every owned token, each rank's read of q, O and LSE written
     algo = 2 * tokens * Hkv * D * e + N * B * H * D * e + N * B * H * D * e + N * B * H * 4
     return {"launches": [call], "keep": (a, o, lse, ws), "tokens": tokens, "workspace_bytes": nbytes,
+            "name": name,
             "names": [f"dcp_decode_attention (N={N} B={B} H={H} Hkv={Hkv} D={D} bf16, "
                       f"{tokens} KV tokens, splits of {split_tokens})"],
             "bytes": [algo]}
@@ -660,6 +661,8 @@ def run_gpu(args):
               "sweep": lambda: setup_sweep_max(device),
               "mla_decode_fp8": lambda: setup_mla_fp8(device),
               "decode_attention": lambda: setup_decode_attention(device, batch=args.att_batch),
+              "gqa_decode_attention": lambda: setup_decode_attention(device, batch=args.att_batch,
+                                                                     name="gqa_decode_attention"),
               "two_collective": lambda: setup_two_collective(device),
               "per_rank": lambda: setup_per_rank(device),
               "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens)}[args.only]()
@@ -712,18 +715,19 @@ def run_gpu(args):
                                                f"unpack+combine = 1/{w2.N} of a call), {el:.1f} s"}
             secondary.append(rec)
             del sw
-        at = setup_decode_attention(device)
-        p4, _ = time_sequence(at["launches"], max(10, args.steps // 20), 3, flush, device)
-        rec = {"workload": "mha_decode_attention (the step before the merge)",
-               "workspace_bytes": at["workspace_bytes"],
-               "kernels": [kernel_record(at["names"][0], p4[0], at["bytes"][0], peak)]}
-        if rank == 0 and not args.no_cpu_baseline:
-            us, el, n = time_oracle_attention(at, min(5.0, args.cpu_budget))
-            rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": 1,
-                                 "sample": f"{n} sampled (request, head) rows, {el:.1f} s, scaled by KV tokens"}
-        secondary.append(rec)
-        del at
-        torch.cuda.empty_cache()
+        for att_name in ("mha_decode_attention", "gqa_decode_attention"):
+            at = setup_decode_attention(device, name=att_name)
+            p4, _ = time_sequence(at["launches"], max(10, args.steps // 20), 3, flush, device)
+            rec = {"workload": f"{att_name} (the step before the merge)",
+                   "workspace_bytes": at["workspace_bytes"],
+                   "kernels": [kernel_record(at["names"][0], p4[0], at["bytes"][0], peak)]}
+            if rank == 0 and not args.no_cpu_baseline:
+                us, el, n = time_oracle_attention(at, min(5.0, args.cpu_budget))
+                rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": 1,
+                                     "sample": f"{n} sampled (request, head) rows, {el:.1f} s, scaled by KV tokens"}
+            secondary.append(rec)
+            del at
+            torch.cuda.empty_cache()
         ce = setup_cached_extend(device, slices=True)
         p3, _ = time_sequence(ce["launches"], args.ext_steps, 3, None, device)
         rec = {"workload": "cached_extend N=8 T=16384 H=96 D=512 fp32",
@@ -935,7 +939,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=["mla_decode", "sweep", "mla_decode_fp8", "two_collective", "per_rank",
-                                       "cached_extend", "decode_attention"],
+                                       "cached_extend", "decode_attention", "gqa_decode_attention"],
                     help="run just this workload's launches (profiling); no JSON line")
     ap.add_argument("--att-batch", type=int, default=None,
                     help="requests of the decode-attention workload under --only (default 64)")

@@ -31,10 +31,15 @@
 #include <stdio.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "dcp_device.cuh"
 
 namespace dcp {
+
+#ifndef DCP_ATTN_MMA
+#define DCP_ATTN_MMA 1
+#endif
 
 constexpr int kAttnThreads = 128;
 constexpr int kAttnBlockTokens = 4;   // tokens per softmax block per lane group
@@ -55,6 +60,43 @@ __device__ __forceinline__ void vec8_to_f32(const uint4& v, float (&f)[8]) {
 
 // Local token count of rank r for a request of global length L (round robin).
 __device__ __forceinline__ int local_len(int L, int N, int r) { return L / N + (r < L % N ? 1 : 0); }
+
+// The CTA's NG partial softmax states per query head (base 2: running max m,
+// sum l, unnormalised accumulator acc) merged into (O, lse): written as the
+// rank's result with one split, or as the split's fp32 partial otherwise.
+template <typename T, int D, int GQ, int NG>
+__device__ __forceinline__ void write_cta_result(const AttnParams& p, int r, int b, int hkv, int split,
+                                                 const float (*s_m)[GQ], const float (*s_l)[GQ],
+                                                 const float (*s_acc)[GQ][D]) {
+    for (int idx = threadIdx.x; idx < GQ * D; idx += blockDim.x) {
+        const int g = idx / D;
+        const int e = idx - g * D;
+        float M = -INFINITY;
+        for (int k = 0; k < NG; ++k) M = fmaxf(M, s_m[k][g]);
+        float Ls = 0.f, A = 0.f;
+        if (M != -INFINITY) {
+            for (int k = 0; k < NG; ++k) {
+                const float sc = exp2f(s_m[k][g] - M);
+                Ls += sc * s_l[k][g];
+                A += sc * s_acc[k][g][e];
+            }
+        }
+        const int h = hkv * GQ + g;
+        const float o = Ls > 0.f ? A / Ls : 0.f;
+        const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
+        if (p.nsplit == 1) {
+            T* orow = reinterpret_cast<T*>(p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh);
+            orow[e] = from_f32<T>(o);
+            if (e == 0)
+                p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] =
+                    p.base2 ? lse2 : lse2 * kLn2;
+        } else {
+            const int64_t row = (((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split;
+            p.ws_o[row * D + e] = o;
+            if (e == 0) p.ws_lse[row] = lse2;
+        }
+    }
+}
 
 template <typename T, int D, int GQ>
 __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const AttnParams p) {
@@ -166,34 +208,212 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
         for (int i = 0; i < 8; ++i) s_acc[grp][g][jl * 8 + i] = acc[g][i];
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < GQ * D; idx += kAttnThreads) {
-        const int g = idx / D;
-        const int e = idx - g * D;
-        float M = -INFINITY;
-        for (int k = 0; k < NG; ++k) M = fmaxf(M, s_m[k][g]);
-        float Ls = 0.f, A = 0.f;
-        if (M != -INFINITY) {
-            for (int k = 0; k < NG; ++k) {
-                const float sc = exp2f(s_m[k][g] - M);
-                Ls += sc * s_l[k][g];
-                A += sc * s_acc[k][g][e];
-            }
-        }
-        const int h = hkv * GQ + g;
-        const float o = Ls > 0.f ? A / Ls : 0.f;
-        const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
-        if (p.nsplit == 1) {
-            T* orow = reinterpret_cast<T*>(p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh);
-            orow[e] = from_f32<T>(o);
-            if (e == 0)
-                p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] =
-                    p.base2 ? lse2 : lse2 * kLn2;
-        } else {
-            const int64_t row = (((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split;
-            p.ws_o[row * D + e] = o;
-            if (e == 0) p.ws_lse[row] = lse2;
+    write_cta_result<T, D, GQ, NG>(p, r, b, hkv, split, s_m, s_l, s_acc);
+}
+
+// ---------------------------------------------------------------------------
+// Grouped-query heads on the tensor cores.  With G_q query heads per KV head
+// every K/V byte feeds 2 G_q multiply-adds (scores and output), more than the
+// CUDA cores sustain at HBM speed beyond G_q = 2, so for G_q in {2, 4, 8} the
+// products run as warp-level mma.sync (bf16 or f16 operands, fp32
+// accumulation).  One warp takes blocks of 16 tokens of its CTA's split:
+//   S   [16 x 8 tokens]  = Q [16 rows: the G_q heads, the rest zero] . K^T
+//   O^T [D x 8 heads]   += V^T [D x 16 tokens] . P^T [16 tokens x 8 heads]
+// K and V rows arrive by 16-byte loads; the contraction over D does not
+// depend on the order of its terms, so the d positions each lane loads are
+// simply the ones it feeds to the fragments (Q is read in the same order),
+// and V's 8x8 tiles are transposed in registers (movmatrix) so tokens become
+// the contraction index.  P goes in as two 16-bit terms (hi + lo), keeping
+// ~16 significant bits of every probability instead of 8.  The online
+// softmax is in base 2, per head, over the 4 lanes that hold that head's
+// scores; the warps' states meet in shared memory as in the kernel above.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4], unsigned b0, unsigned b1) {
+    if constexpr (std::is_same<T, __half>::value)
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                     "{%8,%9}, {%0,%1,%2,%3};\n"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                     "{%8,%9}, {%0,%1,%2,%3};\n"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 8x8 tile of 16-bit values, lane t holding row t/4, columns 2(t%4)..+1 ->
+// the transposed tile in the same distribution.
+__device__ __forceinline__ unsigned tile_transpose(unsigned x) {
+    unsigned y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Two floats rounded to a T pair (the first in the low half).
+template <typename T>
+__device__ __forceinline__ unsigned round_pair(float lo, float hi) {
+    unsigned u;
+    if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        memcpy(&u, &h, 4);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        memcpy(&u, &h, 4);
+    }
+    return u;
+}
+
+__device__ __forceinline__ unsigned word_of(const uint4& v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+template <typename T, int D, int GQ>
+__global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const AttnParams p) {
+    static_assert(D % 32 == 0 && GQ >= 1 && GQ <= 8, "fragment shapes");
+    constexpr int NI = D / 32;   // 16-byte pieces per lane per token row
+    constexpr int KS = D / 16;   // k-steps of the score products
+    constexpr int NM = D / 16;   // output products (16 d each)
+    constexpr int NW = kAttnThreads / 32;
+    constexpr int TB = 16;       // tokens per warp block
+    constexpr unsigned kFull = 0xffffffffu;
+    __shared__ float s_m[NW][GQ], s_l[NW][GQ];
+    __shared__ float s_acc[NW][GQ][D];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int qr = lane >> 2;  // fragment row (score head / token row / output d row)
+    const int qc = lane & 3;   // fragment column pair
+
+    const int hkv = blockIdx.x % p.Hkv;
+    const int rb = blockIdx.x / p.Hkv;
+    const int b = rb % p.B;
+    const int r = rb / p.B;
+    const int split = blockIdx.y;
+    int L = p.seq_lens[b];
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+    const int Ll = local_len(L, p.N, r);
+    const int t0 = split * p.split_tokens;
+    const int t1 = min(t0 + p.split_tokens, Ll);
+
+    // Q fragments: row qr is head hkv*GQ + qr (zero for qr >= GQ); k-step ks
+    // takes d = 32(ks/2) + 8qc + 4(ks%2) + {0,1} and that + 2, the positions
+    // the K fragments below carry
+    const bool head_ok = qr < GQ;
+    unsigned qa[KS][2];
+    {
+        const unsigned char* qrow =
+            p.q + (int64_t)b * p.q_sb + (int64_t)(hkv * GQ + (head_ok ? qr : 0)) * p.q_sh;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int d0 = 32 * (ks >> 1) + 8 * qc + 4 * (ks & 1);
+            qa[ks][0] = head_ok ? *reinterpret_cast<const unsigned*>(qrow + 2 * d0) : 0u;
+            qa[ks][1] = head_ok ? *reinterpret_cast<const unsigned*>(qrow + 2 * (d0 + 2)) : 0u;
         }
     }
+    const float qscale = p.sm_scale * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    float oacc[NM][4];
+#pragma unroll
+    for (int j = 0; j < NM; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+
+    const unsigned char* kb = p.k + (int64_t)r * p.k_sn + (int64_t)b * p.k_sb + (int64_t)hkv * p.k_sh + 16 * qc;
+    const unsigned char* vb = p.v + (int64_t)r * p.v_sn + (int64_t)b * p.v_sb + (int64_t)hkv * p.v_sh + 16 * qc;
+    for (int tb = t0 + warp * TB; tb < t1; tb += NW * TB) {  // uniform across the warp
+        // lane (qr, qc) loads token tb + 8h + qr, bytes 64i + 16qc .. +15 of its row;
+        // rows past the split are zeros (never read)
+        uint4 kr[2][NI], vr[2][NI];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = tb + 8 * h + qr;
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                kr[h][i] = make_uint4(0u, 0u, 0u, 0u);
+                vr[h][i] = kr[h][i];
+                if (t < t1) {
+                    kr[h][i] = ld_stream<16>(kb + (int64_t)t * p.k_st + 64 * i);
+                    vr[h][i] = ld_stream<16>(vb + (int64_t)t * p.v_st + 64 * i);
+                }
+            }
+        }
+        // scores of head qr for tokens tb + 8h + 2qc + {0,1}, in base-2 units
+        float sc[2][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const unsigned a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+                const uint4& kv = kr[h][ks >> 1];
+                mma_16816<T>(c, a, (ks & 1) ? kv.z : kv.x, (ks & 1) ? kv.w : kv.y);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) sc[h][e] = tb + 8 * h + 2 * qc + e < t1 ? c[e] * qscale : -INFINITY;
+        }
+        // online softmax of head qr over the quad's 16 tokens
+        float bm = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+        const float mn = fmaxf(m_run, bm);
+        float alpha = 1.f;
+        float pr[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        if (head_ok && mn != -INFINITY) {
+            alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) pr[h][e] = exp2f(sc[h][e] - mn);  // masked: exp2(-inf) = 0
+            l_run = l_run * alpha + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+            m_run = mn;
+        }
+        // O^T columns are heads 2qc, 2qc+1: their rescale factors live in quads 2qc, 2qc+1
+        const float al0 = __shfl_sync(kFull, alpha, 8 * qc);
+        const float al1 = __shfl_sync(kFull, alpha, 8 * qc + 4);
+#pragma unroll
+        for (int j = 0; j < NM; ++j) {
+            oacc[j][0] *= al0;
+            oacc[j][1] *= al1;
+            oacc[j][2] *= al0;
+            oacc[j][3] *= al1;
+        }
+        // P^T fragments: this lane's own probabilities, as hi + lo 16-bit terms
+        const unsigned ph0 = round_pair<T>(pr[0][0], pr[0][1]);
+        const unsigned ph1 = round_pair<T>(pr[1][0], pr[1][1]);
+        const float2 bh0 = unpack2(word_to_pair<T>(ph0));
+        const float2 bh1 = unpack2(word_to_pair<T>(ph1));
+        const unsigned pl0 = round_pair<T>(pr[0][0] - bh0.x, pr[0][1] - bh0.y);
+        const unsigned pl1 = round_pair<T>(pr[1][0] - bh1.x, pr[1][1] - bh1.y);
+#pragma unroll
+        for (int j = 0; j < NM; ++j) {
+            const int x0 = 2 * j, x1 = 2 * j + 1;  // 8x8 tiles: word x%4 of piece x/4
+            const unsigned a[4] = {tile_transpose(word_of(vr[0][x0 >> 2], x0 & 3)),
+                                   tile_transpose(word_of(vr[0][x1 >> 2], x1 & 3)),
+                                   tile_transpose(word_of(vr[1][x0 >> 2], x0 & 3)),
+                                   tile_transpose(word_of(vr[1][x1 >> 2], x1 & 3))};
+            mma_16816<T>(oacc[j], a, ph0, ph1);
+            mma_16816<T>(oacc[j], a, pl0, pl1);
+        }
+    }
+
+    // the quad's partial sums of head qr, then the warp's state to shared memory:
+    // output row qr of tile x is d = 32(x/4) + 8(qr/2) + 2(x%4) + qr%2
+    l_run += __shfl_xor_sync(kFull, l_run, 1);
+    l_run += __shfl_xor_sync(kFull, l_run, 2);
+    if (head_ok && qc == 0) {
+        s_m[warp][qr] = m_run;
+        s_l[warp][qr] = l_run;
+    }
+#pragma unroll
+    for (int j = 0; j < NM; ++j)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int x = 2 * j + half;
+            const int d = 32 * (x >> 2) + 8 * (qr >> 1) + 2 * (x & 3) + (qr & 1);
+            if (2 * qc < GQ) s_acc[warp][2 * qc][d] = oacc[j][2 * half];
+            if (2 * qc + 1 < GQ) s_acc[warp][2 * qc + 1][d] = oacc[j][2 * half + 1];
+        }
+    __syncthreads();
+    write_cta_result<T, D, GQ, NW>(p, r, b, hkv, split, s_m, s_l, s_acc);
 }
 
 // Merge the splits of every (rank, request, head) row: the LSE-weighted merge
@@ -238,12 +458,24 @@ __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const
 template <typename T, int D>
 static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) {
     const void* k;
-    switch (p.H / p.Hkv) {
-        case 1: k = (const void*)decode_partial_kernel<T, D, 1>; break;
-        case 2: k = (const void*)decode_partial_kernel<T, D, 2>; break;
-        case 4: k = (const void*)decode_partial_kernel<T, D, 4>; break;
-        case 8: k = (const void*)decode_partial_kernel<T, D, 8>; break;
-        default: return cudaErrorInvalidValue;
+    // grouped-query heads go to the tensor cores (D <= 128 fits the lane's
+    // registers); one query head per KV head stays on the CUDA cores
+    if constexpr (D <= 128 && DCP_ATTN_MMA) {
+        switch (p.H / p.Hkv) {
+            case 1: k = (const void*)decode_partial_kernel<T, D, 1>; break;
+            case 2: k = (const void*)decode_partial_mma_kernel<T, D, 2>; break;
+            case 4: k = (const void*)decode_partial_mma_kernel<T, D, 4>; break;
+            case 8: k = (const void*)decode_partial_mma_kernel<T, D, 8>; break;
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (p.H / p.Hkv) {
+            case 1: k = (const void*)decode_partial_kernel<T, D, 1>; break;
+            case 2: k = (const void*)decode_partial_kernel<T, D, 2>; break;
+            case 4: k = (const void*)decode_partial_kernel<T, D, 4>; break;
+            case 8: k = (const void*)decode_partial_kernel<T, D, 8>; break;
+            default: return cudaErrorInvalidValue;
+        }
     }
     void* args[] = {(void*)&p};
     const dim3 grid((unsigned)((int64_t)p.N * p.B * p.Hkv), (unsigned)p.nsplit);

@@ -36,6 +36,8 @@ cached-extend cases; no model weights or datasets are involved):
                  ~ U(1, 16384); every rank's local K/V cache holds its
                  round-robin share (local token i of rank r = global token
                  i*N + r), values ~ N(0,1); queries ~ N(0,1).
+  gqa_decode_attention  the same with grouped-query heads: 32 query heads
+                 over 4 KV heads (8 per KV head), seed 7.
 
 An empty (rank, token) pair is the pages' neutral state for a rank that owns
 no KV slice of that request: O = 0, LSE = -inf (sglang PR #33926 report,
@@ -176,7 +178,9 @@ def generate(w: Workload, device="cuda", seed: int | None = None) -> dict:
 
 
 ATTENTION = {"mha_decode_attention": dict(N=4, B=64, H=32, Hkv=32, D=128, dtype="bf16", max_len=16384,
-                                          base="e", seed=5)}
+                                          base="e", seed=5),
+             "gqa_decode_attention": dict(N=4, B=64, H=32, Hkv=4, D=128, dtype="bf16", max_len=16384,
+                                          base="e", seed=7)}
 
 
 def generate_attention(name="mha_decode_attention", device="cuda", seed=None, **override) -> dict:

@@ -98,6 +98,13 @@ CASES = [
     (8, 2, 4, 1, 256, [3, 9, 17, 500], torch.bfloat16, "2", 40),
     (3, 2, 16, 2, 128, [1, 2, 1000], torch.float16, "2", 100),
     (1, 2, 2, 2, 128, [0, 1, 77], torch.bfloat16, "e", 8),
+    # grouped-query heads (the tensor-core path for D <= 128): block tails,
+    # splits that are and are not multiples of the 16-token block
+    (4, 3, 8, 4, 128, [0, 1, 15, 16, 17, 33, 1500], torch.bfloat16, "e", 48),
+    (2, 2, 32, 4, 128, [5, 100, 257, 4097], torch.bfloat16, "2", 1000),
+    (4, 2, 16, 4, 64, [1, 31, 64, 999], torch.float16, "e", 24),
+    (1, 2, 8, 1, 128, [3, 700], torch.bfloat16, "2", 4096),
+    (3, 2, 4, 2, 64, [2, 18, 95], torch.bfloat16, "e", 7),
 ]
 
 
@@ -176,13 +183,14 @@ def test_whole_dcp_decode_equals_unsplit_attention(base):
     assert_attn_lse(got_lse, want_lse, "merged lse")
 
 
-def test_decode_attention_workload_full_size_sampled():
-    """The benchmark's workload (N=4, B=64, H=32, D=128, lengths up to 16384) in
-    its launch configuration (splits of 1024 local tokens): sampled (request,
-    head) rows of every rank against the oracle."""
+@pytest.mark.parametrize("name", ["mha_decode_attention", "gqa_decode_attention"])
+def test_decode_attention_workload_full_size_sampled(name):
+    """The benchmark's workloads (N=4, B=64, H=32 over 32 or 4 KV heads, D=128,
+    lengths up to 16384) in their launch configuration (splits of 1024 local
+    tokens): sampled (request, head) rows of every rank against the oracle."""
     from decode_context_attention_gb300.workloads import generate_attention
 
-    a = generate_attention(device=DEV)
+    a = generate_attention(name, device=DEV)
     c = a["cfg"]
     N, B, H, Hkv, D = c["N"], c["B"], c["H"], c["Hkv"], c["D"]
     scale = 1.0 / math.sqrt(D)
