@@ -661,7 +661,7 @@ def run_gpu(args):
               "sweep": lambda: setup_sweep_max(device),
               "mla_decode_fp8": lambda: setup_mla_fp8(device),
               "decode_attention": lambda: setup_decode_attention(device, batch=args.att_batch),
-              "gqa_decode_attention": lambda: setup_decode_attention(device, batch=args.att_batch,
+              "gqa_decode_attention": lambda: setup_decode_attention(device, split_tokens=2048, batch=args.att_batch,
                                                                      name="gqa_decode_attention"),
               "two_collective": lambda: setup_two_collective(device),
               "per_rank": lambda: setup_per_rank(device),
@@ -715,8 +715,10 @@ def run_gpu(args):
                                                f"unpack+combine = 1/{w2.N} of a call), {el:.1f} s"}
             secondary.append(rec)
             del sw
-        for att_name in ("mha_decode_attention", "gqa_decode_attention"):
-            at = setup_decode_attention(device, name=att_name)
+        # splits of local tokens per CTA: 1024 for MHA, 2048 for GQA (measured
+        # best among 256..2048: fewer split partials to write and merge)
+        for att_name, att_split in (("mha_decode_attention", 1024), ("gqa_decode_attention", 2048)):
+            at = setup_decode_attention(device, split_tokens=att_split, name=att_name)
             p4, _ = time_sequence(at["launches"], max(10, args.steps // 20), 3, flush, device)
             rec = {"workload": f"{att_name} (the step before the merge)",
                    "workspace_bytes": at["workspace_bytes"],

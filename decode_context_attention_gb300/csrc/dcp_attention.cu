@@ -40,6 +40,9 @@ namespace dcp {
 #ifndef DCP_ATTN_MMA
 #define DCP_ATTN_MMA 1
 #endif
+#ifndef DCP_ATTN_PREFETCH
+#define DCP_ATTN_PREFETCH 1
+#endif
 
 constexpr int kAttnThreads = 128;
 constexpr int kAttnBlockTokens = 4;   // tokens per softmax block per lane group
@@ -231,12 +234,12 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
 template <typename T>
 __device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4], unsigned b0, unsigned b1) {
     if constexpr (std::is_same<T, __half>::value)
-        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
                      "{%8,%9}, {%0,%1,%2,%3};\n"
                      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     else
-        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
                      "{%8,%9}, {%0,%1,%2,%3};\n"
                      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -246,7 +249,7 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4],
 // the transposed tile in the same distribution.
 __device__ __forceinline__ unsigned tile_transpose(unsigned x) {
     unsigned y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
     return y;
 }
 
@@ -319,10 +322,9 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
 
     const unsigned char* kb = p.k + (int64_t)r * p.k_sn + (int64_t)b * p.k_sb + (int64_t)hkv * p.k_sh + 16 * qc;
     const unsigned char* vb = p.v + (int64_t)r * p.v_sn + (int64_t)b * p.v_sb + (int64_t)hkv * p.v_sh + 16 * qc;
-    for (int tb = t0 + warp * TB; tb < t1; tb += NW * TB) {  // uniform across the warp
-        // lane (qr, qc) loads token tb + 8h + qr, bytes 64i + 16qc .. +15 of its row;
-        // rows past the split are zeros (never read)
-        uint4 kr[2][NI], vr[2][NI];
+    // lane (qr, qc) loads token tb + 8h + qr, bytes 64i + 16qc .. +15 of its row;
+    // rows past the split are zeros (never read)
+    auto load_block = [&](uint4 (&kr)[2][NI], uint4 (&vr)[2][NI], int tb) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int t = tb + 8 * h + qr;
@@ -336,20 +338,25 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
                 }
             }
         }
+    };
+    auto merge_block = [&](const uint4 (&kr)[2][NI], const uint4 (&vr)[2][NI], int tb) {
         // scores of head qr for tokens tb + 8h + 2qc + {0,1}, in base-2 units
+        // (the two halves' products alternate, so consecutive mma are independent)
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const unsigned a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint4& kv = kr[h][ks >> 1];
+                mma_16816<T>(c[h], a, (ks & 1) ? kv.z : kv.x, (ks & 1) ? kv.w : kv.y);
+            }
+        }
         float sc[2][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const unsigned a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-                const uint4& kv = kr[h][ks >> 1];
-                mma_16816<T>(c, a, (ks & 1) ? kv.z : kv.x, (ks & 1) ? kv.w : kv.y);
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) sc[h][e] = tb + 8 * h + 2 * qc + e < t1 ? c[e] * qscale : -INFINITY;
-        }
+            for (int e = 0; e < 2; ++e) sc[h][e] = tb + 8 * h + 2 * qc + e < t1 ? c[h][e] * qscale : -INFINITY;
         // online softmax of head qr over the quad's 16 tokens
         float bm = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
         bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
@@ -383,17 +390,43 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
         const float2 bh1 = unpack2(word_to_pair<T>(ph1));
         const unsigned pl0 = round_pair<T>(pr[0][0] - bh0.x, pr[0][1] - bh0.y);
         const unsigned pl1 = round_pair<T>(pr[1][0] - bh1.x, pr[1][1] - bh1.y);
+        unsigned va[NM][4];
 #pragma unroll
         for (int j = 0; j < NM; ++j) {
             const int x0 = 2 * j, x1 = 2 * j + 1;  // 8x8 tiles: word x%4 of piece x/4
-            const unsigned a[4] = {tile_transpose(word_of(vr[0][x0 >> 2], x0 & 3)),
-                                   tile_transpose(word_of(vr[0][x1 >> 2], x1 & 3)),
-                                   tile_transpose(word_of(vr[1][x0 >> 2], x0 & 3)),
-                                   tile_transpose(word_of(vr[1][x1 >> 2], x1 & 3))};
-            mma_16816<T>(oacc[j], a, ph0, ph1);
-            mma_16816<T>(oacc[j], a, pl0, pl1);
+            va[j][0] = tile_transpose(word_of(vr[0][x0 >> 2], x0 & 3));
+            va[j][1] = tile_transpose(word_of(vr[0][x1 >> 2], x1 & 3));
+            va[j][2] = tile_transpose(word_of(vr[1][x0 >> 2], x0 & 3));
+            va[j][3] = tile_transpose(word_of(vr[1][x1 >> 2], x1 & 3));
         }
+        // hi terms of every d block, then lo terms: consecutive mma are independent
+#pragma unroll
+        for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], ph0, ph1);
+#pragma unroll
+        for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], pl0, pl1);
+    };
+    const int stride = NW * TB;
+#if DCP_ATTN_PREFETCH
+    // two register sets: the next block's loads are in flight while this one merges
+    uint4 ka[2][NI], va[2][NI], kn[2][NI], vn[2][NI];
+    int tb = t0 + warp * TB;  // uniform across the warp
+    if (tb < t1) load_block(ka, va, tb);
+    while (tb < t1) {
+        if (tb + stride < t1) load_block(kn, vn, tb + stride);
+        merge_block(ka, va, tb);
+        tb += stride;
+        if (tb >= t1) break;
+        if (tb + stride < t1) load_block(ka, va, tb + stride);
+        merge_block(kn, vn, tb);
+        tb += stride;
     }
+#else
+    for (int tb = t0 + warp * TB; tb < t1; tb += stride) {  // uniform across the warp
+        uint4 kr[2][NI], vr[2][NI];
+        load_block(kr, vr, tb);
+        merge_block(kr, vr, tb);
+    }
+#endif
 
     // the quad's partial sums of head qr, then the warp's state to shared memory:
     // output row qr of tile x is d = 32(x/4) + 8(qr/2) + 2(x%4) + qr%2

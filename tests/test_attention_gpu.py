@@ -196,10 +196,10 @@ def test_decode_attention_workload_full_size_sampled(name):
     scale = 1.0 / math.sqrt(D)
     o = torch.empty((N, B, H, D), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty((N, B, H), dtype=torch.float32, device=DEV)
-    nbytes = binding.workspace_bytes(N, B, H, D, a["max_len"], 1024)
+    nbytes = binding.workspace_bytes(N, B, H, D, a["max_len"], split)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     binding.decode_attention(a["q"], a["k"], a["v"], a["seq_lens"], a["max_len"], o, lse, scale,
-                             base=c["base"], split_tokens=1024, workspace=ws)
+                             base=c["base"], split_tokens=split, workspace=ws)
     torch.cuda.synchronize()
     lens = a["seq_lens"].cpu().tolist()
     rng = np.random.default_rng(3)
