@@ -271,6 +271,7 @@ KERNEL_SOURCES = {
     "pack_kernel": ("dcp_pack.cu", "dcp_device.cuh"),
     "combine_kernel": ("dcp_combine.cuh", "dcp_combine_bf16.cu", "dcp_device.cuh"),
     "decode_partial_kernel": ("dcp_attention.cu", "dcp_device.cuh"),
+    "decode_partial_mma_kernel": ("dcp_attention.cu", "dcp_device.cuh"),
 }
 
 

@@ -183,11 +183,11 @@ def test_whole_dcp_decode_equals_unsplit_attention(base):
     assert_attn_lse(got_lse, want_lse, "merged lse")
 
 
-@pytest.mark.parametrize("name", ["mha_decode_attention", "gqa_decode_attention"])
-def test_decode_attention_workload_full_size_sampled(name):
+@pytest.mark.parametrize("name,split", [("mha_decode_attention", 1024), ("gqa_decode_attention", 2048)])
+def test_decode_attention_workload_full_size_sampled(name, split):
     """The benchmark's workloads (N=4, B=64, H=32 over 32 or 4 KV heads, D=128,
-    lengths up to 16384) in their launch configuration (splits of 1024 local
-    tokens): sampled (request, head) rows of every rank against the oracle."""
+    lengths up to 16384) in their launch configuration (splits of 1024 / 2048
+    local tokens): sampled (request, head) rows of every rank against the oracle."""
     from decode_context_attention_gb300.workloads import generate_attention
 
     a = generate_attention(name, device=DEV)
