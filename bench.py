@@ -761,11 +761,13 @@ def run_gpu(args):
         "metric": METRIC, "value": round(ms_per_step * 1e3, 3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 6), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded O ~ N(0,1), LSE ~ U(0,20) base 2)",
         "config": {"workload": f"mla_decode N={w.N} B={w.B} H={w.H} D={w.D} bf16 base-2, "
                                "peer-inside pack + combine over strided recv views, all ranks on "
                                "one GPU", "calls_per_step_per_gpu": 1,
+                   "arithmetic": "bf16 payload and fp32 LSE; the pack is a bit copy, the merge "
+                                 "accumulates in fp32 and rounds once to bf16",
                    "l2": "flushed before every kernel (2x-L2 write, then 2x-L2 read), outside "
                          "the timed events",
                    "parallelism": f"{world} independent replica(s), no collective"},
