@@ -245,6 +245,20 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4],
                      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+template <typename T>
+__device__ __forceinline__ void mma_1688(float (&d)[4], const unsigned (&a)[2], unsigned b0) {
+    if constexpr (std::is_same<T, __half>::value)
+        asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(b0));
+    else
+        asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(b0));
+}
+
 // 8x8 tile of 16-bit values, lane t holding row t/4, columns 2(t%4)..+1 ->
 // the transposed tile in the same distribution.
 __device__ __forceinline__ unsigned tile_transpose(unsigned x) {
@@ -278,7 +292,9 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
     constexpr int KS = D / 16;   // k-steps of the score products
     constexpr int NM = D / 16;   // output products (16 d each)
     constexpr int NW = kAttnThreads / 32;
-    constexpr int TB = 16;       // tokens per warp block
+    constexpr int HB = D <= 128 ? 2 : 1;  // 8-token halves per warp block (registers bound D = 256 to one)
+    constexpr int TB = 8 * HB;            // tokens per warp block
+    constexpr bool PF = DCP_ATTN_PREFETCH && D <= 128;  // second register set for the next block
     constexpr unsigned kFull = 0xffffffffu;
     __shared__ float s_m[NW][GQ], s_l[NW][GQ];
     __shared__ float s_acc[NW][GQ][D];
@@ -324,9 +340,9 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
     const unsigned char* vb = p.v + (int64_t)r * p.v_sn + (int64_t)b * p.v_sb + (int64_t)hkv * p.v_sh + 16 * qc;
     // lane (qr, qc) loads token tb + 8h + qr, bytes 64i + 16qc .. +15 of its row;
     // rows past the split are zeros (never read)
-    auto load_block = [&](uint4 (&kr)[2][NI], uint4 (&vr)[2][NI], int tb) {
+    auto load_block = [&](uint4 (&kr)[HB][NI], uint4 (&vr)[HB][NI], int tb) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < HB; ++h) {
             const int t = tb + 8 * h + qr;
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
@@ -339,38 +355,48 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
             }
         }
     };
-    auto merge_block = [&](const uint4 (&kr)[2][NI], const uint4 (&vr)[2][NI], int tb) {
+    auto merge_block = [&](const uint4 (&kr)[HB][NI], const uint4 (&vr)[HB][NI], int tb) {
         // scores of head qr for tokens tb + 8h + 2qc + {0,1}, in base-2 units
         // (the two halves' products alternate, so consecutive mma are independent)
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float c[HB][4];
+#pragma unroll
+        for (int h = 0; h < HB; ++h) c[h][0] = c[h][1] = c[h][2] = c[h][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const unsigned a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < HB; ++h) {
                 const uint4& kv = kr[h][ks >> 1];
                 mma_16816<T>(c[h], a, (ks & 1) ? kv.z : kv.x, (ks & 1) ? kv.w : kv.y);
             }
         }
-        float sc[2][2];
+        float sc[HB][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < HB; ++h)
 #pragma unroll
             for (int e = 0; e < 2; ++e) sc[h][e] = tb + 8 * h + 2 * qc + e < t1 ? c[h][e] * qscale : -INFINITY;
-        // online softmax of head qr over the quad's 16 tokens
-        float bm = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        // online softmax of head qr over the quad's TB tokens
+        float bm = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < HB; ++h) bm = fmaxf(bm, fmaxf(sc[h][0], sc[h][1]));
         bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
         bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
         const float mn = fmaxf(m_run, bm);
         float alpha = 1.f;
-        float pr[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        float pr[HB][2];
+#pragma unroll
+        for (int h = 0; h < HB; ++h) pr[h][0] = pr[h][1] = 0.f;
         if (head_ok && mn != -INFINITY) {
             alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
+            float ps = 0.f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < HB; ++h)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) pr[h][e] = exp2f(sc[h][e] - mn);  // masked: exp2(-inf) = 0
-            l_run = l_run * alpha + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+                for (int e = 0; e < 2; ++e) {
+                    pr[h][e] = exp2f(sc[h][e] - mn);  // masked: exp2(-inf) = 0
+                    ps += pr[h][e];
+                }
+            l_run = l_run * alpha + ps;
             m_run = mn;
         }
         // O^T columns are heads 2qc, 2qc+1: their rescale factors live in quads 2qc, 2qc+1
@@ -384,49 +410,59 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
             oacc[j][3] *= al1;
         }
         // P^T fragments: this lane's own probabilities, as hi + lo 16-bit terms
-        const unsigned ph0 = round_pair<T>(pr[0][0], pr[0][1]);
-        const unsigned ph1 = round_pair<T>(pr[1][0], pr[1][1]);
-        const float2 bh0 = unpack2(word_to_pair<T>(ph0));
-        const float2 bh1 = unpack2(word_to_pair<T>(ph1));
-        const unsigned pl0 = round_pair<T>(pr[0][0] - bh0.x, pr[0][1] - bh0.y);
-        const unsigned pl1 = round_pair<T>(pr[1][0] - bh1.x, pr[1][1] - bh1.y);
-        unsigned va[NM][4];
+        unsigned ph[HB], pl[HB];
 #pragma unroll
-        for (int j = 0; j < NM; ++j) {
-            const int x0 = 2 * j, x1 = 2 * j + 1;  // 8x8 tiles: word x%4 of piece x/4
-            va[j][0] = tile_transpose(word_of(vr[0][x0 >> 2], x0 & 3));
-            va[j][1] = tile_transpose(word_of(vr[0][x1 >> 2], x1 & 3));
-            va[j][2] = tile_transpose(word_of(vr[1][x0 >> 2], x0 & 3));
-            va[j][3] = tile_transpose(word_of(vr[1][x1 >> 2], x1 & 3));
+        for (int h = 0; h < HB; ++h) {
+            ph[h] = round_pair<T>(pr[h][0], pr[h][1]);
+            const float2 bh = unpack2(word_to_pair<T>(ph[h]));
+            pl[h] = round_pair<T>(pr[h][0] - bh.x, pr[h][1] - bh.y);
         }
+        // V^T fragments: 8x8 tiles x = 2j (rows 0-7) and 2j+1 (rows 8-15), word
+        // x%4 of piece x/4, one per 8-token half
+        unsigned va[NM][2 * HB];
+#pragma unroll
+        for (int j = 0; j < NM; ++j)
+#pragma unroll
+            for (int h = 0; h < HB; ++h) {
+                const int x0 = 2 * j, x1 = 2 * j + 1;
+                va[j][2 * h] = tile_transpose(word_of(vr[h][x0 >> 2], x0 & 3));
+                va[j][2 * h + 1] = tile_transpose(word_of(vr[h][x1 >> 2], x1 & 3));
+            }
         // hi terms of every d block, then lo terms: consecutive mma are independent
+        if constexpr (HB == 2) {
 #pragma unroll
-        for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], ph0, ph1);
+            for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], ph[0], ph[1]);
 #pragma unroll
-        for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], pl0, pl1);
+            for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], pl[0], pl[1]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < NM; ++j) mma_1688<T>(oacc[j], va[j], ph[0]);
+#pragma unroll
+            for (int j = 0; j < NM; ++j) mma_1688<T>(oacc[j], va[j], pl[0]);
+        }
     };
     const int stride = NW * TB;
-#if DCP_ATTN_PREFETCH
-    // two register sets: the next block's loads are in flight while this one merges
-    uint4 ka[2][NI], va[2][NI], kn[2][NI], vn[2][NI];
-    int tb = t0 + warp * TB;  // uniform across the warp
-    if (tb < t1) load_block(ka, va, tb);
-    while (tb < t1) {
-        if (tb + stride < t1) load_block(kn, vn, tb + stride);
-        merge_block(ka, va, tb);
-        tb += stride;
-        if (tb >= t1) break;
-        if (tb + stride < t1) load_block(ka, va, tb + stride);
-        merge_block(kn, vn, tb);
-        tb += stride;
+    if constexpr (PF) {
+        // two register sets: the next block's loads are in flight while this one merges
+        uint4 ka[HB][NI], va[HB][NI], kn[HB][NI], vn[HB][NI];
+        int tb = t0 + warp * TB;  // uniform across the warp
+        if (tb < t1) load_block(ka, va, tb);
+        while (tb < t1) {
+            if (tb + stride < t1) load_block(kn, vn, tb + stride);
+            merge_block(ka, va, tb);
+            tb += stride;
+            if (tb >= t1) break;
+            if (tb + stride < t1) load_block(ka, va, tb + stride);
+            merge_block(kn, vn, tb);
+            tb += stride;
+        }
+    } else {
+        for (int tb = t0 + warp * TB; tb < t1; tb += stride) {  // uniform across the warp
+            uint4 kr[HB][NI], vr[HB][NI];
+            load_block(kr, vr, tb);
+            merge_block(kr, vr, tb);
+        }
     }
-#else
-    for (int tb = t0 + warp * TB; tb < t1; tb += stride) {  // uniform across the warp
-        uint4 kr[2][NI], vr[2][NI];
-        load_block(kr, vr, tb);
-        merge_block(kr, vr, tb);
-    }
-#endif
 
     // the quad's partial sums of head qr, then the warp's state to shared memory:
     // output row qr of tile x is d = 32(x/4) + 8(qr/2) + 2(x%4) + qr%2
@@ -491,12 +527,17 @@ __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const
 template <typename T, int D>
 static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) {
     const void* k;
-    // grouped-query heads go to the tensor cores (D <= 128 fits the lane's
-    // registers); one query head per KV head stays on the CUDA cores
-    if constexpr (D <= 128 && DCP_ATTN_MMA) {
+    // grouped-query heads go to the tensor cores; one query head per KV head
+    // stays on the CUDA cores, and so do two at D = 256 (measured: 1.51 ms on
+    // the CUDA cores against 1.71 ms for the 8-token tensor-core blocks that
+    // D = 256 is limited to by registers; from four heads up the tensor
+    // cores win, 0.90 vs 1.28 ms and 0.51 vs 1.38 ms)
+    if constexpr (DCP_ATTN_MMA) {
         switch (p.H / p.Hkv) {
             case 1: k = (const void*)decode_partial_kernel<T, D, 1>; break;
-            case 2: k = (const void*)decode_partial_mma_kernel<T, D, 2>; break;
+            case 2:
+                k = D == 256 ? (const void*)decode_partial_kernel<T, D, 2> : (const void*)decode_partial_mma_kernel<T, D, 2>;
+                break;
             case 4: k = (const void*)decode_partial_mma_kernel<T, D, 4>; break;
             case 8: k = (const void*)decode_partial_mma_kernel<T, D, 8>; break;
             default: return cudaErrorInvalidValue;

@@ -105,6 +105,8 @@ CASES = [
     (4, 2, 16, 4, 64, [1, 31, 64, 999], torch.float16, "e", 24),
     (1, 2, 8, 1, 128, [3, 700], torch.bfloat16, "2", 4096),
     (3, 2, 4, 2, 64, [2, 18, 95], torch.bfloat16, "e", 7),
+    (2, 3, 16, 2, 256, [1, 9, 300], torch.float16, "e", 64),
+    (3, 1, 8, 4, 256, [77], torch.bfloat16, "2", 16),
 ]
 
 
