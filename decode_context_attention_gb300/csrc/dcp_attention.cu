@@ -219,9 +219,10 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
 // every K/V byte feeds 2 G_q multiply-adds (scores and output), more than the
 // CUDA cores sustain at HBM speed beyond G_q = 2, so for G_q in {2, 4, 8} the
 // products run as warp-level mma.sync (bf16 or f16 operands, fp32
-// accumulation).  One warp takes blocks of 16 tokens of its CTA's split:
+// accumulation).  One warp takes blocks of 16 tokens (8 at D = 256, where the
+// registers hold no more) of its CTA's split, per 8-token half:
 //   S   [16 x 8 tokens]  = Q [16 rows: the G_q heads, the rest zero] . K^T
-//   O^T [D x 8 heads]   += V^T [D x 16 tokens] . P^T [16 tokens x 8 heads]
+//   O^T [D x 8 heads]   += V^T [D x tokens] . P^T [tokens x 8 heads]
 // K and V rows arrive by 16-byte loads; the contraction over D does not
 // depend on the order of its terms, so the d positions each lane loads are
 // simply the ones it feeds to the fragments (Q is read in the same order),
@@ -235,14 +236,14 @@ template <typename T>
 __device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4], unsigned b0, unsigned b1) {
     if constexpr (std::is_same<T, __half>::value)
         asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-                     "{%8,%9}, {%0,%1,%2,%3};\n"
-                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+            "{%8,%9}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     else
         asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-                     "{%8,%9}, {%0,%1,%2,%3};\n"
-                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+            "{%8,%9}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 template <typename T>
