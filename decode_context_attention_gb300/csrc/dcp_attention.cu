@@ -22,6 +22,9 @@
 //  * each lane group keeps an online softmax in base 2 (scores pre-scaled by
 //    log2 e, exp2f) per query head, rescaled once per block of 4 tokens whose
 //    K and V loads are all issued first;
+//  * grouped-query heads (2..8 per KV head) instead run the score and output
+//    products on the tensor cores (decode_partial_mma_kernel below), since
+//    their multiply-adds per byte outrun the CUDA cores;
 //  * the CTA's lane groups merge their states through shared memory; with one
 //    split the CTA writes (O_r, lse_r) directly, otherwise an fp32 partial
 //    (O, lse) per split goes to the caller's workspace and a second kernel
