@@ -466,8 +466,8 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
         return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
     if (B == 0) return ok();
     const int nsplit = attn_nsplit(N, max_seq_len, split_tokens);
-    if ((int64_t)N * B * Hkv >= (1ll << 31) || nsplit > 65535)
-        return fail(DCP_ERR_INVALID_ARG, "%s: too many work items", who);
+    if ((int64_t)N * B * Hkv * nsplit >= (1ll << 31))
+        return fail(DCP_ERR_INVALID_ARG, "%s: too many work items (N*B*Hkv*splits >= 2^31)", who);
     if (!q || !k || !v || !seq_lens || !o || !lse)
         return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
     if (any_negative({q_sb, q_sh, k_sn, k_sb, k_st, k_sh, v_sn, v_sb, v_st, v_sh, o_sn, o_sb, o_sh, l_sn, l_sb, l_sh}))

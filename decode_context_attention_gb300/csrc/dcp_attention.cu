@@ -64,6 +64,13 @@ __device__ __forceinline__ void vec8_to_f32(const uint4& v, float (&f)[8]) {
     }
 }
 
+// Work item (rank, request, KV head) and split of a CTA in a 1-D grid with the
+// split fastest: the splits of one item are neighbours in launch order, so a
+// long request's splits start together instead of every second split
+// trailing at the end of the launch (GQ = 8: 186.9 -> 181.4 us).
+__device__ __forceinline__ int attn_item(int nsplit) { return (int)(blockIdx.x / (unsigned)nsplit); }
+__device__ __forceinline__ int attn_split(int nsplit) { return (int)(blockIdx.x % (unsigned)nsplit); }
+
 // Local token count of rank r for a request of global length L (round robin).
 __device__ __forceinline__ int local_len(int L, int N, int r) { return L / N + (r < L % N ? 1 : 0); }
 
@@ -119,12 +126,13 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
     const int grp = warp * TPW + lane / LPT;
     const unsigned gmask = LPT == 32 ? 0xffffffffu : (((1u << LPT) - 1u) << ((lane / LPT) * LPT));
 
-    // work item: blockIdx.x = (r * B + b) * Hkv + hkv, blockIdx.y = split
-    const int hkv = blockIdx.x % p.Hkv;
-    const int rb = blockIdx.x / p.Hkv;
+    // work item (r * B + b) * Hkv + hkv and split, from the 1-D grid
+    const int item = attn_item(p.nsplit);
+    const int hkv = item % p.Hkv;
+    const int rb = item / p.Hkv;
     const int b = rb % p.B;
     const int r = rb / p.B;
-    const int split = blockIdx.y;
+    const int split = attn_split(p.nsplit);
     int L = p.seq_lens[b];
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
     const int Ll = local_len(L, p.N, r);
@@ -308,11 +316,12 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
     const int qr = lane >> 2;  // fragment row (score head / token row / output d row)
     const int qc = lane & 3;   // fragment column pair
 
-    const int hkv = blockIdx.x % p.Hkv;
-    const int rb = blockIdx.x / p.Hkv;
+    const int item = attn_item(p.nsplit);
+    const int hkv = item % p.Hkv;
+    const int rb = item / p.Hkv;
     const int b = rb % p.B;
     const int r = rb / p.B;
-    const int split = blockIdx.y;
+    const int split = attn_split(p.nsplit);
     int L = p.seq_lens[b];
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
     const int Ll = local_len(L, p.N, r);
@@ -556,7 +565,7 @@ static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) 
         }
     }
     void* args[] = {(void*)&p};
-    const dim3 grid((unsigned)((int64_t)p.N * p.B * p.Hkv), (unsigned)p.nsplit);
+    const dim3 grid((unsigned)((int64_t)p.N * p.B * p.Hkv * p.nsplit));  // split fastest
     cudaError_t e = cudaLaunchKernel(k, grid, dim3(kAttnThreads), args, 0, stream);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const int64_t rows = (int64_t)p.N * p.B * p.H;
