@@ -50,26 +50,6 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
 }
 
-// VB bytes of payload -> VB / sizeof(T) floats, and back (round to nearest even).
-template <typename T, int VB>
-__device__ __forceinline__ void unpack_vec(const typename VecT<VB>::type& v,
-                                           float (&f)[VB / sizeof(T)]) {
-    T e[VB / sizeof(T)];
-    memcpy(e, &v, VB);
-#pragma unroll
-    for (int i = 0; i < VB / (int)sizeof(T); ++i) f[i] = to_f32(e[i]);
-}
-
-template <typename T, int VB>
-__device__ __forceinline__ typename VecT<VB>::type pack_vec(const float (&f)[VB / sizeof(T)]) {
-    T e[VB / sizeof(T)];
-#pragma unroll
-    for (int i = 0; i < VB / (int)sizeof(T); ++i) e[i] = from_f32<T>(f[i]);
-    typename VecT<VB>::type v;
-    memcpy(&v, e, VB);
-    return v;
-}
-
 // ---- paired fp32 arithmetic (sm_100+ fma.rn.f32x2: two IEEE fp32 FMAs,
 // each rounded to nearest, in one instruction) ---------------------------------
 __device__ __forceinline__ float2 ffma2(float w, float2 x, float2 acc) {
