@@ -21,13 +21,18 @@
 //    exponentials are reduced with xor shuffles inside the group, then each
 //    rank's weight is broadcast to the group with one shuffle;
 //  * payload is streamed with 16-byte vectors when every row start is 16-byte
-//    aligned (4- or 2-byte otherwise); 16-bit elements are widened two at a
-//    time and accumulated with paired fp32 FMAs (fma.rn.f32x2), about 1.5
-//    instructions per element, so the merge stays below the HBM time;
-//  * two variants keep bytes in flight: a register variant issues all ranks'
-//    loads of a chunk before the weights are reduced; a staged variant copies
-//    the next rows' rank stack into shared memory with cp.async, rows several
-//    deep, while it merges the current row;
+//    aligned; rows that start only 4-byte aligned (the interleaved receive
+//    rows) are read as 16-byte-aligned chunks shifted per row when every rank
+//    shares the misalignment, else with 4- (or 2-) byte vectors; 16-bit
+//    elements are widened two at a time and accumulated with paired fp32 FMAs
+//    (fma.rn.f32x2), about 1.5 instructions per element, fp8 e4m3 pairs
+//    through the hardware e4m3x2 -> f16x2 convert, so the merge stays below
+//    the HBM time;
+//  * the register variants issue all ranks' loads of a chunk before the
+//    weights are reduced (fixed-shape templates for the common row lengths,
+//    runtime-shaped ones otherwise); a staged variant that copies the next
+//    rows' rank stack into shared memory with cp.async is built only on
+//    request (measured slower on GB300);
 //  * persistent grid: SM count x resident CTAs, grid-stride over rows with
 //    division-free row cursors.
 #pragma once
