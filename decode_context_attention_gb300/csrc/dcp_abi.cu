@@ -457,9 +457,11 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
                     who, N, B, H, Hkv, max_seq_len, split_tokens);
     if (H % Hkv) return fail(DCP_ERR_HEADS_NOT_DIVISIBLE, "%s: H=%d is not a multiple of Hkv=%d", who, H, Hkv);
     const int gq = H / Hkv;
-    if (gq != 1 && gq != 2 && gq != 4 && gq != 8)
-        return fail(DCP_ERR_INVALID_ARG, "%s: H/Hkv=%d (1, 2, 4 or 8 query heads per KV head)", who, gq);
+    if (gq != 1 && gq != 2 && gq != 4 && gq != 8 && gq != 16)
+        return fail(DCP_ERR_INVALID_ARG, "%s: H/Hkv=%d (1, 2, 4, 8 or 16 query heads per KV head)", who, gq);
     if (D != 64 && D != 128 && D != 256) return fail(DCP_ERR_INVALID_ARG, "%s: D=%d (64, 128 or 256)", who, D);
+    if (gq == 16 && D > 128)
+        return fail(DCP_ERR_INVALID_ARG, "%s: 16 query heads per KV head need D <= 128", who);
     if (!(sm_scale == sm_scale) || sm_scale == INFINITY || sm_scale == -INFINITY)
         return fail(DCP_ERR_INVALID_ARG, "%s: sm_scale is not finite", who);
     if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)

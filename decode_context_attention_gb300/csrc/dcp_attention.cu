@@ -228,12 +228,13 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
 // ---------------------------------------------------------------------------
 // Grouped-query heads on the tensor cores.  With G_q query heads per KV head
 // every K/V byte feeds 2 G_q multiply-adds (scores and output), more than the
-// CUDA cores sustain at HBM speed beyond G_q = 2, so for G_q in {2, 4, 8} the
-// products run as warp-level mma.sync (bf16 or f16 operands, fp32
+// CUDA cores sustain at HBM speed beyond G_q = 2, so for G_q in {2, 4, 8, 16}
+// the products run as warp-level mma.sync (bf16 or f16 operands, fp32
 // accumulation).  One warp takes blocks of 16 tokens (8 at D = 256, where the
 // registers hold no more) of its CTA's split, per 8-token half:
-//   S   [16 x 8 tokens]  = Q [16 rows: the G_q heads, the rest zero] . K^T
+//   S   [16 x 8 tokens]  = Q [16 rows: the G_q heads, zero past G_q] . K^T
 //   O^T [D x 8 heads]   += V^T [D x tokens] . P^T [tokens x 8 heads]
+// (the output product once per block of 8 heads: twice for G_q = 16).
 // K and V rows arrive by 16-byte loads; the contraction over D does not
 // depend on the order of its terms, so the d positions each lane loads are
 // simply the ones it feeds to the fragments (Q is read in the same order),
@@ -299,14 +300,16 @@ __device__ __forceinline__ unsigned word_of(const uint4& v, int w) {
 
 template <typename T, int D, int GQ>
 __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const AttnParams p) {
-    static_assert(D % 32 == 0 && GQ >= 1 && GQ <= 8, "fragment shapes");
+    static_assert(D % 32 == 0 && GQ >= 1 && GQ <= 16, "fragment shapes");
+    constexpr int NB = GQ > 8 ? 2 : 1;    // blocks of 8 query heads (fragment rows qr and qr + 8)
     constexpr int NI = D / 32;   // 16-byte pieces per lane per token row
     constexpr int KS = D / 16;   // k-steps of the score products
-    constexpr int NM = D / 16;   // output products (16 d each)
+    constexpr int NM = D / 16;   // output products (16 d each) per head block
     constexpr int NW = kAttnThreads / 32;
     constexpr int HB = D <= 128 ? 2 : 1;  // 8-token halves per warp block (registers bound D = 256 to one)
     constexpr int TB = 8 * HB;            // tokens per warp block
-    constexpr bool PF = DCP_ATTN_PREFETCH && D <= 128;  // second register set for the next block
+    // second register set for the next block, where the registers allow it
+    constexpr bool PF = DCP_ATTN_PREFETCH && D <= 128 && NB == 1;
     constexpr unsigned kFull = 0xffffffffu;
     __shared__ float s_m[NW][GQ], s_l[NW][GQ];
     __shared__ float s_acc[NW][GQ][D];
@@ -328,26 +331,33 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
     const int t0 = split * p.split_tokens;
     const int t1 = min(t0 + p.split_tokens, Ll);
 
-    // Q fragments: row qr is head hkv*GQ + qr (zero for qr >= GQ); k-step ks
-    // takes d = 32(ks/2) + 8qc + 4(ks%2) + {0,1} and that + 2, the positions
-    // the K fragments below carry
-    const bool head_ok = qr < GQ;
-    unsigned qa[KS][2];
-    {
+    // Q fragments: fragment row qr + 8nb is head hkv*GQ + 8nb + qr (zero past
+    // GQ); k-step ks takes d = 32(ks/2) + 8qc + 4(ks%2) + {0,1} and that + 2,
+    // the positions the K fragments below carry
+    bool head_ok[NB];
+    unsigned qa[KS][NB][2];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        head_ok[nb] = 8 * nb + qr < GQ;
         const unsigned char* qrow =
-            p.q + (int64_t)b * p.q_sb + (int64_t)(hkv * GQ + (head_ok ? qr : 0)) * p.q_sh;
+            p.q + (int64_t)b * p.q_sb + (int64_t)(hkv * GQ + (head_ok[nb] ? 8 * nb + qr : 0)) * p.q_sh;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const int d0 = 32 * (ks >> 1) + 8 * qc + 4 * (ks & 1);
-            qa[ks][0] = head_ok ? *reinterpret_cast<const unsigned*>(qrow + 2 * d0) : 0u;
-            qa[ks][1] = head_ok ? *reinterpret_cast<const unsigned*>(qrow + 2 * (d0 + 2)) : 0u;
+            qa[ks][nb][0] = head_ok[nb] ? *reinterpret_cast<const unsigned*>(qrow + 2 * d0) : 0u;
+            qa[ks][nb][1] = head_ok[nb] ? *reinterpret_cast<const unsigned*>(qrow + 2 * (d0 + 2)) : 0u;
         }
     }
     const float qscale = p.sm_scale * kLog2e;
-    float m_run = -INFINITY, l_run = 0.f;
-    float oacc[NM][4];
+    float m_run[NB], l_run[NB];
+    float oacc[NB][NM][4];
 #pragma unroll
-    for (int j = 0; j < NM; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+    for (int nb = 0; nb < NB; ++nb) {
+        m_run[nb] = -INFINITY;
+        l_run[nb] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NM; ++j) oacc[nb][j][0] = oacc[nb][j][1] = oacc[nb][j][2] = oacc[nb][j][3] = 0.f;
+    }
 
     const unsigned char* kb = p.k + (int64_t)r * p.k_sn + (int64_t)b * p.k_sb + (int64_t)hkv * p.k_sh + 16 * qc;
     const unsigned char* vb = p.v + (int64_t)r * p.v_sn + (int64_t)b * p.v_sb + (int64_t)hkv * p.v_sh + 16 * qc;
@@ -369,67 +379,78 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
         }
     };
     auto merge_block = [&](const uint4 (&kr)[HB][NI], const uint4 (&vr)[HB][NI], int tb) {
-        // scores of head qr for tokens tb + 8h + 2qc + {0,1}, in base-2 units
-        // (the two halves' products alternate, so consecutive mma are independent)
+        // scores of heads qr (c0, c1) and qr + 8 (c2, c3) for tokens
+        // tb + 8h + 2qc + {0,1}; the halves' products alternate, so
+        // consecutive mma are independent
         float c[HB][4];
 #pragma unroll
         for (int h = 0; h < HB; ++h) c[h][0] = c[h][1] = c[h][2] = c[h][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            const unsigned a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+            const unsigned a[4] = {qa[ks][0][0], NB > 1 ? qa[ks][NB - 1][0] : 0u, qa[ks][0][1],
+                                   NB > 1 ? qa[ks][NB - 1][1] : 0u};
 #pragma unroll
             for (int h = 0; h < HB; ++h) {
                 const uint4& kv = kr[h][ks >> 1];
                 mma_16816<T>(c[h], a, (ks & 1) ? kv.z : kv.x, (ks & 1) ? kv.w : kv.y);
             }
         }
-        float sc[HB][2];
+        // online softmax (base 2) of each of the lane's heads over the quad's TB tokens
+        float alpha[NB], pr[NB][HB][2];
 #pragma unroll
-        for (int h = 0; h < HB; ++h)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) sc[h][e] = tb + 8 * h + 2 * qc + e < t1 ? c[h][e] * qscale : -INFINITY;
-        // online softmax of head qr over the quad's TB tokens
-        float bm = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < HB; ++h) bm = fmaxf(bm, fmaxf(sc[h][0], sc[h][1]));
-        bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
-        bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
-        const float mn = fmaxf(m_run, bm);
-        float alpha = 1.f;
-        float pr[HB][2];
-#pragma unroll
-        for (int h = 0; h < HB; ++h) pr[h][0] = pr[h][1] = 0.f;
-        if (head_ok && mn != -INFINITY) {
-            alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
-            float ps = 0.f;
+        for (int nb = 0; nb < NB; ++nb) {
+            float sc[HB][2];
+            float bm = -INFINITY;
 #pragma unroll
             for (int h = 0; h < HB; ++h)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    pr[h][e] = exp2f(sc[h][e] - mn);  // masked: exp2(-inf) = 0
-                    ps += pr[h][e];
+                    sc[h][e] = tb + 8 * h + 2 * qc + e < t1 ? c[h][2 * nb + e] * qscale : -INFINITY;
+                    bm = fmaxf(bm, sc[h][e]);
+                    pr[nb][h][e] = 0.f;
                 }
-            l_run = l_run * alpha + ps;
-            m_run = mn;
-        }
-        // O^T columns are heads 2qc, 2qc+1: their rescale factors live in quads 2qc, 2qc+1
-        const float al0 = __shfl_sync(kFull, alpha, 8 * qc);
-        const float al1 = __shfl_sync(kFull, alpha, 8 * qc + 4);
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+            const float mn = fmaxf(m_run[nb], bm);
+            alpha[nb] = 1.f;
+            if (head_ok[nb] && mn != -INFINITY) {
+                alpha[nb] = m_run[nb] == -INFINITY ? 0.f : exp2f(m_run[nb] - mn);
+                float ps = 0.f;
 #pragma unroll
-        for (int j = 0; j < NM; ++j) {
-            oacc[j][0] *= al0;
-            oacc[j][1] *= al1;
-            oacc[j][2] *= al0;
-            oacc[j][3] *= al1;
+                for (int h = 0; h < HB; ++h)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        pr[nb][h][e] = exp2f(sc[h][e] - mn);  // masked: exp2(-inf) = 0
+                        ps += pr[nb][h][e];
+                    }
+                l_run[nb] = l_run[nb] * alpha[nb] + ps;
+                m_run[nb] = mn;
+            }
+        }
+        // O^T columns of head block nb are heads 8nb + 2qc + {0,1}: their rescale
+        // factors live in quads 2qc and 2qc + 1
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const float al0 = __shfl_sync(kFull, alpha[nb], 8 * qc);
+            const float al1 = __shfl_sync(kFull, alpha[nb], 8 * qc + 4);
+#pragma unroll
+            for (int j = 0; j < NM; ++j) {
+                oacc[nb][j][0] *= al0;
+                oacc[nb][j][1] *= al1;
+                oacc[nb][j][2] *= al0;
+                oacc[nb][j][3] *= al1;
+            }
         }
         // P^T fragments: this lane's own probabilities, as hi + lo 16-bit terms
-        unsigned ph[HB], pl[HB];
+        unsigned ph[NB][HB], pl[NB][HB];
 #pragma unroll
-        for (int h = 0; h < HB; ++h) {
-            ph[h] = round_pair<T>(pr[h][0], pr[h][1]);
-            const float2 bh = unpack2(word_to_pair<T>(ph[h]));
-            pl[h] = round_pair<T>(pr[h][0] - bh.x, pr[h][1] - bh.y);
-        }
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int h = 0; h < HB; ++h) {
+                ph[nb][h] = round_pair<T>(pr[nb][h][0], pr[nb][h][1]);
+                const float2 bh = unpack2(word_to_pair<T>(ph[nb][h]));
+                pl[nb][h] = round_pair<T>(pr[nb][h][0] - bh.x, pr[nb][h][1] - bh.y);
+            }
         // V^T fragments: 8x8 tiles x = 2j (rows 0-7) and 2j+1 (rows 8-15), word
         // x%4 of piece x/4, one per 8-token half
         unsigned va[NM][2 * HB];
@@ -441,18 +462,18 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
                 va[j][2 * h] = tile_transpose(word_of(vr[h][x0 >> 2], x0 & 3));
                 va[j][2 * h + 1] = tile_transpose(word_of(vr[h][x1 >> 2], x1 & 3));
             }
-        // hi terms of every d block, then lo terms: consecutive mma are independent
-        if constexpr (HB == 2) {
+        // hi terms of every (head block, d block), then lo terms: consecutive mma
+        // are independent
 #pragma unroll
-            for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], ph[0], ph[1]);
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int j = 0; j < NM; ++j) mma_16816<T>(oacc[j], va[j], pl[0], pl[1]);
-        } else {
+            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int j = 0; j < NM; ++j) mma_1688<T>(oacc[j], va[j], ph[0]);
-#pragma unroll
-            for (int j = 0; j < NM; ++j) mma_1688<T>(oacc[j], va[j], pl[0]);
-        }
+                for (int j = 0; j < NM; ++j) {
+                    const unsigned* pb = t == 0 ? ph[nb] : pl[nb];
+                    if constexpr (HB == 2) mma_16816<T>(oacc[nb][j], va[j], pb[0], pb[1]);
+                    else mma_1688<T>(oacc[nb][j], va[j], pb[0]);
+                }
     };
     const int stride = NW * TB;
     if constexpr (PF) {
@@ -477,23 +498,27 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
         }
     }
 
-    // the quad's partial sums of head qr, then the warp's state to shared memory:
-    // output row qr of tile x is d = 32(x/4) + 8(qr/2) + 2(x%4) + qr%2
-    l_run += __shfl_xor_sync(kFull, l_run, 1);
-    l_run += __shfl_xor_sync(kFull, l_run, 2);
-    if (head_ok && qc == 0) {
-        s_m[warp][qr] = m_run;
-        s_l[warp][qr] = l_run;
-    }
+    // the quad's partial sums of each head, then the warp's state to shared
+    // memory: output row qr of tile x is d = 32(x/4) + 8(qr/2) + 2(x%4) + qr%2
 #pragma unroll
-    for (int j = 0; j < NM; ++j)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int x = 2 * j + half;
-            const int d = 32 * (x >> 2) + 8 * (qr >> 1) + 2 * (x & 3) + (qr & 1);
-            if (2 * qc < GQ) s_acc[warp][2 * qc][d] = oacc[j][2 * half];
-            if (2 * qc + 1 < GQ) s_acc[warp][2 * qc + 1][d] = oacc[j][2 * half + 1];
+    for (int nb = 0; nb < NB; ++nb) {
+        l_run[nb] += __shfl_xor_sync(kFull, l_run[nb], 1);
+        l_run[nb] += __shfl_xor_sync(kFull, l_run[nb], 2);
+        if (head_ok[nb] && qc == 0) {
+            s_m[warp][8 * nb + qr] = m_run[nb];
+            s_l[warp][8 * nb + qr] = l_run[nb];
         }
+#pragma unroll
+        for (int j = 0; j < NM; ++j)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int x = 2 * j + half;
+                const int d = 32 * (x >> 2) + 8 * (qr >> 1) + 2 * (x & 3) + (qr & 1);
+                const int g0 = 8 * nb + 2 * qc;
+                if (g0 < GQ) s_acc[warp][g0][d] = oacc[nb][j][2 * half];
+                if (g0 + 1 < GQ) s_acc[warp][g0 + 1][d] = oacc[nb][j][2 * half + 1];
+            }
+    }
     __syncthreads();
     write_cta_result<T, D, GQ, NW>(p, r, b, hkv, split, s_m, s_l, s_acc);
 }
@@ -553,6 +578,10 @@ static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) 
                 break;
             case 4: k = (const void*)decode_partial_mma_kernel<T, D, 4>; break;
             case 8: k = (const void*)decode_partial_mma_kernel<T, D, 8>; break;
+            case 16:
+                if constexpr (D <= 128) k = (const void*)decode_partial_mma_kernel<T, D, 16>;
+                else return cudaErrorInvalidValue;  // refused by the host checks
+                break;
             default: return cudaErrorInvalidValue;
         }
     } else {

@@ -234,7 +234,8 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
  *   lse      [N, B, H]              fp32, strides (l_sn, l_sb, l_sh)
  *
  * dtype: DCP_F16 or DCP_BF16 (q, k, v and o); D in {64, 128, 256}; H / Hkv in
- * {1, 2, 4, 8}; q, k and v rows start on 16-byte boundaries.  Work is split
+ * {1, 2, 4, 8, 16} (16 only with D <= 128); q, k and v rows start on 16-byte
+ * boundaries.  Work is split
  * into chunks of `split_tokens` local tokens; with more than one chunk the
  * partial results go through `workspace` (caller-owned device memory, 16-byte
  * aligned, at least dcp_decode_attention_workspace_size(...) bytes; NULL is

@@ -159,6 +159,8 @@ def test_decode_attention_validation(lib):
     assert attn(dtype=FP8) == 2
     assert attn(H=6, Hkv=4) == 3
     assert attn(H=6, Hkv=2) == 1               # three query heads per KV head
+    assert attn(H=64, Hkv=2) == 1              # 32 query heads per KV head
+    assert attn(H=32, Hkv=2, D=256) == 1       # 16 per KV head only with D <= 128
     assert attn(D=96) == 1
     assert attn(split=0) == 1
     assert attn(scale=float("nan")) == 1

@@ -106,6 +106,9 @@ CASES = [
     (1, 2, 8, 1, 128, [3, 700], torch.bfloat16, "2", 4096),
     (3, 2, 4, 2, 64, [2, 18, 95], torch.bfloat16, "e", 7),
     (2, 3, 16, 2, 256, [1, 9, 300], torch.float16, "e", 64),
+    # 16 query heads per KV head (two blocks of 8 fragment rows)
+    (2, 2, 32, 2, 128, [3, 250, 1025], torch.bfloat16, "2", 96),
+    (3, 2, 16, 1, 64, [1, 17, 400], torch.float16, "e", 40),
     (3, 1, 8, 4, 256, [77], torch.bfloat16, "2", 16),
 ]
 
