@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
     constexpr int HB = D <= 128 ? 2 : 1;  // 8-token halves per warp block (registers bound D = 256 to one)
     constexpr int TB = 8 * HB;            // tokens per warp block
     // second register set for the next block, where the registers allow it
-    constexpr bool PF = DCP_ATTN_PREFETCH && D <= 128 && NB == 1;
+    constexpr bool PF = DCP_ATTN_PREFETCH && (NB == 1 ? D <= 128 : D <= 64);
     constexpr unsigned kFull = 0xffffffffu;
     __shared__ float s_m[NW][GQ], s_l[NW][GQ];
     __shared__ float s_acc[NW][GQ][D];
