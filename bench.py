@@ -364,7 +364,28 @@ def setup_cached_extend(device, tokens=None, slices=False):
             "bytes": [bytes_merge(1, N, T, H, D, 4)] * 2}
 
 
-def setup_decode_attention(device, split_tokens=1024, batch=None, name="mha_decode_attention"):
+def page_pools(k, v, page_size, seed=0):
+    """Each rank's local caches [N, B, Lc, Hkv, D] moved into a page pool
+    [N, B * max_pages, page_size, Hkv, D] in a shuffled page order, with the
+    page table [N, B, max_pages] int32 that finds them."""
+    import torch
+
+    N, B, Lc, Hkv, D = k.shape
+    max_pages = (Lc + page_size - 1) // page_size
+    g = torch.Generator().manual_seed(seed)
+    bt = torch.stack([torch.randperm(B * max_pages, generator=g) for _ in range(N)]).to(k.device)
+    pools = []
+    for src in (k, v):
+        pool = torch.empty((N, B * max_pages, page_size, Hkv, D), dtype=src.dtype, device=src.device)
+        for r in range(N):
+            pad = torch.zeros((B, max_pages * page_size, Hkv, D), dtype=src.dtype, device=src.device)
+            pad[:, :Lc] = src[r]
+            pool[r, bt[r]] = pad.view(B * max_pages, page_size, Hkv, D)
+        pools.append(pool)
+    return pools[0], pools[1], bt.view(N, B, max_pages).to(torch.int32)
+
+
+def setup_decode_attention(device, split_tokens=1024, batch=None, name="mha_decode_attention", page_size=0):
     import math
 
     import torch
@@ -379,17 +400,26 @@ def setup_decode_attention(device, split_tokens=1024, batch=None, name="mha_deco
     lse = torch.empty((N, B, H), dtype=torch.float32, device=device)
     nbytes = binding.workspace_bytes(N, B, H, D, a["max_len"], split_tokens)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
-    call = binding.prepare_decode_attention(a["q"], a["k"], a["v"], a["seq_lens"], a["max_len"], o, lse,
-                                            1.0 / math.sqrt(D), base=c["base"], split_tokens=split_tokens,
-                                            workspace=ws)
+    if page_size:
+        kp, vp, bt = page_pools(a["k"], a["v"], page_size)
+        del a["k"], a["v"]
+        a["k_pages"], a["v_pages"], a["block_table"] = kp, vp, bt
+        call = binding.prepare_decode_attention_paged(a["q"], kp, vp, bt, a["seq_lens"], a["max_len"], o, lse,
+                                                      1.0 / math.sqrt(D), base=c["base"],
+                                                      split_tokens=split_tokens, workspace=ws)
+    else:
+        call = binding.prepare_decode_attention(a["q"], a["k"], a["v"], a["seq_lens"], a["max_len"], o, lse,
+                                                1.0 / math.sqrt(D), base=c["base"], split_tokens=split_tokens,
+                                                workspace=ws)
     tokens = int(a["seq_lens"].sum().item())
     e = a["q"].element_size()
     # K and V rows of every owned token, each rank's read of q, O and LSE written
     algo = 2 * tokens * Hkv * D * e + N * B * H * D * e + N * B * H * D * e + N * B * H * 4
     return {"launches": [call], "keep": (a, o, lse, ws), "tokens": tokens, "workspace_bytes": nbytes,
             "name": name,
-            "names": [f"dcp_decode_attention (N={N} B={B} H={H} Hkv={Hkv} D={D} bf16, "
-                      f"{tokens} KV tokens, splits of {split_tokens})"],
+            "names": [f"dcp_decode_attention{'_paged' if page_size else ''} (N={N} B={B} H={H} Hkv={Hkv} "
+                      f"D={D} bf16, {tokens} KV tokens, splits of {split_tokens}"
+                      f"{f', {page_size}-token pages' if page_size else ''})"],
             "bytes": [algo]}
 
 
@@ -718,13 +748,15 @@ def run_gpu(args):
             del sw
         # splits of local tokens per CTA: 1024 for MHA, 2048 for GQA (measured
         # best among 256..2048: fewer split partials to write and merge)
-        for att_name, att_split in (("mha_decode_attention", 1024), ("gqa_decode_attention", 2048)):
-            at = setup_decode_attention(device, split_tokens=att_split, name=att_name)
+        for att_name, att_split, att_page in (("mha_decode_attention", 1024, 0), ("gqa_decode_attention", 2048, 0),
+                                              ("gqa_decode_attention", 2048, 64)):
+            at = setup_decode_attention(device, split_tokens=att_split, name=att_name, page_size=att_page)
             p4, _ = time_sequence(at["launches"], max(10, args.steps // 20), 3, flush, device)
-            rec = {"workload": f"{att_name} (the step before the merge)",
+            rec = {"workload": f"{att_name}{f' over {att_page}-token pages' if att_page else ''} "
+                               "(the step before the merge)",
                    "workspace_bytes": at["workspace_bytes"],
                    "kernels": [kernel_record(at["names"][0], p4[0], at["bytes"][0], peak)]}
-            if rank == 0 and not args.no_cpu_baseline:
+            if rank == 0 and not args.no_cpu_baseline and not att_page:  # paging leaves the arithmetic alone
                 us, el, n = time_oracle_attention(at, min(5.0, args.cpu_budget))
                 rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": 1,
                                      "sample": f"{n} sampled (request, head) rows, {el:.1f} s, scaled by KV tokens"}

@@ -37,7 +37,7 @@ STATUS_NAMES = {0: "DCP_OK", 1: "DCP_ERR_INVALID_ARG", 2: "DCP_ERR_UNSUPPORTED_D
 # Every symbol include/dcp.h declares.
 EXPORTS = ("dcp_lse_pack_dim", "dcp_status_string", "dcp_last_error_message", "dcp_pack_send",
            "dcp_lse_combine", "dcp_unpack_combine", "dcp_decode_attention_workspace_size",
-           "dcp_decode_attention", "dcp_decode_attention_noalloc")
+           "dcp_decode_attention", "dcp_decode_attention_paged", "dcp_decode_attention_noalloc")
 
 
 class DcpError(RuntimeError):
@@ -84,6 +84,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                              + [vp, i64, i64, i64, i64] + [vp, i32, ctypes.c_float, i32]
                                              + [vp, i64, i64, i64] + [vp, i64, i64, i64]
                                              + [i32, vp, ctypes.c_size_t, vp])
+        lib.dcp_decode_attention_paged.restype = i32
+        lib.dcp_decode_attention_paged.argtypes = ([i32] * 6 + [vp, i64, i64] + [vp, i64, i64, i64, i64]
+                                                   + [vp, i64, i64, i64, i64] + [i32, i32]
+                                                   + [vp, i64, i64, i32]
+                                                   + lib.dcp_decode_attention.argtypes[19:])
         lib.dcp_decode_attention_noalloc.restype = i32
         lib.dcp_decode_attention_noalloc.argtypes = lib.dcp_decode_attention.argtypes[:-3] + [vp]
         _lib = lib
@@ -297,6 +302,46 @@ def prepare_decode_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
             _base_code(base), None if workspace is None else workspace.data_ptr(), ws_bytes,
             _stream_handle(stream))
     return _Prepared("dcp_decode_attention", args, (q, k, v, seq_lens, o, lse, workspace))
+
+
+def prepare_decode_attention_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                                   block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                                   o: torch.Tensor, lse: torch.Tensor, sm_scale: float, base: str = "e",
+                                   split_tokens: int = 1024, workspace: torch.Tensor | None = None,
+                                   stream=None) -> _Prepared:
+    """prepare_decode_attention over paged caches: k_pages, v_pages
+    [N, num_pages, page_size, Hkv, D]; block_table [N, B, max_pages] int32, local
+    token i of request b on rank r in slot i % page_size of page
+    block_table[r, b, i // page_size]."""
+    _need_cuda(q, k_pages, v_pages, block_table, seq_lens, o, lse, workspace)
+    if seq_lens.dtype != torch.int32 or block_table.dtype != torch.int32:
+        raise ValueError("seq_lens and block_table must be int32")
+    if block_table.dim() != 3 or block_table.shape[-1] > 1 and block_table.stride(-1) != 1:
+        raise ValueError("block_table is [N, B, max_pages] with unit stride along the pages")
+    for t in (q, k_pages, v_pages, o):
+        _inner_ok(t)
+    B, H, D = q.shape
+    N, num_pages, page_size, Hkv, _ = k_pages.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = (_dtype_code(q), N, B, H, Hkv, D,
+            q.data_ptr(), q.stride(0), q.stride(1),
+            k_pages.data_ptr(), k_pages.stride(0), k_pages.stride(1), k_pages.stride(2), k_pages.stride(3),
+            v_pages.data_ptr(), v_pages.stride(0), v_pages.stride(1), v_pages.stride(2), v_pages.stride(3),
+            num_pages, page_size,
+            block_table.data_ptr(), block_table.stride(0), block_table.stride(1), block_table.shape[2],
+            seq_lens.data_ptr(), int(max_seq_len), float(sm_scale), int(split_tokens),
+            o.data_ptr(), o.stride(0), o.stride(1), o.stride(2),
+            lse.data_ptr(), lse.stride(0), lse.stride(1), lse.stride(2),
+            _base_code(base), None if workspace is None else workspace.data_ptr(), ws_bytes,
+            _stream_handle(stream))
+    return _Prepared("dcp_decode_attention_paged", args,
+                     (q, k_pages, v_pages, block_table, seq_lens, o, lse, workspace))
+
+
+def decode_attention_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, o, lse, sm_scale, base="e",
+                           split_tokens=1024, workspace=None, stream=None) -> None:
+    prepare_decode_attention_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, o, lse, sm_scale,
+                                   base, split_tokens, workspace, stream)()
 
 
 def decode_attention(q, k, v, seq_lens, max_seq_len, o, lse, sm_scale, base="e", split_tokens=1024,

@@ -440,15 +440,25 @@ size_t dcp_decode_attention_workspace_size(int N, int B, int H, int D, int max_s
     return attn_workspace_bytes(N, B, H, D, attn_nsplit(N, max_seq_len, split_tokens));
 }
 
-dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D,
-                                  const void* q, int64_t q_sb, int64_t q_sh,
-                                  const void* k, int64_t k_sn, int64_t k_sb, int64_t k_st, int64_t k_sh,
-                                  const void* v, int64_t v_sn, int64_t v_sb, int64_t v_st, int64_t v_sh,
+// Where the K/V rows live: per-request contiguous local caches, or pages of a
+// per-rank pool addressed through a page table.
+struct AttnKv {
+    const void* k;
+    int64_t k_sn, k_sb, k_st, k_sh;  // k_sb: request stride (contiguous) or page stride (paged)
+    const void* v;
+    int64_t v_sn, v_sb, v_st, v_sh;
+    bool paged;
+    int num_pages, page_size, max_pages;
+    const int* bt;
+    int64_t bt_sn, bt_sb;
+};
+
+static dcp_status_t run_attention(const char* who, int dtype, int N, int B, int H, int Hkv, int D,
+                                  const void* q, int64_t q_sb, int64_t q_sh, const AttnKv& kv,
                                   const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
                                   void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
                                   float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
                                   int lse_base, void* workspace, size_t workspace_bytes, void* stream) {
-    const char* who = "dcp_decode_attention";
     if (dtype != DCP_F16 && dtype != DCP_BF16)
         return fail(DCP_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d (f16 or bf16 caches only)", who, dtype);
     const int e = 2;
@@ -466,27 +476,46 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
         return fail(DCP_ERR_INVALID_ARG, "%s: sm_scale is not finite", who);
     if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)
         return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
+    const int64_t lcap = ((int64_t)max_seq_len + N - 1) / N;  // local tokens a rank may hold
+    int page_shift = -1;
+    if (kv.paged) {
+        if (kv.page_size < 1 || kv.page_size > (1 << 16) || (kv.page_size & (kv.page_size - 1)))
+            return fail(DCP_ERR_INVALID_ARG, "%s: page_size %d (a power of two up to 65536)", who, kv.page_size);
+        page_shift = 0;
+        while ((1 << page_shift) < kv.page_size) ++page_shift;
+        if (kv.num_pages < 1) return fail(DCP_ERR_INVALID_ARG, "%s: num_pages %d", who, kv.num_pages);
+        const int64_t need_pages = (lcap + kv.page_size - 1) / kv.page_size;
+        if (kv.max_pages < need_pages)
+            return fail(DCP_ERR_INVALID_ARG, "%s: page table rows of %d entries; %lld needed for %lld local tokens",
+                        who, kv.max_pages, (long long)need_pages, (long long)lcap);
+    }
     if (B == 0) return ok();
     const int nsplit = attn_nsplit(N, max_seq_len, split_tokens);
     if ((int64_t)N * B * Hkv * nsplit >= (1ll << 31))
         return fail(DCP_ERR_INVALID_ARG, "%s: too many work items (N*B*Hkv*splits >= 2^31)", who);
-    if (!q || !k || !v || !seq_lens || !o || !lse)
+    if (!q || !kv.k || !kv.v || !seq_lens || !o || !lse || (kv.paged && !kv.bt))
         return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
-    if (any_negative({q_sb, q_sh, k_sn, k_sb, k_st, k_sh, v_sn, v_sb, v_st, v_sh, o_sn, o_sb, o_sh, l_sn, l_sb, l_sh}))
+    if (any_negative({q_sb, q_sh, kv.k_sn, kv.k_sb, kv.k_st, kv.k_sh, kv.v_sn, kv.v_sb, kv.v_st, kv.v_sh, o_sn,
+                      o_sb, o_sh, l_sn, l_sb, l_sh}) ||
+        (kv.paged && any_negative({kv.bt_sn, kv.bt_sb})))
         return fail(DCP_ERR_INVALID_ARG, "%s: negative stride", who);
     const int64_t rb = (int64_t)D * e;
-    const int64_t lcap = ((int64_t)max_seq_len + N - 1) / N;  // local cache capacity (tokens)
+    // K/V rows: [N][B, lcap] tokens of a contiguous cache, [N][num_pages, page_size] slots of a paged one
+    const int64_t outer = kv.paged ? kv.num_pages : B;
+    const int64_t inner = kv.paged ? kv.page_size : lcap;
     View vq = View(q, rb).dim(B, q_sb * e).dim(H, q_sh * e);
-    View vk = View(k, rb).dim(N, k_sn * e).dim(B, k_sb * e).dim(lcap, k_st * e).dim(Hkv, k_sh * e);
-    View vv = View(v, rb).dim(N, v_sn * e).dim(B, v_sb * e).dim(lcap, v_st * e).dim(Hkv, v_sh * e);
+    View vk = View(kv.k, rb).dim(N, kv.k_sn * e).dim(outer, kv.k_sb * e).dim(inner, kv.k_st * e).dim(Hkv, kv.k_sh * e);
+    View vv = View(kv.v, rb).dim(N, kv.v_sn * e).dim(outer, kv.v_sb * e).dim(inner, kv.v_st * e).dim(Hkv, kv.v_sh * e);
     View vo = View(o, rb).dim(N, o_sn * e).dim(B, o_sb * e).dim(H, o_sh * e);
     View vl = View(lse, 4).dim(N, l_sn * 4).dim(B, l_sb * 4).dim(H, l_sh * 4);
     View vs = View(seq_lens, 4).dim(B, 4);
+    View vt = kv.paged ? View(kv.bt, 4).dim(N, kv.bt_sn * 4).dim(B, kv.bt_sb * 4).dim(kv.max_pages, 4)
+                       : View(nullptr, 0);
     if (vq.align() < 16 || vk.align() < 16 || vv.align() < 16)
         return fail(DCP_ERR_MISALIGNED, "%s: q, k and v rows must start on 16-byte boundaries", who);
-    if ((uintptr_t)o % e || (uintptr_t)lse % 4 || (uintptr_t)seq_lens % 4)
+    if ((uintptr_t)o % e || (uintptr_t)lse % 4 || (uintptr_t)seq_lens % 4 || (uintptr_t)kv.bt % 4)
         return fail(DCP_ERR_MISALIGNED, "%s: pointer not aligned to its element type", who);
-    for (const View* in : {&vq, &vk, &vv, &vs})
+    for (const View* in : {&vq, &vk, &vv, &vs, &vt})
         if (overlap(vo, *in) || overlap(vl, *in))
             return fail(DCP_ERR_ALIAS, "%s: an output overlaps an input", who);
     if (overlap(vo, vl) || !vo.rows_disjoint() || !vl.rows_disjoint())
@@ -498,7 +527,7 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
                         workspace ? workspace_bytes : (size_t)0);
         if ((uintptr_t)workspace % 16) return fail(DCP_ERR_MISALIGNED, "%s: workspace not 16-byte aligned", who);
         View vw = View(workspace, (int64_t)need);
-        for (const View* other : {&vq, &vk, &vv, &vs, &vo, &vl})
+        for (const View* other : {&vq, &vk, &vv, &vs, &vt, &vo, &vl})
             if (overlap(vw, *other)) return fail(DCP_ERR_ALIAS, "%s: workspace overlaps an operand", who);
     }
     dcp::AttnParams p;
@@ -507,8 +536,15 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
     p.base2 = lse_base == DCP_LSE_BASE_2;
     p.sm_scale = sm_scale;
     p.q = (const unsigned char*)q; p.q_sb = q_sb * e; p.q_sh = q_sh * e;
-    p.k = (const unsigned char*)k; p.k_sn = k_sn * e; p.k_sb = k_sb * e; p.k_st = k_st * e; p.k_sh = k_sh * e;
-    p.v = (const unsigned char*)v; p.v_sn = v_sn * e; p.v_sb = v_sb * e; p.v_st = v_st * e; p.v_sh = v_sh * e;
+    p.k = (const unsigned char*)kv.k; p.k_sn = kv.k_sn * e; p.k_st = kv.k_st * e; p.k_sh = kv.k_sh * e;
+    p.v = (const unsigned char*)kv.v; p.v_sn = kv.v_sn * e; p.v_st = kv.v_st * e; p.v_sh = kv.v_sh * e;
+    p.k_sb = kv.paged ? 0 : kv.k_sb * e;
+    p.v_sb = kv.paged ? 0 : kv.v_sb * e;
+    p.k_sp = kv.paged ? kv.k_sb * e : 0;
+    p.v_sp = kv.paged ? kv.v_sb * e : 0;
+    p.bt = kv.bt; p.bt_sn = kv.bt_sn; p.bt_sb = kv.bt_sb;
+    p.page_shift = page_shift;
+    p.num_pages = kv.paged ? kv.num_pages : 0;
     p.seq_lens = seq_lens;
     p.o = (unsigned char*)o; p.o_sn = o_sn * e; p.o_sb = o_sb * e; p.o_sh = o_sh * e;
     p.lse = lse; p.l_sn = l_sn; p.l_sb = l_sb; p.l_sh = l_sh;
@@ -516,6 +552,37 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
     p.ws_o = need ? (float*)workspace : nullptr;
     p.ws_lse = need ? (float*)workspace + rows * D : nullptr;
     return launched(dcp::launch_decode_attention(p, dtype, (cudaStream_t)stream), who);
+}
+
+dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D,
+                                  const void* q, int64_t q_sb, int64_t q_sh,
+                                  const void* k, int64_t k_sn, int64_t k_sb, int64_t k_st, int64_t k_sh,
+                                  const void* v, int64_t v_sn, int64_t v_sb, int64_t v_st, int64_t v_sh,
+                                  const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                  void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                  float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                  int lse_base, void* workspace, size_t workspace_bytes, void* stream) {
+    AttnKv kv{k, k_sn, k_sb, k_st, k_sh, v, v_sn, v_sb, v_st, v_sh, false, 0, 0, 0, nullptr, 0, 0};
+    return run_attention("dcp_decode_attention", dtype, N, B, H, Hkv, D, q, q_sb, q_sh, kv, seq_lens,
+                         max_seq_len, sm_scale, split_tokens, o, o_sn, o_sb, o_sh, lse, l_sn, l_sb, l_sh,
+                         lse_base, workspace, workspace_bytes, stream);
+}
+
+dcp_status_t dcp_decode_attention_paged(int dtype, int N, int B, int H, int Hkv, int D,
+                                        const void* q, int64_t q_sb, int64_t q_sh,
+                                        const void* k_pages, int64_t k_sn, int64_t k_sp, int64_t k_st, int64_t k_sh,
+                                        const void* v_pages, int64_t v_sn, int64_t v_sp, int64_t v_st, int64_t v_sh,
+                                        int num_pages, int page_size,
+                                        const int* block_table, int64_t bt_sn, int64_t bt_sb, int max_pages,
+                                        const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                        void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                        float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                        int lse_base, void* workspace, size_t workspace_bytes, void* stream) {
+    AttnKv kv{k_pages, k_sn, k_sp, k_st, k_sh, v_pages, v_sn, v_sp, v_st, v_sh, true,
+              num_pages, page_size, max_pages, block_table, bt_sn, bt_sb};
+    return run_attention("dcp_decode_attention_paged", dtype, N, B, H, Hkv, D, q, q_sb, q_sh, kv, seq_lens,
+                         max_seq_len, sm_scale, split_tokens, o, o_sn, o_sb, o_sh, lse, l_sn, l_sb, l_sh,
+                         lse_base, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -71,6 +71,23 @@ __device__ __forceinline__ void vec8_to_f32(const uint4& v, float (&f)[8]) {
 __device__ __forceinline__ int attn_item(int nsplit) { return (int)(blockIdx.x / (unsigned)nsplit); }
 __device__ __forceinline__ int attn_split(int nsplit) { return (int)(blockIdx.x % (unsigned)nsplit); }
 
+// Where local token t of request b on rank r lives: (page, slot) with the row
+// at page * sp + slot * st.  Contiguous caches are one page of every token;
+// a paged cache reads the rank's page table (sglang PR #33926 report,
+// "实现拆解" item 1, `_fill_dcp_block_kv_indices`: the table covers the
+// rank's round-robin slice).  An index outside the pool gives page -1 and the
+// row is read as zeros, never from outside the pool.
+struct KvPlace {
+    int64_t page;
+    int slot;
+};
+__device__ __forceinline__ KvPlace kv_place(const AttnParams& p, int r, int b, int t) {
+    if (p.page_shift < 0) return {0, t};
+    const int pg = __ldg(p.bt + (int64_t)r * p.bt_sn + (int64_t)b * p.bt_sb + (t >> p.page_shift));
+    if ((unsigned)pg >= (unsigned)p.num_pages) return {-1, 0};
+    return {(int64_t)pg, t & ((1 << p.page_shift) - 1)};
+}
+
 // Local token count of rank r for a request of global length L (round robin).
 __device__ __forceinline__ int local_len(int L, int N, int r) { return L / N + (r < L % N ? 1 : 0); }
 
@@ -172,8 +189,11 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
             kv[u] = make_uint4(0u, 0u, 0u, 0u);  // tokens past the split stay finite (masked below)
             vv[u] = kv[u];
             if (t < t1) {
-                kv[u] = ld_stream<16>(kb + (int64_t)t * p.k_st);
-                vv[u] = ld_stream<16>(vb + (int64_t)t * p.v_st);
+                const KvPlace at = kv_place(p, r, b, t);
+                if (at.page >= 0) {
+                    kv[u] = ld_stream<16>(kb + at.page * p.k_sp + (int64_t)at.slot * p.k_st);
+                    vv[u] = ld_stream<16>(vb + at.page * p.v_sp + (int64_t)at.slot * p.v_st);
+                }
             }
         }
 #pragma unroll
@@ -367,13 +387,14 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
 #pragma unroll
         for (int h = 0; h < HB; ++h) {
             const int t = tb + 8 * h + qr;
+            const KvPlace at = t < t1 ? kv_place(p, r, b, t) : KvPlace{-1, 0};
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
                 kr[h][i] = make_uint4(0u, 0u, 0u, 0u);
                 vr[h][i] = kr[h][i];
-                if (t < t1) {
-                    kr[h][i] = ld_stream<16>(kb + (int64_t)t * p.k_st + 64 * i);
-                    vr[h][i] = ld_stream<16>(vb + (int64_t)t * p.v_st + 64 * i);
+                if (at.page >= 0) {
+                    kr[h][i] = ld_stream<16>(kb + at.page * p.k_sp + (int64_t)at.slot * p.k_st + 64 * i);
+                    vr[h][i] = ld_stream<16>(vb + at.page * p.v_sp + (int64_t)at.slot * p.v_st + 64 * i);
                 }
             }
         }

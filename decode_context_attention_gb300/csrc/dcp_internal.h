@@ -62,9 +62,17 @@ struct AttnParams {
     const unsigned char* q;
     int64_t q_sb, q_sh;                 // bytes
     const unsigned char* k;
-    int64_t k_sn, k_sb, k_st, k_sh;     // bytes
+    int64_t k_sn, k_sb, k_st, k_sh;     // bytes (k_sb = 0 for paged caches)
     const unsigned char* v;
-    int64_t v_sn, v_sb, v_st, v_sh;     // bytes
+    int64_t v_sn, v_sb, v_st, v_sh;     // bytes (v_sb = 0 for paged caches)
+    // paged caches: local token i of request b on rank r sits in slot
+    // i % page_size of page bt[r][b][i / page_size] (offset page * k_sp +
+    // slot * k_st); page_shift < 0 for contiguous caches
+    const int* bt;
+    int64_t bt_sn, bt_sb;               // int32 elements
+    int64_t k_sp, v_sp;                 // bytes
+    int page_shift;                     // log2(page_size)
+    int num_pages;                      // pages in each rank's pool
     const int* seq_lens;                // [B] global lengths
     unsigned char* o;
     int64_t o_sn, o_sb, o_sh;           // bytes

@@ -255,6 +255,37 @@ dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D
                                   int lse_base, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dcp_decode_attention_paged -- dcp_decode_attention over paged KV caches: the
+ * same computation, outputs, workspace and errors, with each rank's tokens in
+ * pages of a per-rank pool.  (sglang PR #33926 report, "实现拆解" item 1 and
+ * "关键源码片段", `_fill_dcp_block_kv_indices` / `_apply_dcp_cuda_graph_metadata`:
+ * under DCP the page table of a rank is built over that rank's round-robin
+ * slice, from page_size and the rank-local lengths.)
+ *
+ *   k_pages, v_pages [N][num_pages, page_size, Hkv, D]  strides (k_sn, k_sp,
+ *                    k_st, k_sh), same for v: rank, page, slot, head
+ *   block_table      [N][B, max_pages] int32 (device)   strides (bt_sn, bt_sb);
+ *                    local token i of request b on rank r sits in slot
+ *                    i % page_size of page block_table[r][b][i / page_size]
+ *
+ * page_size is a power of two up to 65536; max_pages must cover the local
+ * capacity, ceil(ceil(max_seq_len / N) / page_size) entries, and only the
+ * entries of tokens a rank holds are read.  Page indices must lie in
+ * [0, num_pages): the kernels never read outside the pool, reading a token
+ * whose index does not as a zero row, which makes that result meaningless.
+ */
+dcp_status_t dcp_decode_attention_paged(int dtype, int N, int B, int H, int Hkv, int D,
+                                        const void* q, int64_t q_sb, int64_t q_sh,
+                                        const void* k_pages, int64_t k_sn, int64_t k_sp, int64_t k_st, int64_t k_sh,
+                                        const void* v_pages, int64_t v_sn, int64_t v_sp, int64_t v_st, int64_t v_sh,
+                                        int num_pages, int page_size,
+                                        const int* block_table, int64_t bt_sn, int64_t bt_sb, int max_pages,
+                                        const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                        void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                        float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                        int lse_base, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * dcp_decode_attention_noalloc -- dcp_decode_attention for callers that may
  * not allocate device memory where they run it (a fixed-size memory pool set
  * up front, a serving loop that forbids allocation, a host runtime with no

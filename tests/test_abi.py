@@ -146,6 +146,34 @@ def attn(dtype=BF16, N=2, B=2, H=4, Hkv=4, D=128, q=A, q_s=(512, 128), k=Bp, k_s
                                         scale, split, o, *o_s, lse, *l_s, base, ws, ws_bytes, None)
 
 
+def attn_paged(page_size=4, num_pages=6, max_pages=2, bt=0x80000000, bt_s=(4, 2), k_s=(3072, 512, 128, 128),
+               v_s=(3072, 512, 128, 128), **kw):
+    a = dict(dtype=BF16, N=2, B=2, H=4, Hkv=1, D=128, q=A, q_s=(512, 128), k=Bp, v=C, seq=Dp, max_len=16,
+             scale=0.1, split=4, o=0x50000000, o_s=(1024, 512, 128), lse=0x60000000, l_s=(8, 4, 1), base=0,
+             ws=0x70000000, ws_bytes=1 << 20)
+    a.update(kw)
+    return binding.load().dcp_decode_attention_paged(
+        a["dtype"], a["N"], a["B"], a["H"], a["Hkv"], a["D"], a["q"], *a["q_s"], a["k"], *k_s, a["v"], *v_s,
+        num_pages, page_size, bt, *bt_s, max_pages, a["seq"], a["max_len"], a["scale"], a["split"], a["o"],
+        *a["o_s"], a["lse"], *a["l_s"], a["base"], a["ws"], a["ws_bytes"], None)
+
+
+def test_decode_attention_paged_validation(lib):
+    # every call fails validation (nothing is launched)
+    assert attn_paged(page_size=3) == 1                   # not a power of two
+    assert attn_paged(page_size=1 << 17) == 1
+    assert attn_paged(num_pages=0) == 1
+    assert attn_paged(max_pages=1) == 1                   # 8 local tokens need 2 pages of 4
+    assert "page table" in binding.dcp_last_error_message()
+    assert attn_paged(bt=0) == 1                          # NULL page table
+    assert attn_paged(bt=0x80000002) == 4                 # page table not 4-byte aligned
+    assert attn_paged(bt_s=(-4, 2)) == 1
+    assert attn_paged(bt=0x50000000) == 5                 # page table under the output
+    assert attn_paged(k_s=(3072, 512, 132, 128)) == 4     # slot rows off the 16-byte grid
+    assert attn_paged(dtype=F32) == 2
+    assert attn_paged(B=0) == 0
+
+
 def test_decode_attention_workspace_size(lib):
     # one split: no workspace; else N*B*H*splits rows of D fp32 + one fp32 LSE each
     assert binding.dcp_decode_attention_workspace_size(4, 3, 8, 128, 4000, 1000) == 0

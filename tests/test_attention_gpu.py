@@ -224,3 +224,57 @@ def test_decode_attention_workload_full_size_sampled(name, split):
         O, l = oracle.split_attention(to_f64(a["q"][b, h]), to_f64(kg), to_f64(vg), N, scale, base=c["base"])
         assert_merge_close(o[:, b, h], O, f"row b={b} h={h}")
         assert_attn_lse(lse[:, b, h], l, f"lse b={b} h={h}")
+
+
+def paged_caches(k, v, page_size, seed, spare=3):
+    """Scatter local caches [N, B, Lc, Hkv, D] into per-rank page pools
+    [N, num_pages, page_size, Hkv, D] with each rank's pages in a shuffled
+    order; pages nobody owns hold NaN, so a read of a wrong page shows.
+    Returns (k_pages, v_pages, block_table [N, B, max_pages] int32)."""
+    N, B, Lc, Hkv, D = k.shape
+    max_pages = (Lc + page_size - 1) // page_size
+    num_pages = B * max_pages + spare
+    g = torch.Generator().manual_seed(seed)
+    bt = torch.stack([torch.randperm(num_pages, generator=g)[:B * max_pages] for _ in range(N)])
+    pools = []
+    for src in (k, v):
+        pad = torch.zeros((N, B, max_pages * page_size, Hkv, D), dtype=src.dtype, device=DEV)
+        pad[:, :, :Lc] = src
+        pool = torch.full((N, num_pages, page_size, Hkv, D), float("nan"), device=DEV).to(src.dtype)
+        for r in range(N):
+            pool[r, bt[r].to(DEV)] = pad[r].reshape(B * max_pages, page_size, Hkv, D)
+        pools.append(pool)
+    return pools[0], pools[1], bt.view(N, B, max_pages).to(torch.int32).to(DEV)
+
+
+PAGED = [
+    # N, H, Hkv, D, lengths, dtype, base, split_tokens, page_size
+    (4, 8, 1, 128, [0, 5, 700], torch.bfloat16, "e", 64, 16),
+    (2, 4, 4, 64, [33, 130], torch.float16, "2", 1000, 1),
+    (3, 16, 2, 256, [9, 300], torch.bfloat16, "e", 40, 64),
+    (2, 8, 4, 256, [77, 5], torch.float16, "2", 16, 8),
+    (2, 32, 2, 128, [1, 513], torch.bfloat16, "2", 128, 32),
+]
+
+
+@pytest.mark.parametrize("N,H,Hkv,D,lens,dtype,base,split,page_size", PAGED)
+def test_paged_caches_give_the_contiguous_result(N, H, Hkv, D, lens, dtype, base, split, page_size):
+    """The same partials from paged caches as from contiguous ones, bit for bit
+    (the kernels differ only in where a token's row is read), and the oracle's."""
+    B = len(lens)
+    q, K, V, seq, L = make_case(N, B, H, Hkv, D, lens, dtype, seed=31 * N + D + page_size)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_attention(q, K, V, seq, L, N, scale, base, split)
+    kp, vp, bt = paged_caches(local_caches(K, N), local_caches(V, N), page_size, seed=page_size)
+    o2 = torch.empty_like(o)
+    lse2 = torch.empty_like(lse)
+    nbytes = binding.workspace_bytes(N, B, H, D, L, split)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=DEV) if nbytes else None
+    binding.decode_attention_paged(q, kp, vp, bt, seq, L, o2, lse2, scale, base=base, split_tokens=split,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o2.view(torch.int16), o.view(torch.int16))
+    assert torch.equal(lse2.view(torch.int32), lse.view(torch.int32))
+    want, want_lse = oracle_partials(q, K, V, lens, N, scale, base)
+    assert_merge_close(o2, want, "paged rank partial O")
+    assert_attn_lse(lse2, want_lse)
