@@ -81,8 +81,9 @@ struct KvPlace {
     int64_t page;
     int slot;
 };
+template <bool PAGED>
 __device__ __forceinline__ KvPlace kv_place(const AttnParams& p, int r, int b, int t) {
-    if (p.page_shift < 0) return {0, t};
+    if constexpr (!PAGED) return {0, t};
     const int pg = __ldg(p.bt + (int64_t)r * p.bt_sn + (int64_t)b * p.bt_sb + (t >> p.page_shift));
     if ((unsigned)pg >= (unsigned)p.num_pages) return {-1, 0};
     return {(int64_t)pg, t & ((1 << p.page_shift) - 1)};
@@ -128,7 +129,7 @@ __device__ __forceinline__ void write_cta_result(const AttnParams& p, int r, int
     }
 }
 
-template <typename T, int D, int GQ>
+template <typename T, int D, int GQ, bool PAGED>
 __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const AttnParams p) {
     constexpr int LPT = D / 8;              // lanes per token row (16-byte vectors)
     constexpr int TPW = 32 / LPT;           // token rows per warp step
@@ -188,12 +189,15 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
             const int t = tb + u * NG;
             kv[u] = make_uint4(0u, 0u, 0u, 0u);  // tokens past the split stay finite (masked below)
             vv[u] = kv[u];
-            if (t < t1) {
-                const KvPlace at = kv_place(p, r, b, t);
+            if constexpr (PAGED) {
+                const KvPlace at = t < t1 ? kv_place<true>(p, r, b, t) : KvPlace{-1, 0};
                 if (at.page >= 0) {
                     kv[u] = ld_stream<16>(kb + at.page * p.k_sp + (int64_t)at.slot * p.k_st);
                     vv[u] = ld_stream<16>(vb + at.page * p.v_sp + (int64_t)at.slot * p.v_st);
                 }
+            } else if (t < t1) {
+                kv[u] = ld_stream<16>(kb + (int64_t)t * p.k_st);
+                vv[u] = ld_stream<16>(vb + (int64_t)t * p.v_st);
             }
         }
 #pragma unroll
@@ -318,7 +322,7 @@ __device__ __forceinline__ unsigned word_of(const uint4& v, int w) {
     return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
-template <typename T, int D, int GQ>
+template <typename T, int D, int GQ, bool PAGED>
 __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const AttnParams p) {
     static_assert(D % 32 == 0 && GQ >= 1 && GQ <= 16, "fragment shapes");
     constexpr int NB = GQ > 8 ? 2 : 1;    // blocks of 8 query heads (fragment rows qr and qr + 8)
@@ -387,14 +391,27 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
 #pragma unroll
         for (int h = 0; h < HB; ++h) {
             const int t = tb + 8 * h + qr;
-            const KvPlace at = t < t1 ? kv_place(p, r, b, t) : KvPlace{-1, 0};
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
                 kr[h][i] = make_uint4(0u, 0u, 0u, 0u);
                 vr[h][i] = kr[h][i];
+            }
+            if constexpr (PAGED) {
+                const KvPlace at = t < t1 ? kv_place<true>(p, r, b, t) : KvPlace{-1, 0};
                 if (at.page >= 0) {
-                    kr[h][i] = ld_stream<16>(kb + at.page * p.k_sp + (int64_t)at.slot * p.k_st + 64 * i);
-                    vr[h][i] = ld_stream<16>(vb + at.page * p.v_sp + (int64_t)at.slot * p.v_st + 64 * i);
+                    const unsigned char* kp = kb + at.page * p.k_sp + (int64_t)at.slot * p.k_st;
+                    const unsigned char* vp = vb + at.page * p.v_sp + (int64_t)at.slot * p.v_st;
+#pragma unroll
+                    for (int i = 0; i < NI; ++i) {
+                        kr[h][i] = ld_stream<16>(kp + 64 * i);
+                        vr[h][i] = ld_stream<16>(vp + 64 * i);
+                    }
+                }
+            } else if (t < t1) {
+#pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    kr[h][i] = ld_stream<16>(kb + (int64_t)t * p.k_st + 64 * i);
+                    vr[h][i] = ld_stream<16>(vb + (int64_t)t * p.v_st + 64 * i);
                 }
             }
         }
@@ -473,7 +490,9 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
                 pl[nb][h] = round_pair<T>(pr[nb][h][0] - bh.x, pr[nb][h][1] - bh.y);
             }
         // V^T fragments: 8x8 tiles x = 2j (rows 0-7) and 2j+1 (rows 8-15), word
-        // x%4 of piece x/4, one per 8-token half
+        // x%4 of piece x/4, one per 8-token half; then the hi terms of every
+        // (head block, d block) and the lo terms, so consecutive mma are
+        // independent
         unsigned va[NM][2 * HB];
 #pragma unroll
         for (int j = 0; j < NM; ++j)
@@ -483,8 +502,6 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
                 va[j][2 * h] = tile_transpose(word_of(vr[h][x0 >> 2], x0 & 3));
                 va[j][2 * h + 1] = tile_transpose(word_of(vr[h][x1 >> 2], x1 & 3));
             }
-        // hi terms of every (head block, d block), then lo terms: consecutive mma
-        // are independent
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -583,8 +600,8 @@ __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const
     }
 }
 
-template <typename T, int D>
-static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) {
+template <typename T, int D, bool PAGED>
+static cudaError_t launch_attention_dp(const AttnParams& p, cudaStream_t stream) {
     const void* k;
     // grouped-query heads go to the tensor cores; one query head per KV head
     // stays on the CUDA cores, and so do two at D = 256 (measured: 1.51 ms on
@@ -593,24 +610,24 @@ static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) 
     // cores win, 0.90 vs 1.28 ms and 0.51 vs 1.38 ms)
     if constexpr (DCP_ATTN_MMA) {
         switch (p.H / p.Hkv) {
-            case 1: k = (const void*)decode_partial_kernel<T, D, 1>; break;
+            case 1: k = (const void*)decode_partial_kernel<T, D, 1, PAGED>; break;
             case 2:
-                k = D == 256 ? (const void*)decode_partial_kernel<T, D, 2> : (const void*)decode_partial_mma_kernel<T, D, 2>;
+                k = D == 256 ? (const void*)decode_partial_kernel<T, D, 2, PAGED> : (const void*)decode_partial_mma_kernel<T, D, 2, PAGED>;
                 break;
-            case 4: k = (const void*)decode_partial_mma_kernel<T, D, 4>; break;
-            case 8: k = (const void*)decode_partial_mma_kernel<T, D, 8>; break;
+            case 4: k = (const void*)decode_partial_mma_kernel<T, D, 4, PAGED>; break;
+            case 8: k = (const void*)decode_partial_mma_kernel<T, D, 8, PAGED>; break;
             case 16:
-                if constexpr (D <= 128) k = (const void*)decode_partial_mma_kernel<T, D, 16>;
+                if constexpr (D <= 128) k = (const void*)decode_partial_mma_kernel<T, D, 16, PAGED>;
                 else return cudaErrorInvalidValue;  // refused by the host checks
                 break;
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.H / p.Hkv) {
-            case 1: k = (const void*)decode_partial_kernel<T, D, 1>; break;
-            case 2: k = (const void*)decode_partial_kernel<T, D, 2>; break;
-            case 4: k = (const void*)decode_partial_kernel<T, D, 4>; break;
-            case 8: k = (const void*)decode_partial_kernel<T, D, 8>; break;
+            case 1: k = (const void*)decode_partial_kernel<T, D, 1, PAGED>; break;
+            case 2: k = (const void*)decode_partial_kernel<T, D, 2, PAGED>; break;
+            case 4: k = (const void*)decode_partial_kernel<T, D, 4, PAGED>; break;
+            case 8: k = (const void*)decode_partial_kernel<T, D, 8, PAGED>; break;
             default: return cudaErrorInvalidValue;
         }
     }
@@ -622,6 +639,12 @@ static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) 
     const unsigned mgrid = (unsigned)((rows + kAttnThreads / 32 - 1) / (kAttnThreads / 32));
     return cudaLaunchKernel((const void*)decode_merge_splits_kernel<T, D>, dim3(mgrid), dim3(kAttnThreads),
                             args, 0, stream);
+}
+
+template <typename T, int D>
+static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t stream) {
+    // paged caches take the page-table lookup; contiguous ones compile without it
+    return p.page_shift >= 0 ? launch_attention_dp<T, D, true>(p, stream) : launch_attention_dp<T, D, false>(p, stream);
 }
 
 template <typename T>
