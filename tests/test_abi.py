@@ -201,3 +201,25 @@ def test_decode_attention_validation(lib):
     assert attn(o=A) == 5                      # output over q
     assert attn(lse=0x50000000) == 5           # lse over o
     assert attn(B=0) == 0
+
+
+def test_missing_library_raises_instead_of_falling_back(tmp_path):
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from decode_context_attention_gb300 import binding\n"
+            "try:\n    binding.load(%r)\nexcept RuntimeError as e:\n    print('refused', 'no CPU fallback' in str(e))\n"
+            % (ROOT, str(tmp_path / "absent.so")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.stdout.strip() == "refused True", r.stdout + r.stderr
+
+
+def test_plain_host_tensors_are_refused_before_any_call(lib):
+    import torch
+    o = torch.zeros((1, 2, 2, 4, 8))
+    lse = torch.zeros((1, 2, 2, 4))
+    with pytest.raises(ValueError, match="no CPU fallback"):
+        binding.lse_combine(o, lse, torch.zeros((1, 2, 4, 8)))
+    with pytest.raises(ValueError, match="no CPU fallback"):
+        binding.pack_send(torch.zeros((1, 2, 4, 8)), torch.zeros((1, 2, 4)), torch.zeros((1, 2, 2, 2, 8)),
+                          torch.zeros((1, 2, 2, 2)))
