@@ -81,6 +81,14 @@ int elem_size(int dtype) {
     }
 }
 
+// Limits that keep every byte offset in 64 bits: a stride of at most 2^52
+// elements (times at most 4 bytes), a payload row of at most 2^30 bytes (row
+// and vector offsets are 32-bit in the kernels), and at most 2^56 bytes
+// between the first and the last byte an operand's rows can touch.
+constexpr int64_t kMaxStride = int64_t(1) << 52;
+constexpr int64_t kMaxRowBytes = int64_t(1) << 30;
+constexpr int64_t kMaxSpan = int64_t(1) << 56;
+
 // A strided set of rows: `nd` outer dimensions (size, stride in BYTES) and
 // `inner` contiguous bytes per row.
 struct View {
@@ -101,6 +109,20 @@ struct View {
         for (int i = 0; i < nd; ++i)
             if (size[i] == 0) return true;
         return inner == 0;
+    }
+    // False when the rows would span more than kMaxSpan bytes (or the span
+    // overflows): no device holds that much memory, so such strides are a
+    // caller's mistake, and refusing them keeps every address computation
+    // below (host and device, 64-bit) free of overflow.
+    bool fits() const {
+        int64_t s = inner;
+        for (int i = 0; i < nd; ++i) {
+            if (size[i] <= 1) continue;
+            int64_t t;
+            if (__builtin_mul_overflow(size[i] - 1, stride[i], &t) || __builtin_add_overflow(s, t, &s))
+                return false;
+        }
+        return s <= kMaxSpan;
     }
     // Byte range [lo, hi) that the rows can touch.
     void extent(uintptr_t& lo, uintptr_t& hi) const {
@@ -144,10 +166,17 @@ bool overlap(const View& a, const View& b) {
     return alo < bhi && blo < ahi;
 }
 
-bool any_negative(std::initializer_list<int64_t> s) {
+// A stride below 0 or above kMaxStride elements.
+bool bad_stride(std::initializer_list<int64_t> s) {
     for (int64_t v : s)
-        if (v < 0) return true;
+        if (v < 0 || v > kMaxStride) return true;
     return false;
+}
+
+bool all_fit(std::initializer_list<const View*> views) {
+    for (const View* v : views)
+        if (!v->fits()) return false;
+    return true;
 }
 
 // Widest vector (16, 4 or 2 bytes) that divides the row length and every row
@@ -220,12 +249,14 @@ dcp_status_t dcp_pack_send(int dtype, int N, int B, int H, int D, int G,
         return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: sizes N=%d B=%d H=%d D=%d G=%d", N, B, H, D, G);
     if (H % N)
         return fail(DCP_ERR_HEADS_NOT_DIVISIBLE, "dcp_pack_send: H=%d is not a multiple of N=%d", H, N);
+    if ((int64_t)D * e > kMaxRowBytes)
+        return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: rows of D=%d elements exceed 2^30 bytes", D);
     if (G == 0 || B == 0 || H == 0) return ok();
     if (!o || !lse || !dst_o || !dst_lse)
         return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: NULL pointer");
-    if (any_negative({o_sg, o_sb, o_sh, l_sg, l_sb, l_sh, do_sg, do_sn, do_sb, do_sh, dl_sg, dl_sn,
+    if (bad_stride({o_sg, o_sb, o_sh, l_sg, l_sb, l_sh, do_sg, do_sn, do_sb, do_sh, dl_sg, dl_sn,
                       dl_sb, dl_sh}))
-        return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: negative stride");
+        return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: negative stride or one above 2^52 elements");
     if ((uintptr_t)o % e || (uintptr_t)dst_o % e || (uintptr_t)lse % 4 || (uintptr_t)dst_lse % 4)
         return fail(DCP_ERR_MISALIGNED, "dcp_pack_send: pointer not aligned to its element type");
     const int H_pr = H / N;
@@ -234,6 +265,8 @@ dcp_status_t dcp_pack_send(int dtype, int N, int B, int H, int D, int G,
     View vl = View(lse, 4).dim(G, l_sg * 4).dim(B, l_sb * 4).dim(H, l_sh * 4);
     View vdo = View(dst_o, rb).dim(G, do_sg * e).dim(N, do_sn * e).dim(B, do_sb * e).dim(H_pr, do_sh * e);
     View vdl = View(dst_lse, 4).dim(G, dl_sg * 4).dim(N, dl_sn * 4).dim(B, dl_sb * 4).dim(H_pr, dl_sh * 4);
+    if (!all_fit({&vo, &vl, &vdo, &vdl}))
+        return fail(DCP_ERR_INVALID_ARG, "dcp_pack_send: an operand's strides span more than 2^56 bytes");
     if (overlap(vdo, vo) || overlap(vdo, vl) || overlap(vdl, vo) || overlap(vdl, vl))
         return fail(DCP_ERR_ALIAS, "dcp_pack_send: destination overlaps the source");
     if (!fp8_rows_ok(e, D, vo.align(), vdo.align()))
@@ -329,6 +362,8 @@ dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
     if (!e) return fail(DCP_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", who, dtype);
     if (N < 1 || N > kMaxRanks || D < 1 || B < 0 || Hc < 0 || G < 0)
         return fail(DCP_ERR_INVALID_ARG, "%s: sizes N=%d B=%d Hc=%d D=%d G=%d", who, N, B, Hc, D, G);
+    if ((int64_t)D * e > kMaxRowBytes)
+        return fail(DCP_ERR_INVALID_ARG, "%s: rows of D=%d elements exceed 2^30 bytes", who, D);
     if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)
         return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
     if (flags & ~(unsigned)(DCP_SANITIZE_O | DCP_INPLACE_RANK0))
@@ -336,9 +371,9 @@ dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
     if (G == 0 || B == 0 || Hc == 0) return ok();
     if (!o || !lse || !out || (return_lse && !out_lse))
         return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
-    if (any_negative({o_sg, o_sn, o_sb, o_sh, l_sg, l_sn, l_sb, l_sh, u_sg, u_sb, u_sh}) ||
-        (return_lse && any_negative({ul_sg, ul_sb, ul_sh})))
-        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride", who);
+    if (bad_stride({o_sg, o_sn, o_sb, o_sh, l_sg, l_sn, l_sb, l_sh, u_sg, u_sb, u_sh}) ||
+        (return_lse && bad_stride({ul_sg, ul_sb, ul_sh})))
+        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride or one above 2^52 elements", who);
     if ((uintptr_t)o % e || (uintptr_t)out % e || (uintptr_t)lse % 4 ||
         (return_lse && (uintptr_t)out_lse % 4))
         return fail(DCP_ERR_MISALIGNED, "%s: pointer not aligned to its element type", who);
@@ -347,6 +382,9 @@ dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
     View vo = View(o, rb).dim(G, o_sg * e).dim(N, o_sn * e).dim(B, o_sb * e).dim(Hc, o_sh * e);
     View vl = View(lse, 4).dim(G, l_sg * 4).dim(N, l_sn * 4).dim(B, l_sb * 4).dim(Hc, l_sh * 4);
     View vu = View(out, rb).dim(G, u_sg * e).dim(B, u_sb * e).dim(Hc, u_sh * e);
+    View vul = View(out_lse, 4).dim(G, ul_sg * 4).dim(B, ul_sb * 4).dim(Hc, ul_sh * 4);
+    if (!all_fit({&vo, &vl, &vu}) || (return_lse && !vul.fits()))
+        return fail(DCP_ERR_INVALID_ARG, "%s: an operand's strides span more than 2^56 bytes", who);
     if (inplace) {
         if (out != o || (G > 1 && u_sg != o_sg) || (B > 1 && u_sb != o_sb) || (Hc > 1 && u_sh != o_sh))
             return fail(DCP_ERR_INVALID_ARG,
@@ -361,7 +399,6 @@ dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
     if (overlap(vu, vl)) return fail(DCP_ERR_ALIAS, "%s: out overlaps lse", who);
     if (!vu.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out rows overlap one another", who);
     if (return_lse) {
-        View vul = View(out_lse, 4).dim(G, ul_sg * 4).dim(B, ul_sb * 4).dim(Hc, ul_sh * 4);
         if (overlap(vul, vo) || overlap(vul, vl) || overlap(vul, vu))
             return fail(DCP_ERR_ALIAS, "%s: out_lse overlaps an input or out", who);
         if (!vul.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out_lse entries overlap", who);
@@ -382,6 +419,8 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
     if (!e) return fail(DCP_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", who, dtype);
     if (N < 1 || N > kMaxRanks || D < 1 || B < 0 || Hpr < 0 || G < 0)
         return fail(DCP_ERR_INVALID_ARG, "%s: sizes N=%d B=%d Hpr=%d D=%d G=%d", who, N, B, Hpr, D, G);
+    if ((int64_t)D * e > kMaxRowBytes)
+        return fail(DCP_ERR_INVALID_ARG, "%s: rows of D=%d elements exceed 2^30 bytes", who, D);
     if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)
         return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
     if (flags & ~(unsigned)DCP_SANITIZE_O)
@@ -391,22 +430,24 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
     if (G == 0 || B == 0 || Hpr == 0) return ok();
     if (!recv || !out || (return_lse && !out_lse))
         return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
-    if (any_negative({r_sg, r_sn, r_sb, r_sh, u_sg, u_sb, u_sh}) ||
-        (return_lse && any_negative({ul_sg, ul_sb, ul_sh})))
-        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride", who);
+    if (bad_stride({r_sg, r_sn, r_sb, r_sh, u_sg, u_sb, u_sh}) ||
+        (return_lse && bad_stride({ul_sg, ul_sb, ul_sh})))
+        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride or one above 2^52 elements", who);
     if ((uintptr_t)out % e || (return_lse && (uintptr_t)out_lse % 4))
         return fail(DCP_ERR_MISALIGNED, "%s: pointer not aligned to its element type", who);
     const int64_t rb = (int64_t)D * e;
     View vr = View(recv, rb + 4).dim(G, r_sg * e).dim(N, r_sn * e).dim(B, r_sb * e).dim(Hpr, r_sh * e);
+    View vu = View(out, rb).dim(G, u_sg * e).dim(B, u_sb * e).dim(Hpr, u_sh * e);
+    View vul = View(out_lse, 4).dim(G, ul_sg * 4).dim(B, ul_sb * 4).dim(Hpr, ul_sh * 4);
+    if (!all_fit({&vr, &vu}) || (return_lse && !vul.fits()))
+        return fail(DCP_ERR_INVALID_ARG, "%s: an operand's strides span more than 2^56 bytes", who);
     if (vr.align() < 4)
         return fail(DCP_ERR_MISALIGNED, "%s: receive rows must start on 4-byte boundaries", who);
-    View vu = View(out, rb).dim(G, u_sg * e).dim(B, u_sb * e).dim(Hpr, u_sh * e);
     if (!fp8_rows_ok(e, D, vr.align(), vu.align()))
         return fail(DCP_ERR_MISALIGNED, "%s: fp8 rows need 4-byte aligned row starts", who);
     if (overlap(vu, vr)) return fail(DCP_ERR_ALIAS, "%s: out overlaps recv", who);
     if (!vu.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out rows overlap one another", who);
     if (return_lse) {
-        View vul = View(out_lse, 4).dim(G, ul_sg * 4).dim(B, ul_sb * 4).dim(Hpr, ul_sh * 4);
         if (overlap(vul, vr) || overlap(vul, vu))
             return fail(DCP_ERR_ALIAS, "%s: out_lse overlaps recv or out", who);
         if (!vul.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out_lse entries overlap", who);
@@ -429,15 +470,21 @@ static int attn_nsplit(int N, int max_seq_len, int split_tokens) {
     return s < 1 ? 1 : (int)s;
 }
 
+// fp32 partial rows and their LSE words, one per (rank, request, head, split);
+// SIZE_MAX when that does not fit in size_t.
 static size_t attn_workspace_bytes(int N, int B, int H, int D, int nsplit) {
     if (nsplit <= 1) return 0;
-    const size_t rows = (size_t)N * B * H * nsplit;
-    return rows * (size_t)D * 4 + rows * 4;
+    size_t rows = 1, bytes = 0;
+    for (int f : {N, B, H, nsplit})
+        if (__builtin_mul_overflow(rows, (size_t)f, &rows)) return SIZE_MAX;
+    if (__builtin_mul_overflow(rows, (size_t)D * 4 + 4, &bytes)) return SIZE_MAX;
+    return bytes;
 }
 
 size_t dcp_decode_attention_workspace_size(int N, int B, int H, int D, int max_seq_len, int split_tokens) {
-    if (N < 1 || B < 0 || H < 1 || D < 1 || max_seq_len < 0 || split_tokens < 1) return 0;
-    return attn_workspace_bytes(N, B, H, D, attn_nsplit(N, max_seq_len, split_tokens));
+    if (N < 1 || N > kMaxRanks || B < 0 || H < 1 || D < 1 || max_seq_len < 0 || split_tokens < 1) return 0;
+    const size_t need = attn_workspace_bytes(N, B, H, D, attn_nsplit(N, max_seq_len, split_tokens));
+    return need == SIZE_MAX ? 0 : need;
 }
 
 // Where the K/V rows live: per-request contiguous local caches, or pages of a
@@ -495,10 +542,10 @@ static dcp_status_t run_attention(const char* who, int dtype, int N, int B, int 
         return fail(DCP_ERR_INVALID_ARG, "%s: too many work items (N*B*Hkv*splits >= 2^31)", who);
     if (!q || !kv.k || !kv.v || !seq_lens || !o || !lse || (kv.paged && !kv.bt))
         return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
-    if (any_negative({q_sb, q_sh, kv.k_sn, kv.k_sb, kv.k_st, kv.k_sh, kv.v_sn, kv.v_sb, kv.v_st, kv.v_sh, o_sn,
+    if (bad_stride({q_sb, q_sh, kv.k_sn, kv.k_sb, kv.k_st, kv.k_sh, kv.v_sn, kv.v_sb, kv.v_st, kv.v_sh, o_sn,
                       o_sb, o_sh, l_sn, l_sb, l_sh}) ||
-        (kv.paged && any_negative({kv.bt_sn, kv.bt_sb})))
-        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride", who);
+        (kv.paged && bad_stride({kv.bt_sn, kv.bt_sb})))
+        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride or one above 2^52 elements", who);
     const int64_t rb = (int64_t)D * e;
     // K/V rows: [N][B, lcap] tokens of a contiguous cache, [N][num_pages, page_size] slots of a paged one
     const int64_t outer = kv.paged ? kv.num_pages : B;
@@ -511,6 +558,8 @@ static dcp_status_t run_attention(const char* who, int dtype, int N, int B, int 
     View vs = View(seq_lens, 4).dim(B, 4);
     View vt = kv.paged ? View(kv.bt, 4).dim(N, kv.bt_sn * 4).dim(B, kv.bt_sb * 4).dim(kv.max_pages, 4)
                        : View(nullptr, 0);
+    if (!all_fit({&vq, &vk, &vv, &vo, &vl, &vs, &vt}))
+        return fail(DCP_ERR_INVALID_ARG, "%s: an operand's strides span more than 2^56 bytes", who);
     if (vq.align() < 16 || vk.align() < 16 || vv.align() < 16)
         return fail(DCP_ERR_MISALIGNED, "%s: q, k and v rows must start on 16-byte boundaries", who);
     if ((uintptr_t)o % e || (uintptr_t)lse % 4 || (uintptr_t)seq_lens % 4 || (uintptr_t)kv.bt % 4)

@@ -31,9 +31,14 @@
  *   valid once the stream reaches that point.
  * - Strides are in ELEMENTS of the pointed-to type: payload elements (dtype)
  *   for O / dst_o / out / recv, fp32 words for every LSE pointer.  Strides
- *   must be >= 0.  The innermost (D) stride is always 1 and is not passed.
+ *   must be >= 0 and <= 2^52.  The innermost (D) stride is always 1 and is
+ *   not passed.
  * - Sizes: N >= 1 and D >= 1.  B, H (or Hc, Hpr) and G may be 0, in which
- *   case the call does nothing and returns DCP_OK.  N <= 4096.
+ *   case the call does nothing and returns DCP_OK.  N <= 4096.  A payload
+ *   row (D elements) is at most 2^30 bytes, and the rows of one operand span
+ *   at most 2^56 bytes from its first to its last byte (no device holds more;
+ *   larger strides are refused as DCP_ERR_INVALID_ARG rather than left to
+ *   wrap around in 64-bit address arithmetic).
  * - G is a batch of independent groups (for example all N destination ranks,
  *   or all N source ranks, of a group held on one device).
  * - Validation happens on the host, before any launch; a failing call
@@ -70,7 +75,7 @@ extern "C" {
 
 typedef enum dcp_status {
     DCP_OK = 0,
-    DCP_ERR_INVALID_ARG = 1,          /* bad size, NULL pointer, negative stride, bad flag */
+    DCP_ERR_INVALID_ARG = 1,          /* bad size, NULL pointer, stride out of range, bad flag */
     DCP_ERR_UNSUPPORTED_DTYPE = 2,    /* dtype other than f32 / f16 / bf16 / fp8 e4m3 */
     DCP_ERR_HEADS_NOT_DIVISIBLE = 3,  /* H % N != 0 in the pack */
     DCP_ERR_MISALIGNED = 4,           /* D % lpd != 0, a pointer/stride not aligned to its type,
@@ -235,13 +240,15 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
  *
  * dtype: DCP_F16 or DCP_BF16 (q, k, v and o); D in {64, 128, 256}; H / Hkv in
  * {1, 2, 4, 8, 16} (16 only with D <= 128); q, k and v rows start on 16-byte
- * boundaries.  Work is split
- * into chunks of `split_tokens` local tokens; with more than one chunk the
- * partial results go through `workspace` (caller-owned device memory, 16-byte
- * aligned, at least dcp_decode_attention_workspace_size(...) bytes; NULL is
- * fine when that size is 0).  Errors: DCP_ERR_HEADS_NOT_DIVISIBLE when
- * H % Hkv != 0, DCP_ERR_INVALID_ARG for unsupported sizes or a too small
- * workspace, DCP_ERR_MISALIGNED, DCP_ERR_ALIAS for overlapping operands.
+ * boundaries.  Work is split into chunks of `split_tokens` local tokens;
+ * with more than one chunk the partial results go through `workspace`
+ * (caller-owned device memory, 16-byte aligned, at least
+ * dcp_decode_attention_workspace_size(...) bytes; NULL is fine when that
+ * size is 0; the size function returns 0 as well for arguments the call
+ * itself refuses, such as N > 4096).  Errors: DCP_ERR_HEADS_NOT_DIVISIBLE
+ * when H % Hkv != 0, DCP_ERR_INVALID_ARG for unsupported sizes or a too
+ * small workspace, DCP_ERR_MISALIGNED, DCP_ERR_ALIAS for overlapping
+ * operands.
  */
 size_t dcp_decode_attention_workspace_size(int N, int B, int H, int D, int max_seq_len, int split_tokens);
 

@@ -133,6 +133,43 @@ def test_fp8_rows_need_four_byte_granularity(lib):
     assert unpack(dtype=FP8, r_s=(160, 80, 40, 10)) == 4     # receive rows off the grid
 
 
+def test_strides_sizes_and_spans_beyond_any_address_space_are_refused(lib):
+    # every call fails validation on the host: the limits keep 64-bit byte
+    # offsets (stride * index, summed over dimensions) from wrapping around
+    big = 1 << 53                                      # a stride above 2^52 elements
+    assert pack(o_s=(64, big, 8)) == 1
+    assert "2^52" in binding.dcp_last_error_message()
+    assert combine(l_s=(16, big, 4, 1)) == 1
+    assert unpack(u_s=(64, big, 8)) == 1
+    assert attn(q_s=(big, 128)) == 1
+    # a payload row above 2^30 bytes
+    assert pack(D=(1 << 28) + 8, o_s=(1 << 31, 1 << 30, 1 << 29)) == 1
+    assert "2^30" in binding.dcp_last_error_message()
+    assert combine(dtype=F16, D=(1 << 29) + 8) == 1
+    assert unpack(D=(1 << 29) + 8) == 1
+    # strides within range whose rows together would span more than 2^56 bytes:
+    # 2^30 tokens 2^31 fp32 elements apart
+    far = 1 << 31
+    for call in (lambda: pack(B=1 << 30, o_s=(0, far, 8)),
+                 lambda: combine(B=1 << 30, u_s=(0, far, 8)),
+                 lambda: combine(B=1 << 30, ul_s=(0, far, 1)),     # the returned-LSE view as well
+                 lambda: unpack(B=1 << 30, r_s=(0, 16, far, 10)),
+                 lambda: attn(B=1 << 25, k_s=(8192, far, 512, 128))):
+        assert call() == 1
+        assert "2^56" in binding.dcp_last_error_message()
+    # just inside the span limit the same kind of call passes this check and is
+    # refused only by the next one (here: rows that overlap the output)
+    assert pack(B=1 << 20, o_s=(0, 1 << 20, 8), dst=A + (1 << 30)) == 5
+
+
+def test_workspace_size_refuses_sizes_the_call_refuses(lib):
+    ws = binding.dcp_decode_attention_workspace_size
+    assert ws(4097, 1, 1, 64, 1 << 20, 1) == 0                     # N above 4096
+    # rows * (D + 1) * 4 overflows 64 bits: 0, not a wrapped-around small size
+    assert ws(4096, (1 << 31) - 1, (1 << 31) - 1, 256, (1 << 31) - 1, 1) == 0
+    assert ws(4096, 1 << 10, 64, 128, 1 << 24, 1024) == 4096 * 1024 * 64 * 4 * 129 * 4
+
+
 def test_binding_raises_with_message(lib):
     with pytest.raises(binding.DcpError) as ei:
         binding.check(pack(N=3), "dcp_pack_send")
