@@ -183,6 +183,9 @@ int oracle_pack(int dtype, int N, int B, int H, int D, int G,
     return 0;
 }
 
+/* Ranks one merge may take: as many as the library under test accepts. */
+#define ORACLE_MAX_RANKS 4096
+
 /* ---- the merge of one row ------------------------------------------------ */
 /*
  * x[r]   : the N rank LSE values, already in natural-log units
@@ -212,7 +215,7 @@ static double logsumexp_ext(int N, const double* x) {
 
 static void merge_row(int dtype, int N, int D, const double* x, const void* const* rows,
                       unsigned flags, double* out, double* G_out) {
-    double w[1024];
+    double w[ORACLE_MAX_RANKS];
     const double G = logsumexp_ext(N, x);
     for (int r = 0; r < N; ++r) {
         w[r] = exp(x[r] - G);
@@ -240,16 +243,16 @@ static double from_nat(double G, int base) { return base == ORACLE_BASE_2 ? G / 
  * O viewed as [G][N, B, Hc, D], LSE as [G][N, B, Hc] (fp32 words).
  * out: contiguous double [G, B, Hc, D]; out_lse: contiguous double [G, B, Hc].
  * N == 1 returns O and lse unchanged (converted to double), for every row.
- * Returns 0, or -1 for N outside 1..1024.
+ * Returns 0, or -1 for N outside 1..ORACLE_MAX_RANKS.
  */
 int oracle_combine(int dtype, int N, int B, int Hc, int D, int G,
                    const void* o, int64_t o_sg, int64_t o_sn, int64_t o_sb, int64_t o_sh,
                    const float* lse, int64_t l_sg, int64_t l_sn, int64_t l_sb, int64_t l_sh,
                    double* out, double* out_lse, int base, unsigned flags) {
-    if (N <= 0 || N > 1024) return -1;
+    if (N <= 0 || N > ORACLE_MAX_RANKS) return -1;
     const int e = elem_bytes(dtype);
-    double x[1024];
-    const void* rows[1024];
+    double x[ORACLE_MAX_RANKS];
+    const void* rows[ORACLE_MAX_RANKS];
     for (int g = 0; g < G; ++g)
         for (int b = 0; b < B; ++b)
             for (int h = 0; h < Hc; ++h) {
@@ -282,12 +285,12 @@ int oracle_combine(int dtype, int N, int B, int Hc, int D, int G,
 int oracle_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
                           const void* recv, int64_t r_sg, int64_t r_sn, int64_t r_sb, int64_t r_sh,
                           double* out, double* out_lse, int base, unsigned flags) {
-    if (N <= 0 || N > 1024) return -1;
+    if (N <= 0 || N > ORACLE_MAX_RANKS) return -1;
     const int lpd = oracle_lse_pack_dim(dtype);
     if (lpd <= 0 || D % lpd != 0) return -2;
     const int e = elem_bytes(dtype);
-    double x[1024];
-    const void* rows[1024];
+    double x[ORACLE_MAX_RANKS];
+    const void* rows[ORACLE_MAX_RANKS];
     for (int g = 0; g < G; ++g)
         for (int b = 0; b < B; ++b)
             for (int h = 0; h < Hpr; ++h) {

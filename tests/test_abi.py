@@ -170,6 +170,30 @@ def test_workspace_size_refuses_sizes_the_call_refuses(lib):
     assert ws(4096, 1 << 10, 64, 128, 1 << 24, 1024) == 4096 * 1024 * 64 * 4 * 129 * 4
 
 
+def test_error_messages_belong_to_the_calling_thread(lib):
+    # three host threads fail (or succeed) differently, wait for one another,
+    # then read dcp_last_error_message(): each sees its own last call only
+    import threading
+    calls = {"heads": lambda: pack(N=3), "flags": lambda: combine(flags=8), "ok": lambda: combine(B=0)}
+    seen, status = {}, {}
+    barrier = threading.Barrier(len(calls))
+
+    def run(name):
+        status[name] = calls[name]()
+        barrier.wait()
+        seen[name] = binding.dcp_last_error_message()
+
+    threads = [threading.Thread(target=run, args=(n,)) for n in calls]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert status == {"heads": 3, "flags": 1, "ok": 0}
+    assert "not a multiple" in seen["heads"]
+    assert "flags" in seen["flags"] and "multiple" not in seen["flags"]
+    assert seen["ok"] == ""
+
+
 def test_binding_raises_with_message(lib):
     with pytest.raises(binding.DcpError) as ei:
         binding.check(pack(N=3), "dcp_pack_send")
