@@ -278,3 +278,58 @@ def test_paged_caches_give_the_contiguous_result(N, H, Hkv, D, lens, dtype, base
     want, want_lse = oracle_partials(q, K, V, lens, N, scale, base)
     assert_merge_close(o2, want, "paged rank partial O")
     assert_attn_lse(lse2, want_lse)
+
+
+STRIDED = [
+    # N, H, Hkv, D, lengths, dtype, split_tokens, cache layout, paged page size (0: contiguous)
+    (3, 4, 4, 128, [0, 9, 300], torch.bfloat16, 64, "kv_interleaved", 0),      # CUDA cores
+    (2, 16, 2, 128, [5, 700], torch.float16, 128, "head_major", 0),            # tensor cores
+    (2, 4, 2, 256, [33, 90], torch.bfloat16, 32, "kv_interleaved", 0),         # two heads at D = 256
+    (4, 8, 2, 64, [1, 250, 513], torch.bfloat16, 4096, "head_major", 0),       # one split
+    (2, 8, 2, 128, [17, 400], torch.bfloat16, 48, "kv_interleaved", 16),       # paged, interleaved pool
+]
+
+
+@pytest.mark.parametrize("N,H,Hkv,D,lens,dtype,split,layout,page", STRIDED)
+def test_strided_operands_give_the_contiguous_result(N, H, Hkv, D, lens, dtype, split, layout, page):
+    """Operands as serving engines hold them: q sliced out of a fused
+    [B, H + 2 Hkv, D] projection, K and V interleaved in one cache
+    ([.., 2, Hkv, D] per token) or head-major ([.., Hkv, Lc, D]), the output
+    rows padded and the LSE a strided slot of a [.., 2] stats array.  The
+    kernels only follow the strides, so the results equal the contiguous
+    call's bit for bit."""
+    B = len(lens)
+    q, K, V, seq, L = make_case(N, B, H, Hkv, D, lens, dtype, seed=500 + D + H)
+    scale = 1.0 / math.sqrt(D)
+    base = "2" if page else "e"
+    o_ref, lse_ref = run_attention(q, K, V, seq, L, N, scale, base, split)
+
+    fused = torch.randn((B, H + 2 * Hkv, D), device=DEV).to(dtype)
+    fused[:, :H] = q
+    qs = fused[:, :H]
+    k_loc, v_loc = local_caches(K, N), local_caches(V, N)           # [N, B, Lc, Hkv, D]
+    if page:
+        k_loc, v_loc, bt = paged_caches(k_loc, v_loc, page, seed=page)  # pools [N, P, page, Hkv, D]
+    if layout == "kv_interleaved":
+        kv = torch.empty(k_loc.shape[:3] + (2,) + k_loc.shape[3:], dtype=dtype, device=DEV)
+        kv[:, :, :, 0], kv[:, :, :, 1] = k_loc, v_loc
+        ks, vs = kv[:, :, :, 0], kv[:, :, :, 1]
+    else:
+        ks = k_loc.permute(0, 1, 3, 2, 4).contiguous().permute(0, 1, 3, 2, 4)
+        vs = v_loc.permute(0, 1, 3, 2, 4).contiguous().permute(0, 1, 3, 2, 4)
+    assert not ks.is_contiguous() and not qs.is_contiguous()
+    obuf = torch.full((N, B, H, D + 24), 7.0, device=DEV).to(dtype)
+    lbuf = torch.full((N, B, H, 2), 7.0, device=DEV)
+    o, lse = obuf[..., :D], lbuf[..., 0]
+    nbytes = binding.workspace_bytes(N, B, H, D, L, split)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=DEV) if nbytes else None
+    if page:
+        binding.decode_attention_paged(qs, ks, vs, bt, seq, L, o, lse, scale, base=base, split_tokens=split,
+                                       workspace=ws)
+    else:
+        binding.decode_attention(qs, ks, vs, seq, L, o, lse, scale, base=base, split_tokens=split, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o.contiguous().view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse.contiguous().view(torch.int32), lse_ref.view(torch.int32))
+    # nothing outside the views was written
+    assert bool((obuf[..., D:] == 7.0).all()) and bool((lbuf[..., 1] == 7.0).all())
