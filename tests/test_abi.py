@@ -36,6 +36,42 @@ def test_header_declares_exactly_the_binding_exports():
     assert declared_functions() == sorted(binding.EXPORTS)
 
 
+def declared_signatures():
+    """{name: (return type, [parameter types])} parsed from include/dcp.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    sigs = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w ]*?\**)\s*\b(dcp_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", text):
+        types = []
+        for prm in params.split(","):
+            prm = " ".join(prm.split())
+            if prm in ("", "void"):
+                continue
+            types.append(re.sub(r"\s*\b\w+$", "", prm) if not prm.endswith("*") else prm)
+        sigs[name] = (" ".join(ret.split()), types)
+    return sigs
+
+
+def ctype_of(c_type: str):
+    c_type = c_type.replace("const ", "").strip()
+    if c_type.endswith("*"):
+        return ctypes.c_char_p if c_type == "char*" else ctypes.c_void_p
+    return {"int": ctypes.c_int, "unsigned": ctypes.c_uint, "int64_t": ctypes.c_int64,
+            "size_t": ctypes.c_size_t, "float": ctypes.c_float, "dcp_status_t": ctypes.c_int}[c_type]
+
+
+def test_binding_marshals_exactly_the_declared_signatures(lib):
+    # every parameter's C type in the header against the ctypes type the
+    # binding passes (a 32-bit int where the header has int64_t would
+    # truncate strides silently)
+    sigs = declared_signatures()
+    assert sorted(sigs) == sorted(binding.EXPORTS)
+    for name, (ret, params) in sigs.items():
+        fn = getattr(lib, name)
+        want = [ctype_of(t) for t in params]
+        assert list(fn.argtypes) == want, f"{name}: argtypes {fn.argtypes} vs header {params}"
+        assert fn.restype == ctype_of(ret), f"{name}: restype {fn.restype} vs header {ret}"
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
