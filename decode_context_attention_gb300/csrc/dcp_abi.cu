@@ -445,10 +445,16 @@ dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
         return fail(DCP_ERR_MISALIGNED, "%s: receive rows must start on 4-byte boundaries", who);
     if (!fp8_rows_ok(e, D, vr.align(), vu.align()))
         return fail(DCP_ERR_MISALIGNED, "%s: fp8 rows need 4-byte aligned row starts", who);
-    if (overlap(vu, vr)) return fail(DCP_ERR_ALIAS, "%s: out overlaps recv", who);
+    // Rows that start 4 but not 16 bytes past a 16-byte boundary are read in
+    // 16-byte chunks from that boundary, so up to 12 bytes before the first
+    // row's start are read (and ignored): the outputs must not lie there.
+    View vr_read = vr;
+    vr_read.inner += (int64_t)(vr.base & 15u);
+    vr_read.base &= ~(uintptr_t)15u;
+    if (overlap(vu, vr_read)) return fail(DCP_ERR_ALIAS, "%s: out overlaps recv", who);
     if (!vu.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out rows overlap one another", who);
     if (return_lse) {
-        if (overlap(vul, vr) || overlap(vul, vu))
+        if (overlap(vul, vr_read) || overlap(vul, vu))
             return fail(DCP_ERR_ALIAS, "%s: out_lse overlaps recv or out", who);
         if (!vul.rows_disjoint()) return fail(DCP_ERR_ALIAS, "%s: out_lse entries overlap", who);
     }

@@ -33,7 +33,6 @@
 #include <math.h>
 #include <stdio.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "dcp_device.cuh"
@@ -677,8 +676,15 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB, reserved on every device that loads this code
 static __device__ __align__(256) float g_attn_scratch[kNoAllocScratchBytes / sizeof(float)];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {};  // device address of g_attn_scratch, per device
+// The array's device address belongs to the CUDA context the library's code
+// is loaded into, not to the device: cudaDeviceReset destroys the primary
+// context (the next runtime call loads the code again, maybe at another
+// address), and a caller may make its own driver-API context current instead
+// of the primary one.  So every call looks the address up in the context
+// current at that call (cudaGetSymbolAddress allocates nothing; on the first
+// call in a context it also loads the library's code there), and no address
+// outlives the call that looked it up.
+cudaError_t scratch_address(void** out) { return cudaGetSymbolAddress(out, g_attn_scratch); }
 
 }  // namespace
 
@@ -698,31 +704,13 @@ extern "C" dcp_status_t dcp_decode_attention_noalloc(
                  need, kNoAllocScratchBytes);
         return dcp::set_error(DCP_ERR_INVALID_ARG, msg);
     }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    void* scratch = nullptr;
+    const cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) {
         char msg[256];
-        snprintf(msg, sizeof(msg), "dcp_decode_attention_noalloc: no usable current device (%s)",
+        snprintf(msg, sizeof(msg), "dcp_decode_attention_noalloc: cudaGetSymbolAddress failed: %s",
                  cudaGetErrorString(e));
         return dcp::set_error(DCP_ERR_CUDA, msg);
-    }
-    void* scratch = nullptr;
-    {
-        // first call on this device: look up the array's device address once,
-        // with this device current
-        std::lock_guard<std::mutex> lock(g_scratch_mu);
-        if (!g_scratch_ptr[dev]) {
-            void* ptr = nullptr;
-            e = cudaGetSymbolAddress(&ptr, g_attn_scratch);
-            if (e != cudaSuccess) {
-                char msg[256];
-                snprintf(msg, sizeof(msg), "dcp_decode_attention_noalloc: cudaGetSymbolAddress failed: %s",
-                         cudaGetErrorString(e));
-                return dcp::set_error(DCP_ERR_CUDA, msg);
-            }
-            g_scratch_ptr[dev] = ptr;
-        }
-        scratch = g_scratch_ptr[dev];
     }
     return dcp_decode_attention(dtype, N, B, H, Hkv, D, q, q_sb, q_sh, k, k_sn, k_sb, k_st, k_sh, v, v_sn,
                                 v_sb, v_st, v_sh, seq_lens, max_seq_len, sm_scale, split_tokens, o, o_sn,

@@ -206,6 +206,15 @@ dcp_status_t dcp_lse_combine(int dtype, int N, int B, int Hc, int D, int G,
  * Same arithmetic, flags (except DCP_INPLACE_RANK0, rejected) and N == 1 rule
  * as dcp_lse_combine.  Errors: DCP_ERR_MISALIGNED if D % lpd != 0 or a row
  * start is not 4-byte aligned; DCP_ERR_ALIAS if out / out_lse overlap recv.
+ *
+ * Reads: rows that start on a 4- but not a 16-byte boundary (an interleaved
+ * row is D*e + 4 bytes long) may be read in 16-byte chunks from the 16-byte
+ * boundary at or before the row start, so up to 12 bytes before each row are
+ * read and ignored.  Those bytes lie in the same 16-byte granule as the row's
+ * first byte (never on another page); for every row but the first they are
+ * inside recv's own extent.  The bytes before the first row count as part of
+ * recv for the overlap check (an out or out_lse there is DCP_ERR_ALIAS), and
+ * another stream must not be writing them during the call.
  */
 dcp_status_t dcp_unpack_combine(int dtype, int N, int B, int Hpr, int D, int G,
                                 const void* recv, int64_t r_sg, int64_t r_sn, int64_t r_sb, int64_t r_sh,
@@ -306,9 +315,14 @@ dcp_status_t dcp_decode_attention_paged(int dtype, int N, int B, int H, int Hkv,
  * (dcp_decode_attention_workspace_size) exceeds 16 MiB are rejected with
  * DCP_ERR_INVALID_ARG and a message giving both sizes; use a larger
  * split_tokens or dcp_decode_attention with a workspace instead.  The call
- * allocates nothing.  Its first call on a device looks up the scratch
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  All calls share the one
+ * allocates nothing.  The scratch array's device address belongs to the
+ * CUDA context the library is loaded into (the device's primary context, or
+ * a driver-API context the caller made current), so every call looks it up
+ * (cudaGetSymbolAddress) in the context current at that call and keeps it no
+ * longer: after a cudaDeviceReset or a switch of context the next call uses
+ * the array of the new context.  The first call in a context also loads the
+ * library's device code there; make it before any stream capture.  All calls
+ * share the one
  * array and every call writes each scratch entry before reading it (nothing
  * needs to start at zero), so calls whose work overlaps on the GPU (other
  * streams, other threads) race on the scratch: serialise them.

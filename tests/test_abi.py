@@ -156,6 +156,15 @@ def test_unpack_validation(lib):
     assert unpack(B=0) == 0
 
 
+def test_unpack_counts_the_granule_before_the_first_row_as_read(lib):
+    # receive rows 4-byte aligned, the first 12 bytes past a 16-byte boundary:
+    # the merge may read [A, A + 12) in the 16-byte chunk holding the first
+    # row's start, so an output there is an overlap
+    assert unpack(recv=A + 12, out_lse=A - 24) == 5        # out_lse (32 bytes) ends at A + 8
+    assert "overlaps recv" in binding.dcp_last_error_message()
+    assert unpack(recv=A + 12, out=A + 8 - 128) == 5       # out (128 bytes) ends inside the granule
+
+
 def test_fp8_rows_need_four_byte_granularity(lib):
     # one e4m3 element is one byte: D % 4 == 0 and 4-byte aligned row starts
     assert pack(dtype=FP8, D=6, o_s=(48, 24, 6)) == 4

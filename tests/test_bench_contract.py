@@ -26,7 +26,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
     assert abs(d["ms_per_step"] * 1e3 - d["value"]) <= 1e-3 * d["value"]
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["sample"]
+    # timed on every host core the process may use, the 1-core time beside it
+    assert cb["cores"] == len(os.sched_getaffinity(0))
+    assert cb["single_core"]["cores"] == 1 and cb["single_core"]["value"] > 0
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert "workload" in d["config"]

@@ -94,3 +94,94 @@ def test_no_alloc_entry_point_refuses_sizes_beyond_its_scratch():
     st = lib.dcp_decode_attention_noalloc(*args, torch.cuda.current_stream().cuda_stream)
     assert st == 1  # DCP_ERR_INVALID_ARG
     assert "scratch" in binding.dcp_last_error_message()
+
+
+# A process of its own: it resets the device, which would pull the memory out
+# from under every tensor of the test session.  Only the CUDA runtime (through
+# ctypes) and the library run in it.
+_RESET_SCRIPT = r'''
+import ctypes, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from decode_context_attention_gb300 import binding
+
+lib = binding.load()
+cudart_path = next(line.split()[-1] for line in open("/proc/self/maps") if "libcudart.so" in line)
+rt = ctypes.CDLL(cudart_path)
+rt.cudaMalloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t]
+rt.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+rt.cudaFree.argtypes = [ctypes.c_void_p]
+
+def ok(e, what):
+    if e != 0:
+        raise SystemExit(f"{what} failed with CUDA error {e}")
+
+N, B, H, Hkv, D, split = 4, 3, 8, 4, 128, 32
+lens = np.array([700, 5, 129], dtype=np.int32)
+L = int(lens.max())
+lc = (L + N - 1) // N
+rng = np.random.default_rng(5)
+def bf16(shape):
+    f = rng.standard_normal(shape).astype(np.float32)
+    return ((f.view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
+host = {"q": bf16((B, H, D)), "k": bf16((N, B, lc, Hkv, D)), "v": bf16((N, B, lc, Hkv, D)), "seq": lens}
+need = binding.workspace_bytes(N, B, H, D, L, split)
+assert need > 0
+
+def run(noalloc):
+    dev = {}
+    for name, a in host.items():
+        p = ctypes.c_void_p()
+        ok(rt.cudaMalloc(ctypes.byref(p), a.nbytes), "cudaMalloc")
+        ok(rt.cudaMemcpy(p, a.ctypes.data, a.nbytes, 1), "cudaMemcpy H2D")
+        dev[name] = p.value
+    sizes = {"o": N * B * H * D * 2, "lse": N * B * H * 4, "ws": need}
+    for name, n in sizes.items():
+        p = ctypes.c_void_p()
+        ok(rt.cudaMalloc(ctypes.byref(p), n), "cudaMalloc")
+        dev[name] = p.value
+    args = (2, N, B, H, Hkv, D, dev["q"], H * D, D,
+            dev["k"], B * lc * Hkv * D, lc * Hkv * D, Hkv * D, D,
+            dev["v"], B * lc * Hkv * D, lc * Hkv * D, Hkv * D, D,
+            dev["seq"], L, 1.0 / D ** 0.5, split,
+            dev["o"], B * H * D, H * D, D, dev["lse"], B * H, H, 1, 1)
+    if noalloc:
+        st = lib.dcp_decode_attention_noalloc(*args, None)
+    else:
+        st = lib.dcp_decode_attention(*args, dev["ws"], need, None)
+    assert st == 0, binding.dcp_last_error_message()
+    ok(rt.cudaDeviceSynchronize(), "kernels")
+    o = np.empty(N * B * H * D, dtype=np.uint16)
+    lse = np.empty(N * B * H, dtype=np.uint32)
+    ok(rt.cudaMemcpy(o.ctypes.data, dev["o"], o.nbytes, 2), "cudaMemcpy D2H")
+    ok(rt.cudaMemcpy(lse.ctypes.data, dev["lse"], lse.nbytes, 2), "cudaMemcpy D2H")
+    for p in dev.values():
+        ok(rt.cudaFree(ctypes.c_void_p(p)), "cudaFree")
+    return o, lse
+
+ok(rt.cudaSetDevice(0), "cudaSetDevice")
+for attempt in range(2):
+    want_o, want_l = run(noalloc=False)
+    got_o, got_l = run(noalloc=True)
+    assert np.array_equal(want_o, got_o) and np.array_equal(want_l, got_l), f"attempt {attempt}: differs"
+    assert (want_l != 0).any()
+    if attempt == 0:
+        ok(rt.cudaDeviceReset(), "cudaDeviceReset")
+print("noalloc ok across a device reset")
+'''
+
+
+def test_no_alloc_entry_point_after_a_device_reset():
+    # cudaDeviceReset ends the context the scratch array's address was looked
+    # up in; the next call must find the array of the new context, and give
+    # the workspace entry point's result bit for bit again
+    import os
+    import subprocess
+    import sys
+
+    build.build()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _RESET_SCRIPT, root], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "noalloc ok across a device reset" in r.stdout
