@@ -18,7 +18,7 @@ pages and mathematics fix (identity at N=1, neutral empty ranks, shift
 invariance, base-2/base-e agreement, closed forms, brute-force split
 attention equal to unsplit attention, round-robin partition invariants,
 numpy's own fp16/bf16 decoding and index maps); ``tests/test_oracle_mutants.py``
-shows that 24 planted slips in ``dcp_oracle.c`` each make one of those pins fail.
+shows that 28 planted slips in ``dcp_oracle.c`` each make one of those pins fail.
 """
 from __future__ import annotations
 
@@ -79,6 +79,9 @@ def _load():
         lib.oracle_split_attention.restype = None
         lib.oracle_split_attention.argtypes = [i32, i32, i32, ctypes.c_double, vp, vp, vp, i32,
                                                vp, vp]
+        lib.oracle_split_attention_mla.restype = None
+        lib.oracle_split_attention_mla.argtypes = [i32, i32, i32, i32, ctypes.c_double, vp, vp, i32,
+                                                   vp, vp]
         lib.oracle_lse_pack_dim.restype = i32
         lib.oracle_lse_pack_dim.argtypes = [i32]
         lib.oracle_decode_elem.restype = ctypes.c_double
@@ -196,4 +199,21 @@ def split_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int, scale: 
     lse = np.empty((n,), dtype=np.float64)
     _load().oracle_split_attention(L, D, n, float(scale), _ptr(q), _ptr(K), _ptr(V),
                                    BASES[base], _ptr(O), _ptr(lse))
+    return O, lse
+
+
+def split_attention_mla(q: np.ndarray, KV: np.ndarray, Dv: int, n: int, scale: float,
+                        base: str = "e") -> tuple[np.ndarray, np.ndarray]:
+    """Per-rank (O [n,Dv], lse [n]) of single-query attention over a latent
+    cache KV [L, Dk] whose value is each row's first Dv elements (absorbed
+    MLA), under round-robin KV ownership."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    KV = np.ascontiguousarray(KV, dtype=np.float64)
+    L, Dk = KV.shape
+    if q.shape != (Dk,) or not 0 < Dv <= Dk:
+        raise ValueError("q must have Dk elements and 0 < Dv <= Dk")
+    O = np.empty((n, Dv), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _load().oracle_split_attention_mla(L, Dk, Dv, n, float(scale), _ptr(q), _ptr(KV),
+                                       BASES[base], _ptr(O), _ptr(lse))
     return O, lse

@@ -32,6 +32,10 @@
  *   oracle_split_attention sglang PR #33926 report, "实现拆解" item 3
  *                         (each rank returns rank-local (out, lse); a rank
  *                         owning no KV is neutralised to (0, -inf)).
+ *   oracle_split_attention_mla  the same over a latent cache (absorbed MLA,
+ *                         the trtllm_mla decode path of that report): the
+ *                         score uses the whole latent row, the value is its
+ *                         first kv_lora_rank elements.
  *
  * Readings taken where the pages are silent (each is also listed in the
  * design notes):
@@ -365,5 +369,49 @@ void oracle_split_attention(int L, int D, int n, double scale, const double* q,
             for (int d = 0; d < D; ++d) O[(int64_t)r * D + d] += p * V[(int64_t)t * D + d];
         }
         lse[r] = base == ORACLE_BASE_2 ? l / ln2() : l;
+    }
+}
+
+/* ---- split single-query attention over a latent cache (absorbed MLA) ---- */
+/*
+ * sglang PR #33926 report, "功能与动机" and "实现拆解" items 3-4: the trtllm_mla
+ * decode path (absorbed multi-head latent attention, DeepSeek-V3 class) returns
+ * rank-local (out, lse) under the round-robin owner rule; sglang PR #34213
+ * report, "功能与动机": for absorbed MLA the output width is kv_lora_rank.
+ * Every query head scores one shared latent row per token,
+ *   KV_t [Dk] = [ c_t (Dv elements, kv_lora_rank) | k_rope_t (Dk - Dv elements) ],
+ * against its absorbed query q [Dk] (the query's rope part concatenated after
+ * its absorbed no-rope part), and the value is the row's first Dv elements:
+ *   s_t   = scale <q, KV_t>                         (all Dk elements)
+ *   lse_r = log sum_{t owned by r} exp(s_t)         (base 2: lse_r / ln 2)
+ *   O_r   = sum_{t owned by r} exp(s_t - lse_r) KV_t[0:Dv]
+ * A rank that owns no token returns (O = 0, lse = -inf).
+ * q [Dk], KV [L, Dk] (double); O: [n, Dv]; lse: [n].
+ */
+/* <q, KV_t> over the whole latent row. */
+static double latent_dot(const double* q, const double* row, int Dk) {
+    double acc = 0.0;
+    for (int d = 0; d < Dk; ++d) acc += q[d] * row[d];
+    return acc;
+}
+
+void oracle_split_attention_mla(int L, int Dk, int Dv, int n, double scale, const double* q,
+                                const double* KV, int base, double* O, double* lse) {
+    for (int r = 0; r < n; ++r) {
+        double* Or = O + (int64_t)r * Dv;
+        for (int d = 0; d < Dv; ++d) Or[d] = 0.0;
+        lse[r] = -INFINITY; /* the neutral pair, kept when rank r owns no token (none when r >= L) */
+        if (r >= L) continue;
+        double smax = -INFINITY;
+        for (int t = r; t < L; t += n) smax = fmax(smax, scale * latent_dot(q, KV + (int64_t)t * Dk, Dk));
+        double z = 0.0;
+        for (int t = r; t < L; t += n) z += exp(scale * latent_dot(q, KV + (int64_t)t * Dk, Dk) - smax);
+        const double lse_nat = smax + log(z);
+        for (int t = r; t < L; t += n) {
+            const double* row = KV + (int64_t)t * Dk;
+            const double prob = exp(scale * latent_dot(q, row, Dk) - lse_nat);
+            for (int d = 0; d < Dv; ++d) Or[d] += prob * row[d]; /* value: the row's first Dv elements */
+        }
+        lse[r] = base == ORACLE_BASE_2 ? lse_nat / ln2() : lse_nat;
     }
 }

@@ -424,6 +424,73 @@ def test_merged_split_attention_equals_unsplit_attention(base):
         assert np.allclose(G_ * conv, want_lse, rtol=0, atol=2e-6)
 
 
+def latent_attention(q, KV, Dv, scale):
+    """Unsplit single-query attention over latent rows: scores over the whole
+    row, the value is the row's first Dv elements (numpy, for the pins)."""
+    return full_attention(q, KV, KV[:, :Dv], scale)
+
+
+def test_split_attention_mla_single_rank_is_full_latent_attention():
+    # one rank owns every token: attention over the whole latent cache, the
+    # value being each row's first Dv elements; a nonzero rope part moves the
+    # scores, not the value
+    rng = np.random.default_rng(14)
+    for L in (1, 2, 9, 40):
+        Dk, Dv = 12, 8
+        q, KV = rng.standard_normal(Dk), rng.standard_normal((L, Dk))
+        O, lse = oracle.split_attention_mla(q, KV, Dv, 1, 0.4)
+        want, want_lse = latent_attention(q, KV, Dv, 0.4)
+        assert np.allclose(O[0], want, rtol=0, atol=1e-13)
+        assert abs(lse[0] - want_lse) < 1e-13
+        O2, lse2 = oracle.split_attention_mla(q, KV, Dv, 1, 0.4, base="2")
+        assert np.array_equal(O2, O)
+        assert abs(lse2[0] * math.log(2.0) - want_lse) < 1e-13
+        # the rope columns enter only through the scores
+        KV2 = KV.copy()
+        KV2[:, Dv:] = 0.0
+        q2 = q.copy()
+        q2[Dv:] = 0.0
+        O3, lse3 = oracle.split_attention_mla(q2, KV2, Dv, 1, 0.4)
+        want3, want3_lse = full_attention(q[:Dv], KV[:, :Dv], KV[:, :Dv], 0.4)
+        assert np.allclose(O3[0], want3, rtol=0, atol=1e-13) and abs(lse3[0] - want3_lse) < 1e-13
+
+
+def test_split_attention_mla_at_full_value_width_is_split_attention():
+    # with Dv = Dk the latent row is both key and value: the MHA split
+    # attention with K = V = KV, rank by rank, for every group size
+    rng = np.random.default_rng(15)
+    for n in page_cases()["dcp_layout"]["value"]["sizes"]:
+        for L in (0, 1, 3, 17):
+            D = 6
+            q, KV = rng.standard_normal(D), rng.standard_normal((L, D))
+            O, lse = oracle.split_attention_mla(q, KV, D, n, 0.9, base="2")
+            O2, lse2 = oracle.split_attention(q, KV, KV, n, 0.9, base="2")
+            assert np.allclose(O, O2, rtol=0, atol=1e-14)
+            fin = np.isfinite(lse2)
+            assert np.array_equal(np.isfinite(lse), fin) and np.all(lse[~fin] == -np.inf)
+            assert np.allclose(lse[fin], lse2[fin], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("base", ["e", "2"])
+def test_merged_split_attention_mla_equals_unsplit_attention(base):
+    """Split over N ranks by the round-robin owner rule and merged by the
+    combine, latent-cache attention equals unsplit attention (numpy)."""
+    rng = np.random.default_rng(16 if base == "e" else 17)
+    Dk, Dv = 10, 6
+    for N in page_cases()["dcp_layout"]["value"]["sizes"]:
+        for L in range(1, 41, 3):
+            q, KV = rng.standard_normal(Dk), rng.standard_normal((L, Dk))
+            O, lse = oracle.split_attention_mla(q, KV, Dv, N, 0.6, base=base)
+            for r in range(N):
+                assert (lse[r] == -np.inf) == (r >= L)
+            out, G_ = oracle.combine("f64", O[None, :, None, None, :],
+                                     lse.astype(np.float32)[None, :, None, None], base=base)
+            want, want_lse = latent_attention(q, KV, Dv, 0.6)
+            assert np.allclose(out[0, 0, 0], want, rtol=0, atol=2e-6)
+            conv = math.log(2.0) if base == "2" else 1.0
+            assert abs(G_[0, 0, 0] * conv - want_lse) < 2e-6
+
+
 # --------------------------------------------------------------------------
 # fused unpack + combine over the interleaved receive rows
 # --------------------------------------------------------------------------

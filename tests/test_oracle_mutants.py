@@ -60,6 +60,14 @@ MUTANTS = [
      "            lse[r] = 0.0;\n            continue;"),
     ("attention probabilities without the scale", "const double p = exp(s * scale - l);",
      "const double p = exp(s - l);"),
+    ("latent value read from the rope end", "Or[d] += prob * row[d];", "Or[d] += prob * row[Dk - Dv + d];"),
+    ("latent probabilities scored over the value part only",
+     "const double prob = exp(scale * latent_dot(q, row, Dk) - lse_nat);",
+     "const double prob = exp(scale * latent_dot(q, row, Dv) - lse_nat);"),
+    ("latent LSE left in natural-log units for base 2",
+     "lse[r] = base == ORACLE_BASE_2 ? lse_nat / ln2() : lse_nat;", "lse[r] = lse_nat;"),
+    ("latent attention skips each rank's first token", "for (int t = r; t < L; t += n) z +=",
+     "for (int t = r + n; t < L; t += n) z +="),
 ]
 
 
