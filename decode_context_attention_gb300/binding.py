@@ -33,11 +33,12 @@ DCP_LSE_BASE_E, DCP_LSE_BASE_2 = 0, 1
 DCP_SANITIZE_O, DCP_INPLACE_RANK0 = 1, 2
 STATUS_NAMES = {0: "DCP_OK", 1: "DCP_ERR_INVALID_ARG", 2: "DCP_ERR_UNSUPPORTED_DTYPE",
                 3: "DCP_ERR_HEADS_NOT_DIVISIBLE", 4: "DCP_ERR_MISALIGNED", 5: "DCP_ERR_ALIAS",
-                6: "DCP_ERR_CUDA"}
+                6: "DCP_ERR_CUDA", 7: "DCP_ERR_TIMEOUT"}
 # Every symbol include/dcp.h declares.
 EXPORTS = ("dcp_lse_pack_dim", "dcp_status_string", "dcp_last_error_message", "dcp_pack_send",
            "dcp_lse_combine", "dcp_unpack_combine", "dcp_decode_attention_workspace_size",
-           "dcp_decode_attention", "dcp_decode_attention_paged", "dcp_decode_attention_noalloc")
+           "dcp_decode_attention", "dcp_decode_attention_paged", "dcp_decode_attention_noalloc",
+           "dcp_decode_attention_mla", "dcp_device_status")
 
 
 class DcpError(RuntimeError):
@@ -91,6 +92,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                    + lib.dcp_decode_attention.argtypes[19:])
         lib.dcp_decode_attention_noalloc.restype = i32
         lib.dcp_decode_attention_noalloc.argtypes = lib.dcp_decode_attention.argtypes[:-3] + [vp]
+        lib.dcp_decode_attention_mla.restype = i32
+        lib.dcp_decode_attention_mla.argtypes = ([i32] * 6 + [vp, i64, i64] + [vp, i64, i64, i64]
+                                                 + lib.dcp_decode_attention.argtypes[19:])
+        lib.dcp_device_status.restype = i32
+        lib.dcp_device_status.argtypes = []
         _lib = lib
         return lib
 
@@ -130,6 +136,14 @@ def dcp_decode_attention_workspace_size(N: int, B: int, H: int, D: int, max_seq_
 
 def dcp_decode_attention(*args) -> int:
     return load().dcp_decode_attention(*args)
+
+
+def dcp_decode_attention_mla(*args) -> int:
+    return load().dcp_decode_attention_mla(*args)
+
+
+def dcp_device_status() -> int:
+    return load().dcp_device_status()
 
 
 def check(status: int, where: str) -> None:
@@ -348,6 +362,49 @@ def decode_attention(q, k, v, seq_lens, max_seq_len, o, lse, sm_scale, base="e",
                      workspace=None, stream=None) -> None:
     prepare_decode_attention(q, k, v, seq_lens, max_seq_len, o, lse, sm_scale, base, split_tokens,
                              workspace, stream)()
+
+
+def prepare_decode_attention_mla(q: torch.Tensor, kv: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                                 o: torch.Tensor, lse: torch.Tensor, sm_scale: float, base: str = "2",
+                                 split_tokens: int = 1024, workspace: torch.Tensor | None = None,
+                                 stream=None) -> _Prepared:
+    """Each rank's decode attention over its round-robin share of an
+    absorbed-MLA latent cache.
+
+    q [B,H,Dk]; kv [N,B,Lc,Dk] latent caches (the value is each row's first
+    Dv = o.shape[-1] elements); seq_lens [B] int32 global lengths;
+    o [N,B,H,Dv], lse [N,B,H].  `workspace` as for prepare_decode_attention,
+    sized workspace_bytes(N, B, H, Dv, max_seq_len, split_tokens)."""
+    _need_cuda(q, kv, seq_lens, o, lse, workspace)
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    for t in (q, kv, o):
+        _inner_ok(t)
+    B, H, Dk = q.shape
+    N = kv.shape[0]
+    Dv = o.shape[-1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = (_dtype_code(q), N, B, H, Dk, Dv,
+            q.data_ptr(), q.stride(0), q.stride(1),
+            kv.data_ptr(), kv.stride(0), kv.stride(1), kv.stride(2),
+            seq_lens.data_ptr(), int(max_seq_len), float(sm_scale), int(split_tokens),
+            o.data_ptr(), o.stride(0), o.stride(1), o.stride(2),
+            lse.data_ptr(), lse.stride(0), lse.stride(1), lse.stride(2),
+            _base_code(base), None if workspace is None else workspace.data_ptr(), ws_bytes,
+            _stream_handle(stream))
+    return _Prepared("dcp_decode_attention_mla", args, (q, kv, seq_lens, o, lse, workspace))
+
+
+def decode_attention_mla(q, kv, seq_lens, max_seq_len, o, lse, sm_scale, base="2", split_tokens=1024,
+                         workspace=None, stream=None) -> None:
+    prepare_decode_attention_mla(q, kv, seq_lens, max_seq_len, o, lse, sm_scale, base, split_tokens,
+                                 workspace, stream)()
+
+
+def device_status() -> int:
+    """dcp_device_status(): 0, or DCP_ERR_TIMEOUT when a tensor-core kernel
+    gave up on a bounded wait since the last call (synchronises)."""
+    return load().dcp_device_status()
 
 
 def workspace_bytes(N: int, B: int, H: int, D: int, max_seq_len: int, split_tokens: int) -> int:

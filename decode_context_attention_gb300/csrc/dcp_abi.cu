@@ -231,6 +231,7 @@ const char* dcp_status_string(int status) {
         case DCP_ERR_MISALIGNED: return "misaligned pointer, stride or head dim";
         case DCP_ERR_ALIAS: return "an output overlaps an input or itself";
         case DCP_ERR_CUDA: return "CUDA error";
+        case DCP_ERR_TIMEOUT: return "a kernel gave up on a bounded wait (its outputs are invalid)";
         default: return "unknown status";
     }
 }
@@ -638,6 +639,97 @@ dcp_status_t dcp_decode_attention_paged(int dtype, int N, int B, int H, int Hkv,
     return run_attention("dcp_decode_attention_paged", dtype, N, B, H, Hkv, D, q, q_sb, q_sh, kv, seq_lens,
                          max_seq_len, sm_scale, split_tokens, o, o_sn, o_sb, o_sh, lse, l_sn, l_sb, l_sh,
                          lse_base, workspace, workspace_bytes, stream);
+}
+
+dcp_status_t dcp_decode_attention_mla(int dtype, int N, int B, int H, int Dk, int Dv,
+                                      const void* q, int64_t q_sb, int64_t q_sh,
+                                      const void* kv, int64_t kv_sn, int64_t kv_sb, int64_t kv_st,
+                                      const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                      void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                      float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                      int lse_base, void* workspace, size_t workspace_bytes, void* stream) {
+    const char* who = "dcp_decode_attention_mla";
+    if (dtype != DCP_F16 && dtype != DCP_BF16)
+        return fail(DCP_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d (f16 or bf16 caches only)", who, dtype);
+    const int e = 2;
+    if (N < 1 || N > kMaxRanks || B < 0 || H < 1 || max_seq_len < 0)
+        return fail(DCP_ERR_INVALID_ARG, "%s: sizes N=%d B=%d H=%d max_seq_len=%d", who, N, B, H, max_seq_len);
+    if (H > 128) return fail(DCP_ERR_INVALID_ARG, "%s: H=%d query heads (at most 128)", who, H);
+    if (Dk != 576 || Dv != 512)
+        return fail(DCP_ERR_INVALID_ARG, "%s: Dk=%d Dv=%d (latent rows of 576 = 512 + 64 rope, value 512)", who,
+                    Dk, Dv);
+    if (split_tokens < 64 || split_tokens % 64)
+        return fail(DCP_ERR_INVALID_ARG, "%s: split_tokens=%d (a positive multiple of 64)", who, split_tokens);
+    if (!(sm_scale == sm_scale) || sm_scale == INFINITY || sm_scale == -INFINITY)
+        return fail(DCP_ERR_INVALID_ARG, "%s: sm_scale is not finite", who);
+    if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2)
+        return fail(DCP_ERR_INVALID_ARG, "%s: lse_base %d", who, lse_base);
+    if (B == 0) return ok();
+    const int64_t lcap = ((int64_t)max_seq_len + N - 1) / N;
+    const int nsplit = attn_nsplit(N, max_seq_len, split_tokens);
+    if (2 * (int64_t)N * B * nsplit >= (1ll << 31))
+        return fail(DCP_ERR_INVALID_ARG, "%s: too many work items (2*N*B*splits >= 2^31)", who);
+    if (!q || !kv || !seq_lens || !o || !lse) return fail(DCP_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (bad_stride({q_sb, q_sh, kv_sn, kv_sb, kv_st, o_sn, o_sb, o_sh, l_sn, l_sb, l_sh}))
+        return fail(DCP_ERR_INVALID_ARG, "%s: negative stride or one above 2^52 elements", who);
+    // the cache is read by TMA as a [N][B][lcap][576] tensor: 16-byte aligned
+    // base, strides that are nonzero multiples of 16 bytes below 2^40
+    for (int64_t st : {kv_sn, kv_sb, kv_st})
+        if (st <= 0 || st % 8 || st * e >= (int64_t(1) << 40))
+            return fail(DCP_ERR_MISALIGNED, "%s: cache strides must be positive multiples of 8 elements below 2^39",
+                        who);
+    if (kv_st < Dk) return fail(DCP_ERR_INVALID_ARG, "%s: token stride %lld below the row of %d elements", who,
+                                (long long)kv_st, Dk);
+    if ((uintptr_t)kv % 16) return fail(DCP_ERR_MISALIGNED, "%s: cache not 16-byte aligned", who);
+    View vq = View(q, (int64_t)Dk * e).dim(B, q_sb * e).dim(H, q_sh * e);
+    View vk = View(kv, (int64_t)Dk * e).dim(N, kv_sn * e).dim(B, kv_sb * e).dim(lcap, kv_st * e);
+    View vo = View(o, (int64_t)Dv * e).dim(N, o_sn * e).dim(B, o_sb * e).dim(H, o_sh * e);
+    View vl = View(lse, 4).dim(N, l_sn * 4).dim(B, l_sb * 4).dim(H, l_sh * 4);
+    View vs = View(seq_lens, 4).dim(B, 4);
+    if (!all_fit({&vq, &vk, &vo, &vl, &vs}))
+        return fail(DCP_ERR_INVALID_ARG, "%s: an operand's strides span more than 2^56 bytes", who);
+    if (vq.align() < 16 || vo.align() < 16)
+        return fail(DCP_ERR_MISALIGNED, "%s: q and o rows must start on 16-byte boundaries", who);
+    if ((uintptr_t)lse % 4 || (uintptr_t)seq_lens % 4)
+        return fail(DCP_ERR_MISALIGNED, "%s: pointer not aligned to its element type", who);
+    for (const View* in : {&vq, &vk, &vs})
+        if (overlap(vo, *in) || overlap(vl, *in)) return fail(DCP_ERR_ALIAS, "%s: an output overlaps an input", who);
+    if (overlap(vo, vl) || !vo.rows_disjoint() || !vl.rows_disjoint())
+        return fail(DCP_ERR_ALIAS, "%s: outputs overlap", who);
+    const size_t need = attn_workspace_bytes(N, B, H, Dv, nsplit);
+    if (need) {
+        if (!workspace || workspace_bytes < need)
+            return fail(DCP_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed (%zu given)", who, need,
+                        workspace ? workspace_bytes : (size_t)0);
+        if ((uintptr_t)workspace % 16) return fail(DCP_ERR_MISALIGNED, "%s: workspace not 16-byte aligned", who);
+        View vw = View(workspace, (int64_t)need);
+        for (const View* other : {&vq, &vk, &vs, &vo, &vl})
+            if (overlap(vw, *other)) return fail(DCP_ERR_ALIAS, "%s: workspace overlaps an operand", who);
+    }
+    dcp::MlaParams p;
+    p.N = N; p.B = B; p.H = H; p.lcap = lcap;
+    p.max_seq_len = max_seq_len; p.split_tokens = split_tokens; p.nsplit = nsplit;
+    p.base2 = lse_base == DCP_LSE_BASE_2;
+    p.sm_scale = sm_scale;
+    p.q = (const unsigned char*)q; p.q_sb = q_sb * e; p.q_sh = q_sh * e;
+    p.kv = (const unsigned char*)kv; p.kv_sn = kv_sn * e; p.kv_sb = kv_sb * e; p.kv_st = kv_st * e;
+    p.seq_lens = seq_lens;
+    p.o = (unsigned char*)o; p.o_sn = o_sn * e; p.o_sb = o_sb * e; p.o_sh = o_sh * e;
+    p.lse = lse; p.l_sn = l_sn; p.l_sb = l_sb; p.l_sh = l_sh;
+    const size_t rows = (size_t)N * B * H * nsplit;
+    p.ws_o = need ? (float*)workspace : nullptr;
+    p.ws_lse = need ? (float*)workspace + rows * Dv : nullptr;
+    const cudaError_t le = dcp::launch_mla_decode(p, dtype, (cudaStream_t)stream);
+    if (le == cudaErrorNotSupported)
+        return fail(DCP_ERR_CUDA, "%s: the driver offers no tensor-map encoder (cuTensorMapEncodeTiled)", who);
+    return launched(le, who);
+}
+
+dcp_status_t dcp_device_status(void) {
+    const int s = dcp::mla_device_status(true);
+    if (s < 0) return fail(DCP_ERR_CUDA, "dcp_device_status: the device status word could not be read");
+    if (s) return fail((dcp_status_t)s, "dcp_device_status: a tensor-core kernel gave up on a bounded wait");
+    return ok();
 }
 
 }  // extern "C"

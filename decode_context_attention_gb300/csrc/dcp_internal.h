@@ -82,11 +82,40 @@ struct AttnParams {
     float* ws_lse;                      // [N*B*H*nsplit] partial base-2 LSEs
 };
 
+// Decode attention of every rank over its share of an absorbed-MLA latent
+// cache [N][B][lcap][576] (value = the first 512 elements of each row).
+struct MlaParams {
+    int N, B, H;
+    int64_t lcap;      // local capacity: ceil(max_seq_len / N) tokens per (rank, request)
+    int max_seq_len;
+    int split_tokens;  // local tokens per split (a multiple of 64)
+    int nsplit;
+    int base2;
+    float sm_scale;
+    const unsigned char* q;
+    int64_t q_sb, q_sh;                  // bytes
+    const unsigned char* kv;
+    int64_t kv_sn, kv_sb, kv_st;         // bytes
+    const int* seq_lens;
+    unsigned char* o;
+    int64_t o_sn, o_sb, o_sh;            // bytes
+    float* lse;
+    int64_t l_sn, l_sb, l_sh;            // fp32 words
+    float* ws_o;                         // [N*B*H*nsplit][512] (nsplit > 1)
+    float* ws_lse;                       // [N*B*H*nsplit]
+};
+
 // Records `msg` as this host thread's dcp_last_error_message() and returns s.
 dcp_status_t set_error(dcp_status_t s, const char* msg);
 
 // Launchers return the launch's cudaGetLastError().
 cudaError_t launch_decode_attention(const AttnParams& p, int dtype, cudaStream_t stream);
+// cudaErrorNotSupported when the driver offers no tensor-map encoder.
+cudaError_t launch_mla_decode(const MlaParams& p, int dtype, cudaStream_t stream);
+// The tensor-core kernels' device status word (0, or the status of the first
+// bounded wait that ran out), read synchronously and optionally cleared;
+// -1 when it cannot be read.
+int mla_device_status(bool clear);
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_combine_f32(const CombineParams& p, int vb, cudaStream_t stream);
 cudaError_t launch_combine_f16(const CombineParams& p, int vb, cudaStream_t stream);

@@ -1,0 +1,570 @@
+// dcp_mla_attention.cu -- each DCP rank's decode attention over its share of
+// an absorbed-MLA latent cache, on the 5th-generation tensor cores.
+//
+// sglang PR #33926 report, "功能与动机" and "实现拆解" items 3-4: the
+// trtllm_mla decode path (DeepSeek-V3 class models on Blackwell) returns the
+// rank-local (out, lse) of every rank, the LSE in base 2, and a rank that
+// owns no token of a request is the neutral (0, -inf); token t of a request
+// lives on rank t % N.  sglang PR #34213 report, "功能与动机": for absorbed
+// MLA the output width is kv_lora_rank.
+//
+// Every query head h scores one shared latent row per token,
+//     kv_t [576] = [ c_t (512 = kv_lora_rank) | k_rope_t (64) ],
+// against its absorbed query q_h [576]; the value is the row's first 512
+// elements:  s = sm_scale <q_h, kv_t>,  lse = log sum exp(s),
+//            O_h = sum_t exp(s_t - lse) c_t.
+//
+// Design.  128 query heads x 512 output columns of fp32 accumulators are
+// 256 KB: all of one SM's tensor memory, with no room left for the scores.
+// So a pair of CTAs (a thread-block cluster of 2) takes one (rank, request,
+// split): CTA c owns output columns [256c, 256c + 256) and, for the scores,
+// latent columns [256c, 256c + 256) plus rope columns [512 + 32c, 544 + 32c)
+// -- exactly the columns it loads, so the pair reads every latent byte once
+// and does every multiply-add once.  Per tile of 64 tokens:
+//   * TMA (one thread) loads the CTA's four 64-column latent chunks and the
+//     rope chunk of the 64 tokens, 128-byte swizzled, into a 4-stage ring;
+//   * the MMA thread computes the partial scores S_c [128 heads x 64 tokens]
+//     = Q_c . KV_c^T with tcgen05.mma (Q_c, 288 columns of the absorbed
+//     query, held in tensor memory as the A operand; K-major B from shared
+//     memory), fp32 in tensor memory;
+//   * the softmax warpgroup (thread h = head h = TMEM lane h) reads its row
+//     of S_c, sends it to the peer CTA through distributed shared memory,
+//     adds the peer's half (both CTAs form S_0 + S_1 in the same order, so
+//     both get the same bits), and runs an online softmax in base 2 with a
+//     lazily moved reference max (the output is rescaled only when the max
+//     grows by more than 2^8, so most tiles skip it); P goes to tensor
+//     memory as bf16/fp16;
+//   * the MMA thread accumulates O_c [128 x 256] += P . V_c with P as the
+//     TMEM A operand and V_c read MN-major from the same shared-memory tile.
+// With one split the softmax warps normalise O and write (O_r, lse_r);
+// otherwise fp32 partials go to the workspace and a second kernel merges the
+// splits with the combine's LSE rule.  Every barrier wait is bounded (1 s):
+// a wait that runs out records DCP_ERR_TIMEOUT in a device status word and
+// the kernel winds down (its copies and MMAs in flight are waited for, its
+// tensor memory freed) instead of hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "dcp_device.cuh"
+#include "dcp_sm100.cuh"
+
+namespace dcp {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kMlaThreads = 192;   // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kTileTokens = 64;    // tokens per tile
+constexpr int kStages = 4;         // shared-memory ring depth
+constexpr int kChunkBytes = kTileTokens * 128;      // 64 tokens x 64 columns x 2 bytes
+constexpr int kStageBytes = 5 * kChunkBytes;        // 4 latent chunks + the rope chunk
+constexpr int kXbufBytes = kTileTokens * 128 * 4;   // fp32 partial scores, 64 tokens x 128 heads
+constexpr int kSmemBytes = kStages * kStageBytes + kXbufBytes + 1024 /* barriers */ + 1024 /* alignment */;
+// tensor-memory columns
+constexpr uint32_t kColO = 0;      // O_c: 256 fp32 columns
+constexpr uint32_t kColQ = 256;    // Q_c: 288 16-bit elements = 144 columns
+constexpr uint32_t kColS = 400;    // S_c: 64 fp32 columns
+constexpr uint32_t kColP = 464;    // P: 64 16-bit elements = 32 columns
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.f;  // move the reference max when it would grow by more than this
+constexpr float kLog2eF = 1.4426950408889634f;
+constexpr float kLn2F = 0.6931471805599453f;
+
+enum : int { kStatusTimeout = DCP_ERR_TIMEOUT };
+
+__device__ int g_mla_status;  // first bounded wait that ran out (0 if none)
+
+struct Barriers {
+    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t q_full, s_full, s_free, p_full, pv_done, mma_done, xfull, xempty;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack_pair(float a, float b) {
+    if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map,
+                                                                   const MlaParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    float4* xbuf = reinterpret_cast<float4*>(smem + kStages * kStageBytes);  // [16][128] float4
+    Barriers* bar = reinterpret_cast<Barriers*>(smem + kStages * kStageBytes + kXbufBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t c = cluster_ctarank();  // which half of the columns
+    const int item = (int)(blockIdx.x >> 1);
+    const int split = item % p.nsplit;
+    const int rb = item / p.nsplit;
+    const int b = rb % p.B;
+    const int r = rb / p.B;
+    int L = p.seq_lens[b];
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+    const int Ll = L / p.N + (r < L % p.N ? 1 : 0);
+    const int t0 = split * p.split_tokens;
+    const int t1 = min(t0 + p.split_tokens, Ll);
+    const int ntiles = t1 > t0 ? (t1 - t0 + kTileTokens - 1) / kTileTokens : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bar->kv_full[s], 1);
+            mbar_init(&bar->kv_empty[s], 1);
+        }
+        mbar_init(&bar->q_full, 128);
+        mbar_init(&bar->s_full, 1);
+        mbar_init(&bar->s_free, 4);
+        mbar_init(&bar->p_full, 4);
+        mbar_init(&bar->pv_done, 1);
+        mbar_init(&bar->mma_done, 1);
+        mbar_init(&bar->xfull, 128);
+        mbar_init(&bar->xempty, 128);
+        bar->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&bar->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) tma_prefetch_map(&kv_map);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();  // the peer's barriers are initialised before any remote arrival
+    const uint32_t tmem = bar->tmem_base;
+    volatile int* abort = &bar->abort;
+    int* status = &g_mla_status;
+    bool issued_any = false;  // the MMA thread issued at least one MMA
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % kStages, k = i / kStages;
+                if (k > 0 && !mbar_wait(&bar->kv_empty[st], (k - 1) & 1, status, kStatusTimeout, abort)) break;
+                uint8_t* dst = stages + st * kStageBytes;
+                mbar_arrive_expect_tx(&bar->kv_full[st], kStageBytes);
+                const int y = t0 + i * kTileTokens;
+                for (int j = 0; j < 4; ++j)
+                    tma_load_4d(dst + j * kChunkBytes, &kv_map, &bar->kv_full[st], 256 * (int)c + 64 * j, y, b, r);
+                tma_load_4d(dst + 4 * kChunkBytes, &kv_map, &bar->kv_full[st], 512, y, b, r);
+                issued = i + 1;
+            }
+            // copies still in flight (only after an abort) land before the CTA ends
+            for (int i = max(0, issued - kStages); i < issued; ++i) {
+                uint64_t* fb = &bar->kv_full[i % kStages];
+                const uint32_t par = (i / kStages) & 1;
+                const uint64_t t_start = global_timer_ns();
+                while (!mbar_try_wait(fb, par) && global_timer_ns() - t_start < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr bool kBf16 = !std::is_same<T, __half>::value;
+            const uint32_t idesc_qk = idesc_f16(128, kTileTokens, kBf16, 0, 0);
+            const uint32_t idesc_pv = idesc_f16(128, 256, kBf16, 0, 1);
+            const uint32_t tS = tmem + kColS, tQ = tmem + kColQ, tO = tmem + kColO, tP = tmem + kColP;
+            auto issue_pv = [&](int j) -> bool {
+                if (!mbar_wait(&bar->p_full, j & 1, status, kStatusTimeout, abort)) return false;
+                tc_fence_after();
+                const uint32_t base = smem_u32(stages + (j % kStages) * kStageBytes);
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tO, tP + 8 * s, smem_desc(base + 2048 * s, kChunkBytes, 1024, kSwizzle128B), idesc_pv,
+                           (j > 0 || s > 0) ? 1u : 0u);
+                mma_commit(&bar->pv_done);
+                mma_commit(&bar->kv_empty[j % kStages]);
+                return true;
+            };
+            bool ok = mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int st = i % kStages;
+                if (!mbar_wait(&bar->kv_full[st], (i / kStages) & 1, status, kStatusTimeout, abort)) break;
+                if (i > 0 && !mbar_wait(&bar->s_free, (i - 1) & 1, status, kStatusTimeout, abort)) break;
+                tc_fence_after();
+                const uint32_t base = smem_u32(stages + st * kStageBytes);
+                // latent columns: 4 chunks x 4 steps of 16
+                for (int s = 0; s < 16; ++s)
+                    mma_ts(tS, tQ + 8 * s,
+                           smem_desc(base + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B),
+                           idesc_qk, s > 0 ? 1u : 0u);
+                // this CTA's 32 rope columns: the [64c, 64c + 64) bytes of each rope row
+                for (int s = 0; s < 2; ++s)
+                    mma_ts(tS, tQ + 8 * (16 + s),
+                           smem_desc(base + 4 * kChunkBytes + 64 * c + 32 * s, 16, 1024, kSwizzle128B), idesc_qk,
+                           1u);
+                mma_commit(&bar->s_full);
+                issued_any = true;
+                if (i > 0 && !issue_pv(i - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok && ntiles > 0 && !*abort) issue_pv(ntiles - 1);
+            if (issued_any) mma_commit(&bar->mma_done);
+        }
+    } else {
+        // -------------------------------------------------- softmax warpgroup
+        const int h = tid;  // head = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        // Q_c into tensor memory: latent columns [256c, 256c + 256) then rope
+        // columns [512 + 32c, 544 + 32c), as 144 32-bit pairs
+        {
+            const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (int64_t)b * p.q_sb + (int64_t)h * p.q_sh);
+            const bool live = h < p.H;
+#pragma unroll
+            for (int g = 0; g < 9; ++g) {
+                uint32_t w[16];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int vec = 4 * g + v;  // 16-byte vector of the 36 this thread loads
+                    const int col = vec < 32 ? 256 * (int)c + 8 * vec : 512 + 32 * (int)c + 8 * (vec - 32);
+                    const uint4 x = live ? __ldg(qrow + col / 8) : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * v] = x.x;
+                    w[4 * v + 1] = x.y;
+                    w[4 * v + 2] = x.z;
+                    w[4 * v + 3] = x.w;
+                }
+                tmem_st16(tmem + kColQ + lane_off + 16 * g, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar->q_full);
+        }
+        const uint32_t peer = c ^ 1u;
+        const uint32_t peer_xbuf = map_to_cta(xbuf, peer);
+        const uint32_t peer_xfull = map_to_cta(&bar->xfull, peer);
+        const uint32_t peer_xempty = map_to_cta(&bar->xempty, peer);
+        const float scale2 = p.sm_scale * kLog2eF;
+        float m_used = -INFINITY, l = 0.f;
+        // tcgen05.ld / st are warp-collective: every wait's outcome is made
+        // warp-uniform so that the lanes of a warp leave the loop together
+        const unsigned kAll = 0xffffffffu;
+        bool ok = true;
+        for (int i = 0; i < ntiles && ok; ++i) {
+            if (!__all_sync(kAll, mbar_wait(&bar->s_full, i & 1, status, kStatusTimeout, abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[kTileTokens];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t u[16];
+                tmem_ld16(tmem + kColS + lane_off + 16 * k, u);
+                tmem_wait_ld();
+                pin(u);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) s[16 * k + j] = __uint_as_float(u[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->s_free);
+            // exchange the partial scores with the peer CTA
+            if (i > 0 && !__all_sync(kAll, mbar_wait<true>(&bar->xempty, (i - 1) & 1, status, kStatusTimeout, abort))) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                st_cluster_v4(peer_xbuf + (uint32_t)((k * 128 + h) * 16),
+                              make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]));
+            mbar_arrive_remote(peer_xfull);
+            if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull, i & 1, status, kStatusTimeout, abort))) {
+                ok = false;
+                break;
+            }
+            const int valid = t1 - (t0 + i * kTileTokens);
+            float mt = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float4 o4 = xbuf[k * 128 + h];
+                const float other[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = 4 * k + j;
+                    // S_0 + S_1 in that order in both CTAs: the same bits on both sides
+                    const float x = (c == 0 ? s[t] + other[j] : other[j] + s[t]) * scale2;
+                    s[t] = t < valid ? x : -INFINITY;
+                    mt = fmaxf(mt, s[t]);
+                }
+            }
+            __syncwarp();
+            mbar_arrive_remote(peer_xempty);
+            const float m_new = fmaxf(m_used, mt);
+            const bool move = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
+            // P and O are free once the previous tile's P.V has completed
+            if (i > 0 && !__all_sync(kAll, mbar_wait(&bar->pv_done, (i - 1) & 1, status, kStatusTimeout, abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (valid < kTileTokens) {
+                // rows past the split's last token were loaded from the cache
+                // as they are (stale values, possibly NaN): zero their value
+                // columns so that 0-probability rows add exactly 0
+                uint8_t* stage = stages + (i % kStages) * kStageBytes;
+                const int rows = kTileTokens - valid;
+                for (int e = h; e < 4 * rows * 8; e += 128) {
+                    const int chunk = e / (rows * 8), rem = e % (rows * 8);
+                    const int row = valid + rem / 8, v16 = rem % 8;
+                    *reinterpret_cast<uint4*>(stage + chunk * kChunkBytes + row * 128 + v16 * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            float alpha = 1.f;
+            if (move) {
+                alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - m_new);
+                l *= alpha;
+                m_used = m_new;
+            }
+            if (i > 0 && __any_sync(kAll, move)) {
+                // rescale this warp's rows of O (alpha = 1 for rows that keep their max)
+                for (int k = 0; k < 16; ++k) {
+                    uint32_t u[16];
+                    tmem_ld16(tmem + kColO + lane_off + 16 * k, u);
+                    tmem_wait_ld();
+                    pin(u);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
+                    tmem_st16(tmem + kColO + lane_off + 16 * k, u);
+                }
+            }
+            // P = 2^(s - m) in the payload type; the row sum in fp32 (a row
+            // whose scores so far are all -inf has m = -inf and p = 0)
+            const float msub = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float pa = exp2f(s[32 * k + 2 * j] - msub);
+                    const float pb = exp2f(s[32 * k + 2 * j + 1] - msub);
+                    l += pa + pb;
+                    w[j] = pack_pair<T>(pa, pb);
+                }
+                tmem_st16(tmem + kColP + lane_off + 16 * k, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->p_full);
+        }
+        if (ok && ntiles > 0) ok = __all_sync(kAll, mbar_wait(&bar->pv_done, (ntiles - 1) & 1, status, kStatusTimeout, abort));
+        tc_fence_after();
+        // ----------------------------------------------------------- epilogue
+        // `have` is warp-uniform (it decides the warp-collective loads of O);
+        // a row with no probability mass (l = 0) still reads O but writes 0
+        const bool have = ok && ntiles > 0;
+        const bool mass = have && l > 0.f;
+        const float inv = mass ? 1.f / l : 0.f;
+        const float lse2 = mass ? m_used + log2f(l) : -INFINITY;
+        const bool live = h < p.H;
+        if (p.nsplit == 1) {
+            unsigned char* orow = p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + 512 * c;
+            for (int k = 0; k < 16; ++k) {
+                uint32_t u[16];
+                if (have) {
+                    tmem_ld16(tmem + kColO + lane_off + 16 * k, u);
+                    tmem_wait_ld();
+                    pin(u);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) u[j] = 0u;
+                }
+                uint32_t w[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    w[j] = pack_pair<T>(__uint_as_float(u[2 * j]) * inv, __uint_as_float(u[2 * j + 1]) * inv);
+                if (live) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+            if (live && c == 0)
+                p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] = p.base2 ? lse2 : lse2 * kLn2F;
+        } else {
+            const int64_t row = (((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split;
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + row * 512 + 256 * c);
+            for (int k = 0; k < 16; ++k) {
+                uint32_t u[16];
+                if (have) {
+                    tmem_ld16(tmem + kColO + lane_off + 16 * k, u);
+                    tmem_wait_ld();
+                    pin(u);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) u[j] = 0u;
+                }
+                if (live) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[4 * k + j] = make_float4(__uint_as_float(u[4 * j]) * inv, __uint_as_float(u[4 * j + 1]) * inv,
+                                                     __uint_as_float(u[4 * j + 2]) * inv,
+                                                     __uint_as_float(u[4 * j + 3]) * inv);
+                }
+            }
+            if (live && c == 0) p.ws_lse[row] = lse2;
+        }
+    }
+
+    // --------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        if (lane == 0 && issued_any) {
+            // every MMA this CTA issued has completed before its tensor memory goes
+            const uint64_t t_start = global_timer_ns();
+            while (!mbar_try_wait(&bar->mma_done, 0) && global_timer_ns() - t_start < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    cluster_sync();  // no CTA leaves while its peer may still write its shared memory
+}
+
+// Merge of the split partials (fp32, normalised, base-2 LSE) of every
+// (rank, request, head): one warp per row, with the combine's LSE rule
+// (empty splits are (0, -inf) and drop out).
+template <typename T>
+__global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)p.N * p.B * p.H;
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int S = p.nsplit;
+    const float* lrow = p.ws_lse + row * S;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, lrow[s]);
+    float Ls = 0.f;
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+        for (int s = 0; s < S; ++s) {
+            const float w = exp2f(lrow[s] - M);
+            Ls += w;
+            const float4* orow = reinterpret_cast<const float4*>(p.ws_o + (row * S + s) * 512);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = orow[lane + 32 * k];
+                acc[k].x = fmaf(w, v.x, acc[k].x);
+                acc[k].y = fmaf(w, v.y, acc[k].y);
+                acc[k].z = fmaf(w, v.z, acc[k].z);
+                acc[k].w = fmaf(w, v.w, acc[k].w);
+            }
+        }
+    }
+    const int h = (int)(row % p.H);
+    const int64_t rbq = row / p.H;
+    const int b = (int)(rbq % p.B);
+    const int r = (int)(rbq / p.B);
+    unsigned char* orow = p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh;
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint2 w = make_uint2(pack_pair<T>(acc[k].x * inv, acc[k].y * inv), pack_pair<T>(acc[k].z * inv, acc[k].w * inv));
+        *reinterpret_cast<uint2*>(orow + 8 * (lane + 32 * k)) = w;
+    }
+    if (lane == 0) {
+        const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
+        p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] = p.base2 ? lse2 : lse2 * kLn2F;
+    }
+}
+
+// cuTensorMapEncodeTiled, looked up from the driver once (no link-time
+// dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return g_encode;
+}
+
+template <typename T>
+cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, cudaStream_t stream) {
+    // the shared-memory opt-in is a per-device function attribute
+    const cudaError_t attr_err =
+        cudaFuncSetAttribute((const void*)mla_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * (int64_t)p.N * p.B * p.nsplit));
+    cfg.blockDim = dim3(kMlaThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<T>, map, p);
+    if (e != cudaSuccess || p.nsplit == 1) return e;
+    const int64_t rows = (int64_t)p.N * p.B * p.H;
+    mla_merge_splits_kernel<T><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mla_decode(const MlaParams& p, int dtype, cudaStream_t stream) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    // the latent cache as a 4-D tensor [N][B][Lc][576] (elements, then byte strides)
+    CUtensorMap map;
+    const cuuint64_t dims[4] = {576, (cuuint64_t)(p.lcap > 0 ? p.lcap : 1), (cuuint64_t)p.B, (cuuint64_t)p.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)p.kv_st, (cuuint64_t)p.kv_sb, (cuuint64_t)p.kv_sn};
+    const cuuint32_t box[4] = {64, kTileTokens, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult rc = enc(&map, dtype == DCP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            4, const_cast<unsigned char*>(p.kv), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rc != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    return dtype == DCP_F16 ? launch_mla_t<__half>(p, map, stream) : launch_mla_t<__nv_bfloat16>(p, map, stream);
+}
+
+int mla_device_status(bool clear) {
+    int s = 0;
+    if (cudaMemcpyFromSymbol(&s, g_mla_status, sizeof(int)) != cudaSuccess) return -1;
+    if (clear && s) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_mla_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return s;
+}
+
+}  // namespace dcp

@@ -38,6 +38,13 @@ cached-extend cases; no model weights or datasets are involved):
                  i*N + r), values ~ N(0,1); queries ~ N(0,1).
   gqa_decode_attention  the same with grouped-query heads: 32 query heads
                  over 4 KV heads (8 per KV head), seed 7.
+  mla_decode_attention  the attention whose partials the MLA decode merge
+                 takes (DeepSeek-V3-like absorbed MLA): N=8 ranks, B=128
+                 requests, H=128 query heads over one latent row per token of
+                 576 = 512 (kv_lora_rank, the value) + 64 (rope) bf16
+                 elements, base-2 LSE, request lengths ~ U(1, 16384), latent
+                 rows and absorbed queries ~ N(0,1), sm_scale = 1/sqrt(192)
+                 (the no-rope plus rope query width of that model), seed 8.
 
 An empty (rank, token) pair is the pages' neutral state for a rank that owns
 no KV slice of that request: O = 0, LSE = -inf (sglang PR #33926 report,
@@ -202,3 +209,27 @@ def generate_attention(name="mha_decode_attention", device="cuda", seed=None, **
         v[r].normal_(generator=g)
     seq = torch.randint(1, L + 1, (B,), generator=g, device=device, dtype=torch.int64).to(torch.int32)
     return {"q": q, "k": k, "v": v, "seq_lens": seq, "max_len": L, "cfg": c}
+
+
+MLA_ATTENTION = {"mla_decode_attention": dict(N=8, B=128, H=128, Dk=576, Dv=512, dtype="bf16", max_len=16384,
+                                              base="2", seed=8, sm_scale=192 ** -0.5)}
+
+
+def generate_mla_attention(name="mla_decode_attention", device="cuda", seed=None, **override) -> dict:
+    """Draw an absorbed-MLA decode workload: q [B,H,Dk], each rank's latent
+    cache kv [N,B,Lc,Dk] (Lc = ceil(max_len / N); local token i of rank r is
+    global token i*N + r; entries past a rank's local length are never
+    used), seq_lens [B] int32 global lengths in [1, max_len]."""
+    c = dict(MLA_ATTENTION[name], **override)
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(c["seed"] if seed is None else seed)
+    N, B, H, Dk, L = c["N"], c["B"], c["H"], c["Dk"], c["max_len"]
+    dt = TORCH_DTYPES[c["dtype"]]
+    lc = (L + N - 1) // N
+    q = torch.empty((B, H, Dk), dtype=dt, device=device).normal_(generator=g)
+    kv = torch.empty((N, B, lc, Dk), dtype=dt, device=device)
+    for r in range(N):
+        kv[r].normal_(generator=g)
+    seq = torch.randint(1, L + 1, (B,), generator=g, device=device, dtype=torch.int64).to(torch.int32)
+    return {"q": q, "kv": kv, "seq_lens": seq, "max_len": L, "cfg": c}

@@ -13,7 +13,9 @@
  *   dcp_unpack_combine  the combine reading interleaved [payload | LSE word]
  *                       receive rows in one pass;
  *   dcp_decode_attention  the step before the merge: each rank's decode
- *                       attention over its round-robin share of the KV cache.
+ *                       attention over its round-robin share of the KV cache
+ *                       (dcp_decode_attention_mla: over an absorbed-MLA
+ *                       latent cache, on the tcgen05 tensor cores).
  *
  * The cross-rank exchange itself (NCCL all-to-all, MNNVL, all-gather /
  * all-reduce) is not part of this library.  A group's N ranks can be held as
@@ -81,7 +83,8 @@ typedef enum dcp_status {
     DCP_ERR_MISALIGNED = 4,           /* D % lpd != 0, a pointer/stride not aligned to its type,
                                          or fp8 rows not on 4-byte boundaries */
     DCP_ERR_ALIAS = 5,                /* an output overlaps an input or itself */
-    DCP_ERR_CUDA = 6                  /* a CUDA call failed; see dcp_last_error_message() */
+    DCP_ERR_CUDA = 6,                 /* a CUDA call failed; see dcp_last_error_message() */
+    DCP_ERR_TIMEOUT = 7               /* a kernel gave up on a bounded wait (dcp_device_status) */
 } dcp_status_t;
 
 enum { DCP_F32 = 0, DCP_F16 = 1, DCP_BF16 = 2, DCP_FP8_E4M3 = 3 };
@@ -335,6 +338,61 @@ dcp_status_t dcp_decode_attention_noalloc(int dtype, int N, int B, int H, int Hk
                                           void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
                                           float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
                                           int lse_base, void* stream);
+
+/*
+ * dcp_decode_attention_mla -- each DCP rank's single-token decode attention
+ * over the tokens it owns of an absorbed-MLA latent cache (DeepSeek-V3
+ * class: every query head scores one shared latent row per token).
+ * (sglang PR #33926 report, "功能与动机" and "实现拆解" items 3-4: the
+ * trtllm_mla decode path returns rank-local (out, lse), the LSE in base 2; a
+ * rank owning no token of a request is the neutral (0, -inf); token t lives
+ * on rank t % N.  sglang PR #34213 report, "功能与动机": for absorbed MLA the
+ * output width is kv_lora_rank.)
+ *
+ * For rank r < N, request b < B, query head h < H, over the rank's local
+ * tokens i < L_r(b) = L_b / N + (r < L_b % N), L_b = min(seq_lens[b],
+ * max_seq_len), with s_i = sm_scale <q[b, h, 0:Dk], kv[r][b, i, 0:Dk]>:
+ *     lse[r, b, h] = log sum_i exp(s_i)        (base e, or divided by ln 2)
+ *     o  [r, b, h] = sum_i exp(s_i - lse) kv[r][b, i, 0:Dv]
+ * (0 and -inf when L_r(b) = 0): the value is the first Dv elements of each
+ * latent row, the score uses all Dk (kv_lora_rank, then the rope part).
+ *
+ *   q        [B, H, Dk]       absorbed queries (no-rope part, then rope part),
+ *                             strides (q_sb, q_sh)
+ *   kv       [N][B, Lc, Dk]   each rank's latent cache, Lc = ceil(max_seq_len
+ *                             / N); strides (kv_sn, kv_sb, kv_st)
+ *   seq_lens [B] int32 (device) global lengths
+ *   o        [N, B, H, Dv]    strides (o_sn, o_sb, o_sh)
+ *   lse      [N, B, H]        fp32, strides (l_sn, l_sb, l_sh)
+ *
+ * Supported: dtype DCP_BF16 or DCP_F16 (q, kv and o); Dk = 576 and Dv = 512;
+ * 1 <= H <= 128; split_tokens a positive multiple of 64.  q and o rows start
+ * on 16-byte boundaries; kv is 16-byte aligned with strides that are
+ * positive multiples of 8 elements (kv_st >= Dk).  Probabilities enter the
+ * value product rounded to the payload type (an 8- or 11-bit significand);
+ * scores, sums and outputs accumulate in fp32.  Workspace as for
+ * dcp_decode_attention, sized dcp_decode_attention_workspace_size(N, B, H,
+ * Dv, max_seq_len, split_tokens).  Errors as for dcp_decode_attention; the
+ * kernel's waits are bounded, and one that runs out is reported by
+ * dcp_device_status().  Needs a GPU of compute capability 10.x with
+ * tensor-map support in its driver (DCP_ERR_CUDA otherwise).
+ */
+dcp_status_t dcp_decode_attention_mla(int dtype, int N, int B, int H, int Dk, int Dv,
+                                      const void* q, int64_t q_sb, int64_t q_sh,
+                                      const void* kv, int64_t kv_sn, int64_t kv_sb, int64_t kv_st,
+                                      const int* seq_lens, int max_seq_len, float sm_scale, int split_tokens,
+                                      void* o, int64_t o_sn, int64_t o_sb, int64_t o_sh,
+                                      float* lse, int64_t l_sn, int64_t l_sb, int64_t l_sh,
+                                      int lse_base, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dcp_device_status -- DCP_OK, or DCP_ERR_TIMEOUT when a tensor-core kernel
+ * launched on the current device since the last call gave up on one of its
+ * bounded waits (1 s each; its outputs are then invalid).  Synchronises with
+ * the device (it reads a device status word), then clears the status.  The
+ * merge kernels never wait and never set it.
+ */
+dcp_status_t dcp_device_status(void);
 
 #ifdef __cplusplus
 }  /* extern "C" */

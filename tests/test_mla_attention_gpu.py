@@ -1,0 +1,232 @@
+"""Absorbed-MLA decode attention on the tensor cores against the fp64 oracle.
+
+Every rank's partial (O_r, lse_r) from dcp_decode_attention_mla is compared,
+element by element, with oracle.split_attention_mla on the same seeded
+inputs: small cases on every row (ragged tails, ranks owning nothing, one
+split and many, both LSE bases, bf16 and fp16, fewer than 128 heads, strided
+operands), the full-size workload on sampled rows, and the whole one-GPU DCP
+decode of the MLA merge's shape (attention -> peer-inside pack -> combine)
+against unsplit attention.
+
+Tolerance, from the arithmetic (not fitted): the kernel rounds every
+probability once to the payload type before the value product (relative
+error <= u, u = 2^-9 for bf16, 2^-12 for fp16), normalises by the fp32 sum
+of the unrounded probabilities, and rounds the output once (<= u relative).
+So |O - O*|_d <= u sum_t w_t |v_td| + u |O*_d| + the effect of score errors.
+The scores are fp32 sums of 576 products: |ds_t| <= 576 * 2^-24 *
+sum_i |q_i kv_ti| * sm_scale =: E (natural-log units), which moves lse by at
+most E and every weight by a factor within exp(+-2E).  The bounds below take
+twice each term.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_context_attention_gb300 import binding, build, layouts
+from decode_context_attention_gb300.workloads import generate_mla_attention
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+DK, DV = 576, 512
+U = {torch.bfloat16: 2.0 ** -9, torch.float16: 2.0 ** -12}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    return binding.load()
+
+
+def global_rows(kv, b, L, N):
+    """The request's latent rows in global token order: token t = rank t % N, slot t // N."""
+    idx = torch.arange(L, device=kv.device)
+    return kv[idx % N, b, idx // N].double().cpu().numpy()
+
+
+def check_row(got_o, got_lse, q, rows_global, r, N, scale, base, u, what, want=None):
+    """One (rank, request, head): the kernel's (O, lse) against the oracle
+    (`want` = the oracle's (O [N, Dv], lse [N]) for this request and head)."""
+    if want is None:
+        want = oracle.split_attention_mla(q, rows_global, DV, N, scale, base=base)
+    want_o, want_lse = want[0][r], want[1][r]
+    if want_lse == -np.inf:
+        assert got_lse == -np.inf, f"{what}: empty rank must give lse = -inf, got {got_lse}"
+        assert np.all(got_o == 0.0), f"{what}: empty rank must give O = 0"
+        return 0.0
+    conv = math.log(2.0) if base == "2" else 1.0
+    own = rows_global[r::N]
+    s = own @ q * scale                                     # natural-log units
+    E = DK * 2.0 ** -24 * float((np.abs(own) @ np.abs(q)).max()) * scale
+    w = np.exp(s - want_lse * conv)
+    A = w @ np.abs(own[:, :DV])
+    tol_o = 2 * (u * A + u * np.abs(want_o) + 2 * E * A) + 1e-6
+    err = np.abs(got_o - want_o)
+    assert np.all(err <= tol_o), (f"{what}: O error {err.max():.3e} above its bound at "
+                                  f"d={int(np.argmax(err - tol_o))}")
+    tol_l = 2 * (E + 1e-6 * abs(want_lse * conv)) / conv + 1e-6
+    assert abs(got_lse - want_lse) <= tol_l, f"{what}: lse {got_lse} vs {want_lse} (bound {tol_l:.2e})"
+    return float((err / (np.abs(want_o) + 1e-3)).max())
+
+
+def run(q, kv, seq, max_len, scale, base, split, o=None, lse=None):
+    B, H, _ = q.shape
+    N = kv.shape[0]
+    if o is None:
+        o = torch.full((N, B, H, DV), float("nan"), dtype=q.dtype, device=DEV)
+    if lse is None:
+        lse = torch.full((N, B, H), float("nan"), dtype=torch.float32, device=DEV)
+    need = binding.workspace_bytes(N, B, H, DV, max_len, split)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=DEV) if need else None
+    binding.decode_attention_mla(q, kv, seq, max_len, o, lse, scale, base=base, split_tokens=split, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0, "a bounded wait ran out"
+    return o, lse
+
+
+def draw(N, B, H, lens, max_len, dtype, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    lc = (max_len + N - 1) // N
+    q = torch.randn((B, H, DK), generator=g, device=DEV).to(dtype)
+    kv = torch.randn((N, B, lc, DK), generator=g, device=DEV).to(dtype)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    return q, kv, seq
+
+
+CASES = [
+    # N, H, lengths, max_len, split, dtype, base
+    (2, 128, [700, 1, 130], 700, 128, torch.bfloat16, "2"),     # ragged tails, several splits
+    (2, 128, [700, 1, 130], 700, 1024, torch.bfloat16, "e"),    # one split per rank
+    (8, 128, [5, 64 * 8, 64 * 8 + 3, 1000], 1000, 64, torch.bfloat16, "2"),  # ranks with no token
+    (4, 16, [300, 257], 300, 64, torch.float16, "e"),           # fewer heads, fp16
+    (1, 128, [129, 64], 129, 1024, torch.float16, "2"),         # one rank: the whole sequence
+    (3, 96, [0, 200, 1], 200, 64, torch.bfloat16, "e"),         # an empty request
+]
+
+
+@pytest.mark.parametrize("N,H,lens,max_len,split,dtype,base", CASES)
+def test_mla_rank_partials_match_oracle_on_every_row(N, H, lens, max_len, split, dtype, base):
+    B = len(lens)
+    q, kv, seq = draw(N, B, H, lens, max_len, dtype, seed=N * 100 + H + split)
+    scale = 192 ** -0.5
+    o, lse = run(q, kv, seq, max_len, scale, base, split)
+    qn = q.double().cpu().numpy()
+    on = o.double().cpu().numpy()
+    ln = lse.double().cpu().numpy()
+    for b, L in enumerate(lens):
+        rows = global_rows(kv, b, L, N)
+        for h in range(H):
+            want = oracle.split_attention_mla(qn[b, h], rows, DV, N, scale, base=base)
+            for r in range(N):
+                check_row(on[r, b, h], ln[r, b, h], qn[b, h], rows, r, N, scale, base, U[dtype],
+                          f"N={N} b={b} r={r} h={h}", want)
+
+
+def test_mla_stale_cache_rows_do_not_leak_into_the_result():
+    # rows past a rank's local length hold whatever the cache had there (here
+    # NaN and huge values): the tail tile loads them, and they must add
+    # exactly nothing
+    N, B, H, max_len = 2, 2, 128, 1000
+    lens = [333, 77]
+    q, kv, seq = draw(N, B, H, lens, max_len, torch.bfloat16, seed=31)
+    clean_o, clean_lse = run(q, kv, seq, max_len, 0.07, "2", 1024)
+    dirty = kv.clone()
+    for r in range(N):
+        for b, L in enumerate(lens):
+            n_loc = L // N + (1 if r < L % N else 0)
+            dirty[r, b, n_loc:, ::2] = float("nan")
+            dirty[r, b, n_loc:, 1::2] = 3e38
+    o, lse = run(q, dirty, seq, max_len, 0.07, "2", 1024)
+    assert torch.equal(o.view(torch.int16), clean_o.view(torch.int16))
+    assert torch.equal(lse, clean_lse)
+
+
+def test_mla_strided_operands_give_the_contiguous_bits():
+    # q sliced out of a wider projection, the cache rows padded to 640
+    # elements, O rows padded and the LSE a strided slot
+    N, B, H, max_len = 2, 3, 128, 400
+    lens = [400, 129, 64]
+    q, kv, seq = draw(N, B, H, lens, max_len, torch.bfloat16, seed=41)
+    want_o, want_lse = run(q, kv, seq, max_len, 0.08, "e", 128)
+    qw = torch.zeros((B, H, DK + 64), dtype=q.dtype, device=DEV)
+    qw[..., 32:32 + DK] = q
+    lc = kv.shape[2]
+    kvw = torch.zeros((N, B, lc, 640), dtype=kv.dtype, device=DEV)
+    kvw[..., :DK] = kv
+    ow = torch.full((N, B, H, DV + 8), float("nan"), dtype=q.dtype, device=DEV)
+    lw = torch.full((N, B, H, 2), float("nan"), dtype=torch.float32, device=DEV)
+    o, lse = run(qw[..., 32:32 + DK], kvw[..., :DK], seq, max_len, 0.08, "e", 128, ow[..., :DV], lw[..., 0])
+    assert torch.equal(o.view(torch.int16), want_o.view(torch.int16))
+    assert torch.equal(lse, want_lse)
+    assert torch.isnan(ow[..., DV:]).all() and torch.isnan(lw[..., 1]).all()
+
+
+def test_mla_full_size_workload_sampled_rows():
+    a = generate_mla_attention("mla_decode_attention", device=DEV)
+    c = a["cfg"]
+    N, B, H = c["N"], c["B"], c["H"]
+    q, kv, seq, L = a["q"], a["kv"], a["seq_lens"], a["max_len"]
+    o, lse = run(q, kv, seq, L, c["sm_scale"], c["base"], 1024)
+    assert torch.isfinite(o.float()).all() and not torch.isnan(lse).any()
+    lens = seq.cpu().tolist()
+    rng = np.random.default_rng(0)
+    qn = q.double().cpu().numpy()
+    for _ in range(24):
+        b, h, r = int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N))
+        rows = global_rows(kv, b, lens[b], N)
+        check_row(o[r, b, h].double().cpu().numpy(), float(lse[r, b, h]), qn[b, h], rows, r, N,
+                  c["sm_scale"], c["base"], U[q.dtype], f"full size b={b} r={r} h={h}")
+
+
+def test_whole_mla_dcp_decode_equals_unsplit_attention():
+    """The one-GPU DCP decode at the MLA merge's shape (N=8 ranks, 128
+    requests, 128 heads, 512 output columns, base-2 LSE): each rank's
+    tensor-core attention, the peer-inside pack, the exchange as a view and
+    the combine give unsplit latent attention over the whole sequence."""
+    a = generate_mla_attention("mla_decode_attention", device=DEV, max_len=520)
+    c = a["cfg"]
+    N, B, H = c["N"], c["B"], c["H"]
+    q, kv, seq, L = a["q"], a["kv"], a["seq_lens"], a["max_len"]
+    o, lse = run(q, kv, seq, L, c["sm_scale"], c["base"], 64)
+    H_pr = H // N
+    partial_o, stats = layouts.alloc_peer_inside(N, B, H_pr, N, DV, o.dtype, DEV)
+    dst_o, dst_lse = layouts.peer_inside_send_views(partial_o, stats)
+    binding.pack_send(o, lse, dst_o, dst_lse)
+    ro, rl = layouts.exchange_peer_inside(partial_o, stats)
+    out = torch.empty((N, B, H_pr, DV), dtype=o.dtype, device=DEV)
+    out_lse = torch.empty((N, B, H_pr), dtype=torch.float32, device=DEV)
+    binding.lse_combine(ro, rl, out, out_lse, base=c["base"])
+    torch.cuda.synchronize()
+    lens = seq.cpu().tolist()
+    qn = q.double().cpu().numpy()
+    rng = np.random.default_rng(1)
+    for _ in range(48):
+        b, h = int(rng.integers(B)), int(rng.integers(H))
+        rows = global_rows(kv, b, lens[b], N)
+        want_o, want_lse = oracle.split_attention_mla(qn[b, h], rows, DV, 1, c["sm_scale"], base=c["base"])
+        got = out[h // H_pr, b, h % H_pr].double().cpu().numpy()
+        s = rows @ qn[b, h] * c["sm_scale"]
+        w = np.exp(s - want_lse[0] * math.log(2.0))
+        A = w @ np.abs(rows[:, :DV])
+        # the attention's bound, plus one more bf16 rounding of the merged row
+        tol = 3 * U[o.dtype] * (A + np.abs(want_o[0])) + 1e-5
+        assert np.all(np.abs(got - want_o[0]) <= tol), f"b={b} h={h}: {np.abs(got - want_o[0]).max():.3e}"
+        assert abs(float(out_lse[h // H_pr, b, h % H_pr]) - want_lse[0]) <= 1e-3
+
+
+def test_mla_refuses_shapes_it_does_not_compile():
+    q, kv, seq = draw(2, 1, 8, [10], 10, torch.bfloat16, seed=3)
+    o = torch.empty((2, 1, 8, DV), dtype=q.dtype, device=DEV)
+    lse = torch.empty((2, 1, 8), dtype=torch.float32, device=DEV)
+    with pytest.raises(binding.DcpError, match="split_tokens"):
+        binding.decode_attention_mla(q, kv, seq, 10, o, lse, 0.1, split_tokens=100)
+    with pytest.raises(binding.DcpError, match="Dk"):
+        binding.decode_attention_mla(q[..., :512], kv[..., :512], seq, 10, o, lse, 0.1)
+    q3, kv3, seq3 = draw(2, 1, 130, [10], 10, torch.bfloat16, seed=4)
+    o3 = torch.empty((2, 1, 130, DV), dtype=q.dtype, device=DEV)
+    l3 = torch.empty((2, 1, 130), dtype=torch.float32, device=DEV)
+    with pytest.raises(binding.DcpError, match="128"):
+        binding.decode_attention_mla(q3, kv3, seq3, 10, o3, l3, 0.1)
