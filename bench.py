@@ -23,6 +23,9 @@ Also measured in the same run and reported under "secondary":
     (lpd = 4) and the fused unpack+combine;
   * the decode attention that produces the merge's inputs (N = 4 ranks,
     B = 64 requests, H = 32, D = 128, bf16, lengths up to 16384; ~9 GB of K/V);
+  * the absorbed-MLA decode attention whose outputs the headline merge takes
+    (N = 8, B = 128, H = 128, 576-wide latent rows, 512-wide values, bf16, on
+    the tcgen05 tensor cores), in TFLOP/s and GB/s;
   * the cached-extend workload (N = 8, 16384 tokens, 96 heads, D = 512, fp32;
     29 GB per call): the combine writing the per-rank head slices
     contiguously, then the in-place sanitising combine.
@@ -294,6 +297,18 @@ def theoretical_hbm_gbs(gpu_index: int):
         return None
 
 
+def load_tensor_peak():
+    """Dense bf16 tensor throughput (TFLOP/s) for a kernel timed on its own:
+    the burst figure of MEASURED_PEAKS.json, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+    return 1900.0, "fallback"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -458,6 +473,41 @@ def setup_decode_attention(device, split_tokens=1024, batch=None, name="mha_deco
             "names": [f"dcp_decode_attention{'_paged' if page_size else ''} (N={N} B={B} H={H} Hkv={Hkv} "
                       f"D={D} bf16, {tokens} KV tokens, splits of {split_tokens}"
                       f"{f', {page_size}-token pages' if page_size else ''})"],
+            "bytes": [algo]}
+
+
+def setup_mla_attention(device, split_tokens=1024, batch=None, max_len=None):
+    """Each rank's absorbed-MLA decode attention (the step whose outputs the
+    MLA decode merge takes), on the tensor cores."""
+    import torch
+
+    from decode_context_attention_gb300 import binding
+    from decode_context_attention_gb300.workloads import generate_mla_attention
+
+    over = {}
+    if batch:
+        over["B"] = batch
+    if max_len:
+        over["max_len"] = max_len
+    a = generate_mla_attention("mla_decode_attention", device=device, **over)
+    c = a["cfg"]
+    N, B, H, Dk, Dv = c["N"], c["B"], c["H"], c["Dk"], c["Dv"]
+    o = torch.empty((N, B, H, Dv), dtype=a["q"].dtype, device=device)
+    lse = torch.empty((N, B, H), dtype=torch.float32, device=device)
+    nbytes = binding.workspace_bytes(N, B, H, Dv, a["max_len"], split_tokens)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
+    call = binding.prepare_decode_attention_mla(a["q"], a["kv"], a["seq_lens"], a["max_len"], o, lse,
+                                                c["sm_scale"], base=c["base"], split_tokens=split_tokens,
+                                                workspace=ws)
+    tokens = int(a["seq_lens"].sum().item())
+    e = a["q"].element_size()
+    # every owned latent row once, each rank's read of q, O and LSE written
+    algo = tokens * Dk * e + N * B * H * Dk * e + N * B * H * Dv * e + N * B * H * 4
+    flops = 2 * tokens * H * (Dk + Dv)  # scores over Dk, value product over Dv, every head
+    return {"launches": [call], "keep": (a, o, lse, ws), "tokens": tokens, "workspace_bytes": nbytes,
+            "flops": flops,
+            "names": [f"dcp_decode_attention_mla (N={N} B={B} H={H} Dk={Dk} Dv={Dv} bf16, {tokens} latent "
+                      f"rows, splits of {split_tokens})"],
             "bytes": [algo]}
 
 
@@ -681,6 +731,38 @@ def time_oracle_attention(at, budget_s: float, threads: int):
     return el / done * 1e6, el, done
 
 
+def time_oracle_mla_attention(at, budget_s: float, threads: int):
+    """Oracle µs per MLA decode-attention call: sampled (request, head) rows
+    through oracle.split_attention_mla (every rank at once) on `threads` host
+    threads, scaled by the latent rows of the whole call."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    a = at["keep"][0]
+    c = a["cfg"]
+    N, H, Dv = c["N"], c["H"], c["Dv"]
+    lens = a["seq_lens"].cpu().tolist()
+    rng = np.random.default_rng(0)
+    total = at["tokens"] * H
+    samples = []
+    for _ in range(2 * threads):
+        b, h = int(rng.integers(len(lens))), int(rng.integers(H))
+        L = lens[b]
+        idx = torch.arange(L, device=a["kv"].device)
+        rows = a["kv"][idx % N, b, idx // N].double().cpu().numpy()
+        samples.append((a["q"][b, h].double().cpu().numpy(), rows, L))
+
+    def unit(k):
+        q, rows, L = samples[k % len(samples)]
+        oracle.split_attention_mla(q, rows, Dv, N, c["sm_scale"], base=c["base"])
+        return L / total
+
+    el, done = run_oracle_units(unit, threads, budget_s)
+    return el / done * 1e6, el, done
+
+
 def time_oracle_cached_extend(budget_s: float, threads: int):
     """Oracle µs per cached-extend call from a small all-rows sample (the same
     recipe at 64 tokens) on `threads` host threads, scaled by the row count."""
@@ -759,7 +841,8 @@ def run_gpu(args):
                                                                      name="gqa_decode_attention"),
               "two_collective": lambda: setup_two_collective(device),
               "per_rank": lambda: setup_per_rank(device),
-              "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens)}[args.only]()
+              "cached_extend": lambda: setup_cached_extend(device, args.ext_tokens),
+              "mla_decode_attention": lambda: setup_mla_attention(device, batch=args.att_batch)}[args.only]()
         time_sequence(wl["launches"], args.steps, args.warmup,
                       None if args.only == "cached_extend" else flush, device)
         clocks.stop()
@@ -835,6 +918,24 @@ def run_gpu(args):
             secondary.append(rec)
             del at
             torch.cuda.empty_cache()
+        mt = setup_mla_attention(device)
+        p5, _ = time_sequence(mt["launches"], max(10, args.steps // 20), 3, flush, device)
+        krec = kernel_record(mt["names"][0], p5[0], mt["bytes"][0], peak)
+        tf = mt["flops"] / (statistics.fmean(p5[0]) * 1e-3) / 1e12
+        tpeak, tkind = load_tensor_peak()
+        krec.update({"flops": mt["flops"], "achieved_tflops": round(tf, 1), "tensor_peak_tflops": tpeak,
+                     "frac_of_tensor_peak": round(tf / tpeak, 4), "tensor_peak_kind": tkind})
+        rec = {"workload": "mla_decode_attention (absorbed MLA on the tcgen05 tensor cores; the step whose "
+                           "outputs the MLA decode merge takes)",
+               "workspace_bytes": mt["workspace_bytes"], "kernels": [krec]}
+        if rank == 0 and not args.no_cpu_baseline:
+            us, el, n = time_oracle_mla_attention(mt, min(5.0, args.cpu_budget), cores)
+            rec["cpu_oracle"] = {"us_per_call": round(us, 1), "cores": cores,
+                                 "sample": f"sampled (request, head) rows worth {n:.2e} calls, {el:.1f} s "
+                                           f"on {cores} threads, scaled by latent rows"}
+        secondary.append(rec)
+        del mt
+        torch.cuda.empty_cache()
         ce = setup_cached_extend(device, slices=True)
         p3, _ = time_sequence(ce["launches"], args.ext_steps, 3, None, device)
         rec = {"workload": "cached_extend N=8 T=16384 H=96 D=512 fp32",
@@ -1087,7 +1188,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=["mla_decode", "sweep", "mla_decode_fp8", "two_collective", "per_rank",
-                                       "cached_extend", "decode_attention", "gqa_decode_attention"],
+                                       "cached_extend", "decode_attention", "gqa_decode_attention",
+                                       "mla_decode_attention"],
                     help="run just this workload's launches (profiling); no JSON line")
     ap.add_argument("--att-batch", type=int, default=None,
                     help="requests of the decode-attention workload under --only (default 64)")

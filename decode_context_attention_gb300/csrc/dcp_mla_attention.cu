@@ -27,13 +27,13 @@
 //     = Q_c . KV_c^T with tcgen05.mma (Q_c, 288 columns of the absorbed
 //     query, held in tensor memory as the A operand; K-major B from shared
 //     memory), fp32 in tensor memory;
-//   * the softmax warpgroup (thread h = head h = TMEM lane h) reads its row
-//     of S_c, sends it to the peer CTA through distributed shared memory,
-//     adds the peer's half (both CTAs form S_0 + S_1 in the same order, so
-//     both get the same bits), and runs an online softmax in base 2 with a
-//     lazily moved reference max (the output is rescaled only when the max
-//     grows by more than 2^8, so most tiles skip it); P goes to tensor
-//     memory as bf16/fp16;
+//   * two softmax warpgroups (thread (h, g) = head h = TMEM lane h, tokens
+//     [32g, 32g + 32) of the tile) read S_c, send it to the peer CTA with
+//     st.async stores that count their bytes on the peer's barrier (no
+//     fence), add the peer's half as S_0 + S_1 in that order (the same bits
+//     in both CTAs), and run an online softmax in base 2 with a lazily moved
+//     reference max (the output is rescaled only when the max grows by more
+//     than 2^8, so most tiles skip it); P goes to tensor memory as bf16/fp16;
 //   * the MMA thread accumulates O_c [128 x 256] += P . V_c with P as the
 //     TMEM A operand and V_c read MN-major from the same shared-memory tile.
 // With one split the softmax warps normalise O and write (O_r, lse_r);
@@ -59,13 +59,18 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kMlaThreads = 192;   // warps 0-3 softmax, 4 TMA, 5 MMA
-constexpr int kTileTokens = 64;    // tokens per tile
+constexpr int kMlaThreads = 320;   // warps 0-7 softmax (two warpgroups), 8 TMA, 9 MMA
+constexpr int kSoftmaxThreads = 256;
+constexpr int kTileTokens = 64;    // tokens per tile (one ring stage)
+constexpr int kHalf = 32;          // tokens of a tile per softmax warpgroup
 constexpr int kStages = 4;         // shared-memory ring depth
+constexpr int kXslots = 2;         // receive slots for the peer's partial scores
 constexpr int kChunkBytes = kTileTokens * 128;      // 64 tokens x 64 columns x 2 bytes
 constexpr int kStageBytes = 5 * kChunkBytes;        // 4 latent chunks + the rope chunk
-constexpr int kXbufBytes = kTileTokens * 128 * 4;   // fp32 partial scores, 64 tokens x 128 heads
-constexpr int kSmemBytes = kStages * kStageBytes + kXbufBytes + 1024 /* barriers */ + 1024 /* alignment */;
+constexpr int kXbufBytes = kTileTokens * 128 * 4;   // fp32 partial scores of a tile, 64 tokens x 128 heads
+constexpr int kMiscBytes = 1536;                    // barriers, then the warpgroups' row maxima / sums
+// the ring, then the receive slots, then the small things
+constexpr int kSmemBytes = kStages * kStageBytes + kXslots * kXbufBytes + kMiscBytes + 1024 /* alignment */;
 // tensor-memory columns
 constexpr uint32_t kColO = 0;      // O_c: 256 fp32 columns
 constexpr uint32_t kColQ = 256;    // Q_c: 288 16-bit elements = 144 columns
@@ -82,10 +87,13 @@ __device__ int g_mla_status;  // first bounded wait that ran out (0 if none)
 
 struct Barriers {
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t q_full, s_full, s_free, p_full, pv_done, mma_done, xfull, xempty;
+    uint64_t q_full, s_full, s_free, p_full, pv_done, mma_done, xfull[kXslots];
+    uint64_t red_full, red_free;  // the warpgroups' per-row values: written / read
     uint32_t tmem_base;
     int abort;
+    float red[2][128];            // per warpgroup and head: tile max, then the final row sum
 };
+static_assert(sizeof(Barriers) <= kMiscBytes, "misc region too small");
 
 template <typename T>
 __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
@@ -104,8 +112,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float4* xbuf = reinterpret_cast<float4*>(smem + kStages * kStageBytes);  // [16][128] float4
-    Barriers* bar = reinterpret_cast<Barriers*>(smem + kStages * kStageBytes + kXbufBytes);
+    float4* xbuf = reinterpret_cast<float4*>(smem + kStages * kStageBytes);  // kXslots x [16][128] float4
+    Barriers* bar = reinterpret_cast<Barriers*>(smem + kStages * kStageBytes + kXslots * kXbufBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t c = cluster_ctarank();  // which half of the columns
@@ -128,20 +136,28 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         }
         mbar_init(&bar->q_full, 128);
         mbar_init(&bar->s_full, 1);
-        mbar_init(&bar->s_free, 4);
-        mbar_init(&bar->p_full, 4);
+        mbar_init(&bar->s_free, 8);
+        mbar_init(&bar->p_full, 8);
         mbar_init(&bar->pv_done, 1);
         mbar_init(&bar->mma_done, 1);
-        mbar_init(&bar->xfull, 128);
-        mbar_init(&bar->xempty, 128);
+        mbar_init(&bar->red_full, kSoftmaxThreads);
+        mbar_init(&bar->red_free, kSoftmaxThreads);
+        // receive slots for the peer's partial scores of tile i (slot i % 2):
+        // this CTA's own expect_tx is the one arrival, the peer's st.async
+        // stores complete the bytes; both slots are armed before the peer
+        // can send (the cluster barrier below)
+        for (int x = 0; x < kXslots; ++x) {
+            mbar_init(&bar->xfull[x], 1);
+            mbar_arrive_expect_tx(&bar->xfull[x], kXbufBytes);
+        }
         bar->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&bar->tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) tma_prefetch_map(&kv_map);
+    if (warp == 8 && lane == 0) tma_prefetch_map(&kv_map);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -151,12 +167,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     int* status = &g_mla_status;
     bool issued_any = false;  // the MMA thread issued at least one MMA
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             int issued = 0;
             for (int i = 0; i < ntiles; ++i) {
                 const int st = i % kStages, k = i / kStages;
+                // stages 2 and 3 first hold the query (staged by the softmax warps)
+                if (i == 2 && !mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort)) break;
                 if (k > 0 && !mbar_wait(&bar->kv_empty[st], (k - 1) & 1, status, kStatusTimeout, abort)) break;
                 uint8_t* dst = stages + st * kStageBytes;
                 mbar_arrive_expect_tx(&bar->kv_full[st], kStageBytes);
@@ -175,20 +193,22 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             constexpr bool kBf16 = !std::is_same<T, __half>::value;
             const uint32_t idesc_qk = idesc_f16(128, kTileTokens, kBf16, 0, 0);
             const uint32_t idesc_pv = idesc_f16(128, 256, kBf16, 0, 1);
             const uint32_t tS = tmem + kColS, tQ = tmem + kColQ, tO = tmem + kColO, tP = tmem + kColP;
+            // O += P_j . V_j, V_j read MN-major from tile j's stage
             auto issue_pv = [&](int j) -> bool {
                 if (!mbar_wait(&bar->p_full, j & 1, status, kStatusTimeout, abort)) return false;
                 tc_fence_after();
-                const uint32_t base = smem_u32(stages + (j % kStages) * kStageBytes);
+                const uint64_t d0 =
+                    smem_desc(smem_u32(stages + (j % kStages) * kStageBytes), kChunkBytes, 1024, kSwizzle128B);
+#pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_ts(tO, tP + 8 * s, smem_desc(base + 2048 * s, kChunkBytes, 1024, kSwizzle128B), idesc_pv,
-                           (j > 0 || s > 0) ? 1u : 0u);
+                    mma_ts(tO, tP + 8 * s, d0 + (uint64_t)((2048 * s) >> 4), idesc_pv, (j > 0 || s > 0) ? 1u : 0u);
                 mma_commit(&bar->pv_done);
                 mma_commit(&bar->kv_empty[j % kStages]);
                 return true;
@@ -199,16 +219,18 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 if (!mbar_wait(&bar->kv_full[st], (i / kStages) & 1, status, kStatusTimeout, abort)) break;
                 if (i > 0 && !mbar_wait(&bar->s_free, (i - 1) & 1, status, kStatusTimeout, abort)) break;
                 tc_fence_after();
-                const uint32_t base = smem_u32(stages + st * kStageBytes);
+                // the descriptor's address field is bits 0-13 in 16-byte units:
+                // offsets inside the stage are added to it directly
+                const uint64_t d0 = smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kSwizzle128B);
                 // latent columns: 4 chunks x 4 steps of 16
+#pragma unroll
                 for (int s = 0; s < 16; ++s)
-                    mma_ts(tS, tQ + 8 * s,
-                           smem_desc(base + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B),
-                           idesc_qk, s > 0 ? 1u : 0u);
+                    mma_ts(tS, tQ + 8 * s, d0 + (uint64_t)(((s >> 2) * kChunkBytes + (s & 3) * 32) >> 4), idesc_qk,
+                           s > 0 ? 1u : 0u);
                 // this CTA's 32 rope columns: the [64c, 64c + 64) bytes of each rope row
+#pragma unroll
                 for (int s = 0; s < 2; ++s)
-                    mma_ts(tS, tQ + 8 * (16 + s),
-                           smem_desc(base + 4 * kChunkBytes + 64 * c + 32 * s, 16, 1024, kSwizzle128B), idesc_qk,
+                    mma_ts(tS, tQ + 8 * (16 + s), d0 + (uint64_t)((4 * kChunkBytes + 64 * c + 32 * s) >> 4), idesc_qk,
                            1u);
                 mma_commit(&bar->s_full);
                 issued_any = true;
@@ -221,37 +243,72 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             if (issued_any) mma_commit(&bar->mma_done);
         }
     } else {
-        // -------------------------------------------------- softmax warpgroup
-        const int h = tid;  // head = TMEM lane
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        // Q_c into tensor memory: latent columns [256c, 256c + 256) then rope
-        // columns [512 + 32c, 544 + 32c), as 144 32-bit pairs
-        {
-            const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (int64_t)b * p.q_sb + (int64_t)h * p.q_sh);
+        // ------------------------------------------- softmax, two warpgroups
+        // Thread (h, g): head h = TMEM lane h (warp w reaches lanes 32 (w % 4)
+        // onwards), token half g = w / 4 of every tile (S columns [32g, 32g +
+        // 32)), output columns [128g, 128g + 128) of O_c.
+        const int h = tid & 127, g = tid >> 7;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        if (g == 0) {
+            // Q_c into tensor memory: latent columns [256c, 256c + 256) then
+            // rope columns [512 + 32c, 544 + 32c), as 144 32-bit pairs.  The
+            // latent part goes through ring stages 2-3 (unused until q_full):
+            // each warp copies its 32 rows with coalesced 16-byte cp.async
+            // (row h at h*512, 16-byte chunk k at position k ^ (h % 32), so
+            // that both the copy and the per-thread row reads are free of
+            // bank conflicts), then every thread moves its row into its lane.
             const bool live = h < p.H;
+            uint8_t* qs = stages + 2 * kStageBytes;
+            const unsigned char* qbase = p.q + (int64_t)b * p.q_sb + 512 * (int64_t)c;
+            uint4 rope[4];
+            {
+                const uint4* qr = reinterpret_cast<const uint4*>(p.q + (int64_t)b * p.q_sb + (int64_t)h * p.q_sh +
+                                                                 2 * (512 + 32 * (int)c));
 #pragma unroll
-            for (int g = 0; g < 9; ++g) {
+                for (int v = 0; v < 4; ++v) rope[v] = live ? __ldg(qr + v) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            for (int j = 0; j < 32; ++j) {
+                const int row = 32 * warp + j;
+                uint4* dst = reinterpret_cast<uint4*>(qs + row * 512 + 16 * (lane ^ (row & 31)));
+                if (row < p.H)
+                    cp_async_cg16(dst, qbase + (int64_t)row * p.q_sh + 16 * lane);
+                else
+                    *dst = make_uint4(0u, 0u, 0u, 0u);
+            }
+            cp_async_wait_all();
+            __syncwarp();
+#pragma unroll
+            for (int gq = 0; gq < 8; ++gq) {
                 uint32_t w[16];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const int vec = 4 * g + v;  // 16-byte vector of the 36 this thread loads
-                    const int col = vec < 32 ? 256 * (int)c + 8 * vec : 512 + 32 * (int)c + 8 * (vec - 32);
-                    const uint4 x = live ? __ldg(qrow + col / 8) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 x = *reinterpret_cast<const uint4*>(qs + h * 512 + 16 * ((4 * gq + v) ^ (h & 31)));
                     w[4 * v] = x.x;
                     w[4 * v + 1] = x.y;
                     w[4 * v + 2] = x.z;
                     w[4 * v + 3] = x.w;
                 }
-                tmem_st16(tmem + kColQ + lane_off + 16 * g, w);
+                tmem_st16(tmem + kColQ + lane_off + 16 * gq, w);
+            }
+            {
+                uint32_t w[16];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    w[4 * v] = rope[v].x;
+                    w[4 * v + 1] = rope[v].y;
+                    w[4 * v + 2] = rope[v].z;
+                    w[4 * v + 3] = rope[v].w;
+                }
+                tmem_st16(tmem + kColQ + lane_off + 16 * 8, w);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bar->q_full);
+            fence_proxy_async_smem();  // the staging reads come before the TMA writes that reuse it
+            mbar_arrive(&bar->q_full);  // also frees ring stages 2-3 for the latent tiles
         }
         const uint32_t peer = c ^ 1u;
         const uint32_t peer_xbuf = map_to_cta(xbuf, peer);
-        const uint32_t peer_xfull = map_to_cta(&bar->xfull, peer);
-        const uint32_t peer_xempty = map_to_cta(&bar->xempty, peer);
+        const uint32_t peer_xfull = map_to_cta(&bar->xfull[0], peer);  // slot x's barrier is 8x bytes further
         const float scale2 = p.sm_scale * kLog2eF;
         float m_used = -INFINITY, l = 0.f;
         // tcgen05.ld / st are warp-collective: every wait's outcome is made
@@ -264,51 +321,74 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 break;
             }
             tc_fence_after();
-            float s[kTileTokens];
+            float own[kHalf];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 2; ++k) {
                 uint32_t u[16];
-                tmem_ld16(tmem + kColS + lane_off + 16 * k, u);
+                tmem_ld16(tmem + kColS + kHalf * g + lane_off + 16 * k, u);
                 tmem_wait_ld();
                 pin(u);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) s[16 * k + j] = __uint_as_float(u[j]);
+                for (int q = 0; q < 16; ++q) own[16 * k + q] = __uint_as_float(u[q]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar->s_free);
-            // exchange the partial scores with the peer CTA
-            if (i > 0 && !__all_sync(kAll, mbar_wait<true>(&bar->xempty, (i - 1) & 1, status, kStatusTimeout, abort))) {
-                ok = false;
-                break;
-            }
+            // exchange the partial scores with the peer CTA: this thread's row
+            // half goes straight into the peer's receive slot i % 2 by
+            // st.async, counted on the peer's barrier.  The slot is free: the
+            // peer sends tile i + 1 only after all of this CTA's tile-i rows
+            // arrived, and each thread sends its tile-i row only after it read
+            // tile i - 2's.
+            const int slot = i & 1;
+            {
+                const uint32_t dst = peer_xbuf + (uint32_t)(slot * kXbufBytes + (8 * g * 128 + h) * 16);
+                const uint32_t xbar = peer_xfull + 8u * (uint32_t)slot;
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                st_cluster_v4(peer_xbuf + (uint32_t)((k * 128 + h) * 16),
-                              make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]));
-            mbar_arrive_remote(peer_xfull);
-            if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull, i & 1, status, kStatusTimeout, abort))) {
+                for (int k = 0; k < kHalf / 4; ++k)
+                    st_async_v4(dst + k * 128 * 16,
+                                make_float4(own[4 * k], own[4 * k + 1], own[4 * k + 2], own[4 * k + 3]), xbar);
+            }
+            if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[slot], (i >> 1) & 1, status, kStatusTimeout, abort))) {
                 ok = false;
                 break;
             }
-            const int valid = t1 - (t0 + i * kTileTokens);
+            const float4* xin = xbuf + slot * (kXbufBytes / 16) + 8 * g * 128;
+            const int valid = t1 - (t0 + i * kTileTokens) - kHalf * g;  // tokens of this half still in the split
+            float s[kHalf];
             float mt = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float4 o4 = xbuf[k * 128 + h];
+            for (int k = 0; k < kHalf / 4; ++k) {
+                const float4 o4 = xin[k * 128 + h];
                 const float other[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int t = 4 * k + j;
+                for (int q = 0; q < 4; ++q) {
+                    const int t = 4 * k + q;
                     // S_0 + S_1 in that order in both CTAs: the same bits on both sides
-                    const float x = (c == 0 ? s[t] + other[j] : other[j] + s[t]) * scale2;
+                    const float x = (c == 0 ? own[t] + other[q] : other[q] + own[t]) * scale2;
                     s[t] = t < valid ? x : -INFINITY;
                     mt = fmaxf(mt, s[t]);
                 }
             }
-            __syncwarp();
-            mbar_arrive_remote(peer_xempty);
-            const float m_new = fmaxf(m_used, mt);
+            // re-arm the slot for tile i + 2 (the peer sends it only after
+            // this CTA's tile i + 1, i.e. after this point)
+            if (tid == 0) mbar_arrive_expect_tx(&bar->xfull[slot], kXbufBytes);
+            // the row max of the whole tile: this thread's half and the other
+            // warpgroup's (through shared memory, written once the other
+            // warpgroup has read the previous tile's value)
+            if (i > 0 && !__all_sync(kAll, mbar_wait(&bar->red_free, (i - 1) & 1, status, kStatusTimeout, abort))) {
+                ok = false;
+                break;
+            }
+            bar->red[g][h] = mt;
+            mbar_arrive(&bar->red_full);
+            if (!__all_sync(kAll, mbar_wait(&bar->red_full, i & 1, status, kStatusTimeout, abort))) {
+                ok = false;
+                break;
+            }
+            const float mt_all = fmaxf(mt, bar->red[g ^ 1][h]);
+            mbar_arrive(&bar->red_free);
+            const float m_new = fmaxf(m_used, mt_all);
             const bool move = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
             // P and O are free once the previous tile's P.V has completed
             if (i > 0 && !__all_sync(kAll, mbar_wait(&bar->pv_done, (i - 1) & 1, status, kStatusTimeout, abort))) {
@@ -316,19 +396,19 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 break;
             }
             tc_fence_after();
-            if (valid < kTileTokens) {
+            if (valid < kHalf) {
                 // rows past the split's last token were loaded from the cache
                 // as they are (stale values, possibly NaN): zero their value
                 // columns so that 0-probability rows add exactly 0
-                uint8_t* stage = stages + (i % kStages) * kStageBytes;
-                const int rows = kTileTokens - valid;
+                uint8_t* rows0 = stages + (i % kStages) * kStageBytes + kHalf * g * 128;
+                const int first = valid < 0 ? 0 : valid, rows = kHalf - first;
                 for (int e = h; e < 4 * rows * 8; e += 128) {
                     const int chunk = e / (rows * 8), rem = e % (rows * 8);
-                    const int row = valid + rem / 8, v16 = rem % 8;
-                    *reinterpret_cast<uint4*>(stage + chunk * kChunkBytes + row * 128 + v16 * 16) =
+                    const int row = first + rem / 8, v16 = rem % 8;
+                    *reinterpret_cast<uint4*>(rows0 + chunk * kChunkBytes + row * 128 + v16 * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                fence_proxy_async_smem();
             }
             float alpha = 1.f;
             if (move) {
@@ -337,100 +417,116 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 m_used = m_new;
             }
             if (i > 0 && __any_sync(kAll, move)) {
-                // rescale this warp's rows of O (alpha = 1 for rows that keep their max)
-                for (int k = 0; k < 16; ++k) {
+                // rescale this thread's 128 columns of O row h (alpha = 1 for
+                // rows that keep their max)
+                for (int k = 0; k < 8; ++k) {
                     uint32_t u[16];
-                    tmem_ld16(tmem + kColO + lane_off + 16 * k, u);
+                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
                     tmem_wait_ld();
                     pin(u);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
-                    tmem_st16(tmem + kColO + lane_off + 16 * k, u);
+                    for (int q = 0; q < 16; ++q) u[q] = __float_as_uint(__uint_as_float(u[q]) * alpha);
+                    tmem_st16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
                 }
             }
             // P = 2^(s - m) in the payload type; the row sum in fp32 (a row
             // whose scores so far are all -inf has m = -inf and p = 0)
             const float msub = m_used == -INFINITY ? 0.f : m_used;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            {
                 uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float pa = exp2f(s[32 * k + 2 * j] - msub);
-                    const float pb = exp2f(s[32 * k + 2 * j + 1] - msub);
+                for (int q = 0; q < 16; ++q) {
+                    const float pa = exp2f(s[2 * q] - msub);
+                    const float pb = exp2f(s[2 * q + 1] - msub);
                     l += pa + pb;
-                    w[j] = pack_pair<T>(pa, pb);
+                    w[q] = pack_pair<T>(pa, pb);
                 }
-                tmem_st16(tmem + kColP + lane_off + 16 * k, w);
+                tmem_st16(tmem + kColP + 16 * g + lane_off, w);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar->p_full);
         }
-        if (ok && ntiles > 0) ok = __all_sync(kAll, mbar_wait(&bar->pv_done, (ntiles - 1) & 1, status, kStatusTimeout, abort));
+        if (ok && ntiles > 0)
+            ok = __all_sync(kAll, mbar_wait(&bar->pv_done, (ntiles - 1) & 1, status, kStatusTimeout, abort));
         tc_fence_after();
         // ----------------------------------------------------------- epilogue
+        // the row sum is the two warpgroups' partial sums (both relative to
+        // the same reference max)
+        if (ok && ntiles > 0 &&
+            !__all_sync(kAll, mbar_wait(&bar->red_free, (ntiles - 1) & 1, status, kStatusTimeout, abort)))
+            ok = false;
+        float l_all = 0.f;
+        if (ok) {
+            bar->red[g][h] = l;
+            mbar_arrive(&bar->red_full);
+            if (__all_sync(kAll, mbar_wait(&bar->red_full, ntiles & 1, status, kStatusTimeout, abort)))
+                l_all = g == 0 ? l + bar->red[1][h] : bar->red[0][h] + l;
+            else
+                ok = false;
+        }
         // `have` is warp-uniform (it decides the warp-collective loads of O);
-        // a row with no probability mass (l = 0) still reads O but writes 0
+        // a row with no probability mass still reads O but writes 0
         const bool have = ok && ntiles > 0;
-        const bool mass = have && l > 0.f;
-        const float inv = mass ? 1.f / l : 0.f;
-        const float lse2 = mass ? m_used + log2f(l) : -INFINITY;
+        const bool mass = have && l_all > 0.f;
+        const float inv = mass ? 1.f / l_all : 0.f;
+        const float lse2 = mass ? m_used + log2f(l_all) : -INFINITY;
         const bool live = h < p.H;
         if (p.nsplit == 1) {
-            unsigned char* orow = p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + 512 * c;
-            for (int k = 0; k < 16; ++k) {
+            unsigned char* orow =
+                p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + 2 * (256 * c + 128 * g);
+            for (int k = 0; k < 8; ++k) {
                 uint32_t u[16];
                 if (have) {
-                    tmem_ld16(tmem + kColO + lane_off + 16 * k, u);
+                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
                     tmem_wait_ld();
                     pin(u);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) u[j] = 0u;
+                    for (int q = 0; q < 16; ++q) u[q] = 0u;
                 }
                 uint32_t w[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    w[j] = pack_pair<T>(__uint_as_float(u[2 * j]) * inv, __uint_as_float(u[2 * j + 1]) * inv);
+                for (int q = 0; q < 8; ++q)
+                    w[q] = pack_pair<T>(__uint_as_float(u[2 * q]) * inv, __uint_as_float(u[2 * q + 1]) * inv);
                 if (live) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
                     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
-            if (live && c == 0)
+            if (live && c == 0 && g == 0)
                 p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] = p.base2 ? lse2 : lse2 * kLn2F;
         } else {
             const int64_t row = (((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split;
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + row * 512 + 256 * c);
-            for (int k = 0; k < 16; ++k) {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + row * 512 + 256 * c + 128 * g);
+            for (int k = 0; k < 8; ++k) {
                 uint32_t u[16];
                 if (have) {
-                    tmem_ld16(tmem + kColO + lane_off + 16 * k, u);
+                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
                     tmem_wait_ld();
                     pin(u);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) u[j] = 0u;
+                    for (int q = 0; q < 16; ++q) u[q] = 0u;
                 }
                 if (live) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[4 * k + j] = make_float4(__uint_as_float(u[4 * j]) * inv, __uint_as_float(u[4 * j + 1]) * inv,
-                                                     __uint_as_float(u[4 * j + 2]) * inv,
-                                                     __uint_as_float(u[4 * j + 3]) * inv);
+                    for (int q = 0; q < 4; ++q)
+                        dst[4 * k + q] = make_float4(__uint_as_float(u[4 * q]) * inv, __uint_as_float(u[4 * q + 1]) * inv,
+                                                     __uint_as_float(u[4 * q + 2]) * inv,
+                                                     __uint_as_float(u[4 * q + 3]) * inv);
                 }
             }
-            if (live && c == 0) p.ws_lse[row] = lse2;
+            if (live && c == 0 && g == 0) p.ws_lse[row] = lse2;
         }
     }
 
     // --------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         if (lane == 0 && issued_any) {
             // every MMA this CTA issued has completed before its tensor memory goes
             const uint64_t t_start = global_timer_ns();

@@ -220,6 +220,41 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
                  "f"(v.w)
                  : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// the shared::cluster address `dst` of another CTA, completing as
+// transaction bytes on the barrier at shared::cluster address `bar` (in the
+// destination CTA).  The source may be rewritten once that barrier's phase
+// has completed.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// 16 bytes stored into another CTA's shared memory (shared::cluster address
+// `dst`), counted as transaction bytes on the barrier at shared::cluster
+// address `bar` in that CTA: no fence is needed for the receiver to see the
+// data once that barrier's phase completes.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     dst),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
+}
+// Ampere-style asynchronous 16-byte copy global -> this CTA's shared memory.
+__device__ __forceinline__ void cp_async_cg16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+}
+// Orders this thread's shared-memory writes before later async-proxy reads
+// of them (a bulk copy or an MMA operand).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Barrier `id` (1..15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
