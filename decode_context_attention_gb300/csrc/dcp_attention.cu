@@ -130,6 +130,7 @@ __device__ __forceinline__ void write_cta_result(const AttnParams& p, int r, int
 
 template <typename T, int D, int GQ, bool PAGED>
 __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const AttnParams p) {
+    pdl_wait();
     constexpr int LPT = D / 8;              // lanes per token row (16-byte vectors)
     constexpr int TPW = 32 / LPT;           // token rows per warp step
     constexpr int NG = (kAttnThreads / 32) * TPW;  // lane groups per CTA
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_kernel(const Attn
     }
     __syncthreads();
     write_cta_result<T, D, GQ, NG>(p, r, b, hkv, split, s_m, s_l, s_acc);
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -323,6 +325,7 @@ __device__ __forceinline__ unsigned word_of(const uint4& v, int w) {
 
 template <typename T, int D, int GQ, bool PAGED>
 __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const AttnParams p) {
+    pdl_wait();
     static_assert(D % 32 == 0 && GQ >= 1 && GQ <= 16, "fragment shapes");
     constexpr int NB = GQ > 8 ? 2 : 1;    // blocks of 8 query heads (fragment rows qr and qr + 8)
     constexpr int NI = D / 32;   // 16-byte pieces per lane per token row
@@ -558,12 +561,14 @@ __global__ void __launch_bounds__(kAttnThreads) decode_partial_mma_kernel(const 
     }
     __syncthreads();
     write_cta_result<T, D, GQ, NW>(p, r, b, hkv, split, s_m, s_l, s_acc);
+    pdl_trigger();
 }
 
 // Merge the splits of every (rank, request, head) row: the LSE-weighted merge
 // in base 2 over the fp32 partials, one warp per row, lanes over D.
 template <typename T, int D>
 __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const AttnParams p) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t rows = (int64_t)p.N * p.B * p.H;
     const int64_t row = (int64_t)blockIdx.x * (kAttnThreads / 32) + (threadIdx.x >> 5);
@@ -597,6 +602,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const
         const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
         p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] = p.base2 ? lse2 : lse2 * kLn2;
     }
+    pdl_trigger();
 }
 
 template <typename T, int D, bool PAGED>
@@ -632,12 +638,12 @@ static cudaError_t launch_attention_dp(const AttnParams& p, cudaStream_t stream)
     }
     void* args[] = {(void*)&p};
     const dim3 grid((unsigned)((int64_t)p.N * p.B * p.Hkv * p.nsplit));  // split fastest
-    cudaError_t e = cudaLaunchKernel(k, grid, dim3(kAttnThreads), args, 0, stream);
+    cudaError_t e = launch_pdl(k, grid, dim3(kAttnThreads), args, 0, stream);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const int64_t rows = (int64_t)p.N * p.B * p.H;
     const unsigned mgrid = (unsigned)((rows + kAttnThreads / 32 - 1) / (kAttnThreads / 32));
-    return cudaLaunchKernel((const void*)decode_merge_splits_kernel<T, D>, dim3(mgrid), dim3(kAttnThreads),
-                            args, 0, stream);
+    return launch_pdl((const void*)decode_merge_splits_kernel<T, D>, dim3(mgrid), dim3(kAttnThreads), args, 0,
+                      stream);
 }
 
 template <typename T, int D>

@@ -135,6 +135,7 @@ __device__ __forceinline__ void serial_weights(const float* lrow, int64_t l_sn, 
 // ---------------------------------------------------------------------------
 template <typename T, int VB, int NRMAX, bool SAN>
 __global__ void __launch_bounds__(kThreads, 2) combine_kernel(const CombineParams p) {
+    pdl_wait();
     constexpr int EPV = VB / (int)sizeof(T);
     constexpr int RC = NRMAX < 8 ? NRMAX : 8;  // ranks per load batch
     // vectors per lane per batch: at most ~64 registers of loaded payload and
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(const CombineParam
         }
         if (p.return_lse && lg.jl == 0) p.out_lse[c.g * p.ul_sg + (int64_t)c.b * p.ul_sb + (int64_t)c.h * p.ul_sh] = Gl;
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(const CombineParam
 // ---------------------------------------------------------------------------
 template <typename T, int VB, int NR, int LPR, int VPL, bool SAN>
 __global__ void __launch_bounds__(kThreads, (sizeof(T) == 1 && VB == 4) ? 3 : 2) combine_fixed_kernel(const CombineParams p) {
+    pdl_wait();
     constexpr int NP = VB / (int)sizeof(T) / 2;  // fp32 pairs per vector
     // vectors per lane per rank loaded at once: <= 64 registers of payload
     // and <= 64 registers of packed fp32 accumulators
@@ -291,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, (sizeof(T) == 1 && VB == 4) ? 3 : 2)
         if (p.return_lse && lg.jl == 0)
             p.out_lse[c.g * p.ul_sg + (int64_t)c.b * p.ul_sb + (int64_t)c.h * p.ul_sh] = Gl;
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, (sizeof(T) == 1 && VB == 4) ? 3 : 2)
 // ---------------------------------------------------------------------------
 template <typename T, int NR, int LPR, int VPL, bool SAN>
 __global__ void __launch_bounds__(kThreads, 2) combine_shifted_kernel(const CombineParams p) {
+    pdl_wait();
     constexpr int NP = 16 / (int)sizeof(T) / 2;  // fp32 pairs per chunk
     constexpr int EPW = 4 / (int)sizeof(T);      // elements per word
     constexpr int RB = LPR * VPL * 16;           // payload bytes of a row
@@ -397,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) combine_shifted_kernel(const Comb
         if (p.return_lse && lg.jl == 0)
             p.out_lse[c.g * p.ul_sg + (int64_t)c.b * p.ul_sb + (int64_t)c.h * p.ul_sh] = Gl;
     }
+    pdl_trigger();
 }
 
 // Shifted-chunk kernel for (T, NR) and this row length, or nullptr.
@@ -447,6 +453,7 @@ const void* pick_fixed(int row_bytes, int& lpr) {
 // ---------------------------------------------------------------------------
 template <typename T, int VB>
 __global__ void __launch_bounds__(kThreads, 2) combine_kernel_any_n(const CombineParams p) {
+    pdl_wait();
     constexpr int EPV = VB / (int)sizeof(T);
     constexpr int RC = 8;
     using V = typename VecT<VB>::type;
@@ -504,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel_any_n(const Combin
         }
         if (p.return_lse && lg.jl == 0) p.out_lse[g * p.ul_sg + b * p.ul_sb + h * p.ul_sh] = Gl;
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -526,6 +534,7 @@ constexpr size_t staged_smem_bytes() {
 
 template <typename T, int NR, int VPL, bool SAN>
 __global__ void __launch_bounds__(kStagedWarps * 32) combine_staged_kernel(const CombineParams p) {
+    pdl_wait();
     constexpr int VPR = NR * VPL;  // 16-byte slices per lane per row
     constexpr int EPV = 16 / (int)sizeof(T);
     extern __shared__ uint4 smem[];
@@ -633,6 +642,7 @@ __global__ void __launch_bounds__(kStagedWarps * 32) combine_staged_kernel(const
         }
     }
     cp_async_wait<0>();
+    pdl_trigger();
 }
 
 template <typename T, int NR, bool SAN>
@@ -662,7 +672,7 @@ cudaError_t launch_combine_vb(const CombineParams& p, cudaStream_t stream) {
                 q.lpr = lpr;
                 void* qargs[] = {(void*)&q};
                 const int grid = persistent_grid(k, p.rows, (kThreads / 32) * (32 / lpr), kThreads, 0);
-                return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), qargs, 0, stream);
+                return launch_pdl(k, dim3(grid), dim3(kThreads), qargs, 0, stream);
             }
         }
     }
@@ -677,7 +687,7 @@ cudaError_t launch_combine_vb(const CombineParams& p, cudaStream_t stream) {
             q.lpr = lpr;
             void* qargs[] = {(void*)&q};
             const int grid = persistent_grid(k, p.rows, (kThreads / 32) * (32 / lpr), kThreads, 0);
-            return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), qargs, 0, stream);
+            return launch_pdl(k, dim3(grid), dim3(kThreads), qargs, 0, stream);
         }
     }
 #endif
@@ -695,7 +705,7 @@ cudaError_t launch_combine_vb(const CombineParams& p, cudaStream_t stream) {
                                      : pick_staged<T, 8, SAN>(vpl, smem);
             const int threads = kStagedWarps * 32;
             const int grid = persistent_grid(k, p.rows, kStagedWarps * rows_per_warp, threads, smem);
-            return cudaLaunchKernel(k, dim3(grid), dim3(threads), args, smem, stream);
+            return launch_pdl(k, dim3(grid), dim3(threads), args, smem, stream);
         }
     }
     const void* k;
@@ -706,7 +716,7 @@ cudaError_t launch_combine_vb(const CombineParams& p, cudaStream_t stream) {
     else if (p.N <= 32) k = (const void*)combine_kernel<T, VB, 32, SAN>;
     else k = (const void*)combine_kernel_any_n<T, VB>;
     const int grid = persistent_grid(k, p.rows, (kThreads / 32) * rows_per_warp, kThreads, 0);
-    return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, stream);
+    return launch_pdl(k, dim3(grid), dim3(kThreads), args, 0, stream);
 }
 
 template <typename T, int VB>

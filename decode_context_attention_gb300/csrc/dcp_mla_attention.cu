@@ -122,12 +122,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     const int rb = item / p.nsplit;
     const int b = rb % p.B;
     const int r = rb / p.B;
-    int L = p.seq_lens[b];
-    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
-    const int Ll = L / p.N + (r < L % p.N ? 1 : 0);
-    const int t0 = split * p.split_tokens;
-    const int t1 = min(t0 + p.split_tokens, Ll);
-    const int ntiles = t1 > t0 ? (t1 - t0 + kTileTokens - 1) / kTileTokens : 0;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -162,6 +156,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     cluster_sync();  // the peer's barriers are initialised before any remote arrival
+    pdl_wait();      // the set-up above overlapped the previous kernel's tail
+    int L = p.seq_lens[b];
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+    const int Ll = L / p.N + (r < L % p.N ? 1 : 0);
+    const int t0 = split * p.split_tokens;
+    const int t1 = min(t0 + p.split_tokens, Ll);
+    const int ntiles = t1 > t0 ? (t1 - t0 + kTileTokens - 1) / kTileTokens : 0;
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort = &bar->abort;
     int* status = &g_mla_status;
@@ -524,6 +525,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     }
 
     // --------------------------------------------------------------- teardown
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
@@ -545,6 +547,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
 // (empty splits are (0, -inf) and drop out).
 template <typename T>
 __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t rows = (int64_t)p.N * p.B * p.H;
     const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -587,6 +590,7 @@ __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p
         const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
         p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] = p.base2 ? lse2 : lse2 * kLn2F;
     }
+    pdl_trigger();
 }
 
 // cuTensorMapEncodeTiled, looked up from the driver once (no link-time
@@ -620,18 +624,22 @@ cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, cudaStream_
     cfg.blockDim = dim3(kMlaThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = DCP_PDL ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<T>, map, p);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const int64_t rows = (int64_t)p.N * p.B * p.H;
-    mla_merge_splits_kernel<T><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    MlaParams q = p;
+    void* args[] = {(void*)&q};
+    return launch_pdl((const void*)mla_merge_splits_kernel<T>, dim3((unsigned)((rows + 3) / 4)), dim3(128), args, 0,
+                      stream);
 }
 
 }  // namespace

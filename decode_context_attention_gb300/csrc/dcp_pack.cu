@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const PackParams p) {
     constexpr int MAXV = VB == 16 ? 8 : 32;  // vectors held per lane per batch (<= 32 registers)
     constexpr int RB = LINEAR ? (MAXV / VPL > 0 ? MAXV / VPL : 1) : 1;  // rows per batch
     using V = typename VecT<VB>::type;
+    pdl_wait();
     const int lpr = LPR > 0 ? LPR : p.lpr;
     const LaneGroup lg = lane_group(lpr);
     const int nv = p.row_bytes / VB;
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const PackParams p) {
         }
         cur.add(st.dg, st.db, st.dh, p.B, p.H);
     }
+    pdl_trigger();
 }
 
 template <int VB, bool LINEAR>
@@ -104,7 +106,7 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
     const int64_t nbatch = (p.rows + rb - 1) / rb;
     const int grid = grid_for(k, nbatch, batches_per_cta, kThreads, 0, false);
     void* args[] = {(void*)&p};
-    return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, stream);
+    return launch_pdl(k, dim3(grid), dim3(kThreads), args, 0, stream);
 }
 
 }  // namespace dcp
