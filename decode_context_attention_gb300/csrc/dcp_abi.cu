@@ -680,6 +680,9 @@ dcp_status_t dcp_decode_attention_mla(int dtype, int N, int B, int H, int Dk, in
                         who);
     if (kv_st < Dk) return fail(DCP_ERR_INVALID_ARG, "%s: token stride %lld below the row of %d elements", who,
                                 (long long)kv_st, Dk);
+    // the queries' rope columns are read by TMA as well: byte strides below 2^40
+    if (q_sb * e >= (int64_t(1) << 40) || q_sh * e >= (int64_t(1) << 40))
+        return fail(DCP_ERR_INVALID_ARG, "%s: query strides must be below 2^39 elements", who);
     if ((uintptr_t)kv % 16) return fail(DCP_ERR_MISALIGNED, "%s: cache not 16-byte aligned", who);
     View vq = View(q, (int64_t)Dk * e).dim(B, q_sb * e).dim(H, q_sh * e);
     View vk = View(kv, (int64_t)Dk * e).dim(N, kv_sn * e).dim(B, kv_sb * e).dim(lcap, kv_st * e);

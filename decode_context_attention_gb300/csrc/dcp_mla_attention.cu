@@ -22,18 +22,23 @@
 // -- exactly the columns it loads, so the pair reads every latent byte once
 // and does every multiply-add once.  Per tile of 64 tokens:
 //   * TMA (one thread) loads the CTA's four 64-column latent chunks and the
-//     rope chunk of the 64 tokens, 128-byte swizzled, into a 4-stage ring;
+//     rope chunk of the 64 tokens, 128-byte swizzled, into a 3-stage ring;
 //   * the MMA thread computes the partial scores S_c [128 heads x 64 tokens]
-//     = Q_c . KV_c^T with tcgen05.mma (Q_c, 288 columns of the absorbed
-//     query, held in tensor memory as the A operand; K-major B from shared
-//     memory), fp32 in tensor memory;
+//     = Q_c . KV_c^T with tcgen05.mma, fp32 in tensor memory: the query's
+//     256 latent columns are the A operand in tensor memory, its 32 rope
+//     columns an A operand in shared memory (a TMA tile), the latent rows the
+//     K-major B operand;
+//   * an exchange warpgroup reads S_c as soon as it is ready and sends it to
+//     the peer CTA with st.async stores that count their bytes on the peer's
+//     mbarrier (no fence); a 4-byte st.async credit from the peer frees each
+//     of its two receive slots again.  Scores are double-buffered in TMEM,
+//     so the exchange of tile i + 1 overlaps the softmax of tile i;
 //   * two softmax warpgroups (thread (h, g) = head h = TMEM lane h, tokens
-//     [32g, 32g + 32) of the tile) read S_c, send it to the peer CTA with
-//     st.async stores that count their bytes on the peer's barrier (no
-//     fence), add the peer's half as S_0 + S_1 in that order (the same bits
-//     in both CTAs), and run an online softmax in base 2 with a lazily moved
-//     reference max (the output is rescaled only when the max grows by more
-//     than 2^8, so most tiles skip it); P goes to tensor memory as bf16/fp16;
+//     [32g, 32g + 32) of the tile) add the peer's half as S_0 + S_1 in that
+//     order (the same bits in both CTAs) and run an online softmax in base 2
+//     with a lazily moved reference max (the output is rescaled only when the
+//     max grows by more than 2^8, so most tiles skip it); P goes to tensor
+//     memory as bf16/fp16, over its tile's consumed scores;
 //   * the MMA thread accumulates O_c [128 x 256] += P . V_c with P as the
 //     TMEM A operand and V_c read MN-major from the same shared-memory tile.
 // With one split the softmax warps normalise O and write (O_r, lse_r);
@@ -59,23 +64,23 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kMlaThreads = 320;   // warps 0-7 softmax (two warpgroups), 8 TMA, 9 MMA
+constexpr int kMlaThreads = 448;   // warps 0-7 softmax, 8-11 exchange, 12 TMA, 13 MMA
 constexpr int kSoftmaxThreads = 256;
 constexpr int kTileTokens = 64;    // tokens per tile (one ring stage)
 constexpr int kHalf = 32;          // tokens of a tile per softmax warpgroup
-constexpr int kStages = 4;         // shared-memory ring depth
-constexpr int kXslots = 2;         // receive slots for the peer's partial scores
+constexpr int kStages = 3;         // shared-memory ring depth
 constexpr int kChunkBytes = kTileTokens * 128;      // 64 tokens x 64 columns x 2 bytes
 constexpr int kStageBytes = 5 * kChunkBytes;        // 4 latent chunks + the rope chunk
 constexpr int kXbufBytes = kTileTokens * 128 * 4;   // fp32 partial scores of a tile, 64 tokens x 128 heads
-constexpr int kMiscBytes = 1536;                    // barriers, then the warpgroups' row maxima / sums
-// the ring, then the receive slots, then the small things
-constexpr int kSmemBytes = kStages * kStageBytes + kXslots * kXbufBytes + kMiscBytes + 1024 /* alignment */;
+constexpr int kQropeBytes = 128 * 128;              // [128 heads x 64 rope columns], 128-byte swizzled
+constexpr int kMiscBytes = 2048;                    // barriers, the warpgroups' row values, credit words
+// the ring, the two receive slots (first the query's staging area), the
+// query's rope tile, the small things
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kXbufBytes + kQropeBytes + kMiscBytes + 1024 /* align */;
 // tensor-memory columns
 constexpr uint32_t kColO = 0;      // O_c: 256 fp32 columns
-constexpr uint32_t kColQ = 256;    // Q_c: 288 16-bit elements = 144 columns
-constexpr uint32_t kColS = 400;    // S_c: 64 fp32 columns
-constexpr uint32_t kColP = 464;    // P: 64 16-bit elements = 32 columns
+constexpr uint32_t kColQ = 256;    // Q_c latent part: 256 16-bit elements = 128 columns
+constexpr uint32_t kColSP = 384;   // two buffers of 64 columns: S_c of a tile, then its P in the first 32
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;  // move the reference max when it would grow by more than this
 constexpr float kLog2eF = 1.4426950408889634f;
@@ -87,10 +92,14 @@ __device__ int g_mla_status;  // first bounded wait that ran out (0 if none)
 
 struct Barriers {
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t q_full, s_full, s_free, p_full, pv_done, mma_done, xfull[kXslots];
-    uint64_t red_full, red_free;  // the warpgroups' per-row values: written / read
+    uint64_t q_full, qrope_full, mma_done;
+    uint64_t s_full[2], s_read[2], p_full[2], pv_done[2];  // per score / probability buffer
+    uint64_t xfull[2];   // receive slot: the peer's partial scores arrived (st.async bytes)
+    uint64_t credit[2];  // send slot: the peer has freed its receive slot (a st.async credit)
+    uint64_t red_full, red_free;  // the softmax warpgroups' per-row values: written / read
     uint32_t tmem_base;
     int abort;
+    uint32_t credit_word[2];      // landing words of the peer's credits
     float red[2][128];            // per warpgroup and head: tile max, then the final row sum
 };
 static_assert(sizeof(Barriers) <= kMiscBytes, "misc region too small");
@@ -106,17 +115,30 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
     }
 }
 
+// Roles and the flow of one tile i (buffer u = i % 2, slot u, stage i % 3):
+//   TMA      kv_full[stage] <- 5 chunks of the tile's latent rows
+//   MMA      QK(i) -> S in SP[u] (s_full[u]); after P(i): PV(i) (pv_done[u],
+//            kv_empty[stage]); then QK(i + 2) into SP[u] (in issue order after PV(i))
+//   exchange S(i) from SP[u] (s_read[u]) -> the peer's receive slot u by
+//            st.async, once the peer granted that slot (credit[u])
+//   softmax  the peer's S(i) from slot u (xfull[u]) + the own S(i) from
+//            SP[u]; then re-arm xfull[u] and grant the slot back to the peer;
+//            P(i) into SP[u] columns [0, 32) (p_full[u])
 template <typename T>
 __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map,
+                                                                   const __grid_constant__ CUtensorMap q_map,
                                                                    const MlaParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float4* xbuf = reinterpret_cast<float4*>(smem + kStages * kStageBytes);  // kXslots x [16][128] float4
-    Barriers* bar = reinterpret_cast<Barriers*>(smem + kStages * kStageBytes + kXslots * kXbufBytes);
+    uint8_t* slots = smem + kStages * kStageBytes;                           // 2 x [16][128] float4
+    float4* xbuf = reinterpret_cast<float4*>(slots);
+    uint8_t* qrope = slots + 2 * kXbufBytes;
+    Barriers* bar = reinterpret_cast<Barriers*>(qrope + kQropeBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t c = cluster_ctarank();  // which half of the columns
+    const uint32_t peer = c ^ 1u;
     const int item = (int)(blockIdx.x >> 1);
     const int split = item % p.nsplit;
     const int rb = item / p.nsplit;
@@ -129,29 +151,33 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             mbar_init(&bar->kv_empty[s], 1);
         }
         mbar_init(&bar->q_full, 128);
-        mbar_init(&bar->s_full, 1);
-        mbar_init(&bar->s_free, 8);
-        mbar_init(&bar->p_full, 8);
-        mbar_init(&bar->pv_done, 1);
+        mbar_init(&bar->qrope_full, 1);
         mbar_init(&bar->mma_done, 1);
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&bar->s_full[u], 1);
+            mbar_init(&bar->s_read[u], 4);
+            mbar_init(&bar->p_full[u], 8);
+            mbar_init(&bar->pv_done[u], 1);
+            // the peer's bytes complete these; this CTA's expect_tx is the one
+            // arrival, armed here for the first phase
+            mbar_init(&bar->xfull[u], 1);
+            mbar_arrive_expect_tx(&bar->xfull[u], kXbufBytes);
+            mbar_init(&bar->credit[u], 1);
+            mbar_arrive_expect_tx(&bar->credit[u], 4);
+        }
         mbar_init(&bar->red_full, kSoftmaxThreads);
         mbar_init(&bar->red_free, kSoftmaxThreads);
-        // receive slots for the peer's partial scores of tile i (slot i % 2):
-        // this CTA's own expect_tx is the one arrival, the peer's st.async
-        // stores complete the bytes; both slots are armed before the peer
-        // can send (the cluster barrier below)
-        for (int x = 0; x < kXslots; ++x) {
-            mbar_init(&bar->xfull[x], 1);
-            mbar_arrive_expect_tx(&bar->xfull[x], kXbufBytes);
-        }
         bar->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tmem_alloc(&bar->tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) tma_prefetch_map(&kv_map);
+    if (warp == 12 && lane == 0) {
+        tma_prefetch_map(&kv_map);
+        tma_prefetch_map(&q_map);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -167,15 +193,17 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     volatile int* abort = &bar->abort;
     int* status = &g_mla_status;
     bool issued_any = false;  // the MMA thread issued at least one MMA
+    const unsigned kAll = 0xffffffffu;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
+            // the query's rope columns, [128 heads x 64], once (heads past H read 0)
+            mbar_arrive_expect_tx(&bar->qrope_full, kQropeBytes);
+            tma_load_3d(qrope, &q_map, &bar->qrope_full, 512, 0, b);
             int issued = 0;
             for (int i = 0; i < ntiles; ++i) {
                 const int st = i % kStages, k = i / kStages;
-                // stages 2 and 3 first hold the query (staged by the softmax warps)
-                if (i == 2 && !mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort)) break;
                 if (k > 0 && !mbar_wait(&bar->kv_empty[st], (k - 1) & 1, status, kStatusTimeout, abort)) break;
                 uint8_t* dst = stages + st * kStageBytes;
                 mbar_arrive_expect_tx(&bar->kv_full[st], kStageBytes);
@@ -186,91 +214,131 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 issued = i + 1;
             }
             // copies still in flight (only after an abort) land before the CTA ends
+            const uint64_t t_start = global_timer_ns();
+            while (!mbar_try_wait(&bar->qrope_full, 0) && global_timer_ns() - t_start < kWaitLimitNs) {
+            }
             for (int i = max(0, issued - kStages); i < issued; ++i) {
                 uint64_t* fb = &bar->kv_full[i % kStages];
                 const uint32_t par = (i / kStages) & 1;
-                const uint64_t t_start = global_timer_ns();
-                while (!mbar_try_wait(fb, par) && global_timer_ns() - t_start < kWaitLimitNs) {
+                const uint64_t t1w = global_timer_ns();
+                while (!mbar_try_wait(fb, par) && global_timer_ns() - t1w < kWaitLimitNs) {
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             constexpr bool kBf16 = !std::is_same<T, __half>::value;
             const uint32_t idesc_qk = idesc_f16(128, kTileTokens, kBf16, 0, 0);
             const uint32_t idesc_pv = idesc_f16(128, 256, kBf16, 0, 1);
-            const uint32_t tS = tmem + kColS, tQ = tmem + kColQ, tO = tmem + kColO, tP = tmem + kColP;
-            // O += P_j . V_j, V_j read MN-major from tile j's stage
-            auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait(&bar->p_full, j & 1, status, kStatusTimeout, abort)) return false;
-                tc_fence_after();
-                const uint64_t d0 =
-                    smem_desc(smem_u32(stages + (j % kStages) * kStageBytes), kChunkBytes, 1024, kSwizzle128B);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_ts(tO, tP + 8 * s, d0 + (uint64_t)((2048 * s) >> 4), idesc_pv, (j > 0 || s > 0) ? 1u : 0u);
-                mma_commit(&bar->pv_done);
-                mma_commit(&bar->kv_empty[j % kStages]);
-                return true;
-            };
-            bool ok = mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort);
-            for (int i = 0; ok && i < ntiles; ++i) {
+            const uint32_t tQ = tmem + kColQ, tO = tmem + kColO;
+            const uint64_t dq = smem_desc(smem_u32(qrope), 16, 1024, kSwizzle128B);
+            // S(i) = Q_c . KV_c(i)^T into buffer i % 2.  The descriptor's
+            // address field is bits 0-13 in 16-byte units: offsets are added
+            // to it directly.
+            auto issue_qk = [&](int i) -> bool {
                 const int st = i % kStages;
-                if (!mbar_wait(&bar->kv_full[st], (i / kStages) & 1, status, kStatusTimeout, abort)) break;
-                if (i > 0 && !mbar_wait(&bar->s_free, (i - 1) & 1, status, kStatusTimeout, abort)) break;
+                if (!mbar_wait(&bar->kv_full[st], (i / kStages) & 1, status, kStatusTimeout, abort)) return false;
                 tc_fence_after();
-                // the descriptor's address field is bits 0-13 in 16-byte units:
-                // offsets inside the stage are added to it directly
+                const uint32_t tS = tmem + kColSP + 64 * (i & 1);
                 const uint64_t d0 = smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kSwizzle128B);
-                // latent columns: 4 chunks x 4 steps of 16
 #pragma unroll
-                for (int s = 0; s < 16; ++s)
+                for (int s = 0; s < 16; ++s)  // latent columns: 4 chunks x 4 steps of 16, A in TMEM
                     mma_ts(tS, tQ + 8 * s, d0 + (uint64_t)(((s >> 2) * kChunkBytes + (s & 3) * 32) >> 4), idesc_qk,
                            s > 0 ? 1u : 0u);
-                // this CTA's 32 rope columns: the [64c, 64c + 64) bytes of each rope row
 #pragma unroll
-                for (int s = 0; s < 2; ++s)
-                    mma_ts(tS, tQ + 8 * (16 + s), d0 + (uint64_t)((4 * kChunkBytes + 64 * c + 32 * s) >> 4), idesc_qk,
-                           1u);
-                mma_commit(&bar->s_full);
+                for (int s = 0; s < 2; ++s)  // this CTA's 32 rope columns: bytes [64c, 64c + 64) of each row
+                    mma_ss(tS, dq + (uint64_t)((64 * c + 32 * s) >> 4),
+                           d0 + (uint64_t)((4 * kChunkBytes + 64 * c + 32 * s) >> 4), idesc_qk, 1u);
+                mma_commit(&bar->s_full[i & 1]);
                 issued_any = true;
-                if (i > 0 && !issue_pv(i - 1)) {
+                return true;
+            };
+            bool ok = mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort) &&
+                      mbar_wait(&bar->qrope_full, 0, status, kStatusTimeout, abort);
+            for (int i = 0; ok && i < ntiles && i < 2; ++i) ok = issue_qk(i);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                // O += P(i) . V(i): P from TMEM (the first 32 columns of SP[i % 2]),
+                // V read MN-major from tile i's stage
+                const int u = i & 1;
+                if (!mbar_wait(&bar->p_full[u], (i >> 1) & 1, status, kStatusTimeout, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t dv =
+                    smem_desc(smem_u32(stages + (i % kStages) * kStageBytes), kChunkBytes, 1024, kSwizzle128B);
+                const uint32_t tP = tmem + kColSP + 64 * u;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tO, tP + 8 * s, dv + (uint64_t)((2048 * s) >> 4), idesc_pv, (i > 0 || s > 0) ? 1u : 0u);
+                mma_commit(&bar->pv_done[u]);
+                mma_commit(&bar->kv_empty[i % kStages]);
+                // the MMAs run in issue order: QK(i + 2) overwrites SP[u] after PV(i) has read P(i)
+                if (i + 2 < ntiles && !issue_qk(i + 2)) {
                     ok = false;
                     break;
                 }
             }
-            if (ok && ntiles > 0 && !*abort) issue_pv(ntiles - 1);
             if (issued_any) mma_commit(&bar->mma_done);
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------- exchange warpgroup
+        // Thread h: row h of S_c of every tile, to the peer's receive slot.
+        const int h = tid - 256;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t peer_slots = map_to_cta(slots, peer);
+        const uint32_t peer_xfull = map_to_cta(&bar->xfull[0], peer);  // slot u's barrier is 8u bytes further
+        for (int i = 0; i < ntiles; ++i) {
+            const int u = i & 1;
+            if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (i >> 1) & 1, status, kStatusTimeout, abort))) break;
+            tc_fence_after();
+            uint32_t row[64];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t v[16];
+                tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * k, v);
+                tmem_wait_ld();
+                pin(v);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) row[16 * k + q] = v[q];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->s_read[u]);
+            // the peer grants slot u once it has consumed the message before
+            if (!__all_sync(kAll, mbar_wait<true>(&bar->credit[u], (i >> 1) & 1, status, kStatusTimeout, abort)))
+                break;
+            if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
+            const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
+            const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                st_async_v4(dst + k * 128 * 16,
+                            make_float4(__uint_as_float(row[4 * k]), __uint_as_float(row[4 * k + 1]),
+                                        __uint_as_float(row[4 * k + 2]), __uint_as_float(row[4 * k + 3])),
+                            xb);
         }
     } else {
         // ------------------------------------------- softmax, two warpgroups
         // Thread (h, g): head h = TMEM lane h (warp w reaches lanes 32 (w % 4)
         // onwards), token half g = w / 4 of every tile (S columns [32g, 32g +
-        // 32)), output columns [128g, 128g + 128) of O_c.
+        // 32), P columns [16g, 16g + 16)), output columns [128g, 128g + 128).
         const int h = tid & 127, g = tid >> 7;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t peer_credit = map_to_cta(&bar->credit[0], peer);   // slot u's is 8u bytes further
+        const uint32_t peer_cword = map_to_cta(&bar->credit_word[0], peer);
         if (g == 0) {
-            // Q_c into tensor memory: latent columns [256c, 256c + 256) then
-            // rope columns [512 + 32c, 544 + 32c), as 144 32-bit pairs.  The
-            // latent part goes through ring stages 2-3 (unused until q_full):
-            // each warp copies its 32 rows with coalesced 16-byte cp.async
-            // (row h at h*512, 16-byte chunk k at position k ^ (h % 32), so
-            // that both the copy and the per-thread row reads are free of
-            // bank conflicts), then every thread moves its row into its lane.
-            const bool live = h < p.H;
-            uint8_t* qs = stages + 2 * kStageBytes;
+            // Q_c's latent columns [256c, 256c + 256) into tensor memory,
+            // staged through the receive slots (the peer may send only once
+            // they are granted, below): each warp copies its 32 rows with
+            // coalesced 16-byte cp.async (row h at h*512, 16-byte chunk k at
+            // position k ^ (h % 32): no bank conflicts on either side), then
+            // every thread moves its row into its lane.
             const unsigned char* qbase = p.q + (int64_t)b * p.q_sb + 512 * (int64_t)c;
-            uint4 rope[4];
-            {
-                const uint4* qr = reinterpret_cast<const uint4*>(p.q + (int64_t)b * p.q_sb + (int64_t)h * p.q_sh +
-                                                                 2 * (512 + 32 * (int)c));
-#pragma unroll
-                for (int v = 0; v < 4; ++v) rope[v] = live ? __ldg(qr + v) : make_uint4(0u, 0u, 0u, 0u);
-            }
             for (int j = 0; j < 32; ++j) {
                 const int row = 32 * warp + j;
-                uint4* dst = reinterpret_cast<uint4*>(qs + row * 512 + 16 * (lane ^ (row & 31)));
+                uint4* dst = reinterpret_cast<uint4*>(slots + row * 512 + 16 * (lane ^ (row & 31)));
                 if (row < p.H)
                     cp_async_cg16(dst, qbase + (int64_t)row * p.q_sh + 16 * lane);
                 else
@@ -283,7 +351,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 uint32_t w[16];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(qs + h * 512 + 16 * ((4 * gq + v) ^ (h & 31)));
+                    const uint4 x = *reinterpret_cast<const uint4*>(slots + h * 512 + 16 * ((4 * gq + v) ^ (h & 31)));
                     w[4 * v] = x.x;
                     w[4 * v + 1] = x.y;
                     w[4 * v + 2] = x.z;
@@ -291,33 +359,25 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 }
                 tmem_st16(tmem + kColQ + lane_off + 16 * gq, w);
             }
-            {
-                uint32_t w[16];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    w[4 * v] = rope[v].x;
-                    w[4 * v + 1] = rope[v].y;
-                    w[4 * v + 2] = rope[v].z;
-                    w[4 * v + 3] = rope[v].w;
-                }
-                tmem_st16(tmem + kColQ + lane_off + 16 * 8, w);
-            }
             tmem_wait_st();
             tc_fence_before();
-            fence_proxy_async_smem();  // the staging reads come before the TMA writes that reuse it
-            mbar_arrive(&bar->q_full);  // also frees ring stages 2-3 for the latent tiles
+            fence_proxy_async_smem();  // the staging reads come before the peer's writes into the slots
+            mbar_arrive(&bar->q_full);
+            if (tid == 0 &&
+                mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort)) {  // every row read: grant both slots
+                st_async_b32(peer_cword, 1u, peer_credit);
+                st_async_b32(peer_cword + 4u, 1u, peer_credit + 8u);
+            }
         }
-        const uint32_t peer = c ^ 1u;
-        const uint32_t peer_xbuf = map_to_cta(xbuf, peer);
-        const uint32_t peer_xfull = map_to_cta(&bar->xfull[0], peer);  // slot x's barrier is 8x bytes further
         const float scale2 = p.sm_scale * kLog2eF;
         float m_used = -INFINITY, l = 0.f;
         // tcgen05.ld / st are warp-collective: every wait's outcome is made
         // warp-uniform so that the lanes of a warp leave the loop together
-        const unsigned kAll = 0xffffffffu;
         bool ok = true;
         for (int i = 0; i < ntiles && ok; ++i) {
-            if (!__all_sync(kAll, mbar_wait(&bar->s_full, i & 1, status, kStatusTimeout, abort))) {
+            const int u = i & 1;
+            // the own half of S(i) from tensor memory, the peer's from slot u
+            if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
                 ok = false;
                 break;
             }
@@ -325,36 +385,18 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             float own[kHalf];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                uint32_t u[16];
-                tmem_ld16(tmem + kColS + kHalf * g + lane_off + 16 * k, u);
+                uint32_t v[16];
+                tmem_ld16(tmem + kColSP + 64 * u + kHalf * g + lane_off + 16 * k, v);
                 tmem_wait_ld();
-                pin(u);
+                pin(v);
 #pragma unroll
-                for (int q = 0; q < 16; ++q) own[16 * k + q] = __uint_as_float(u[q]);
+                for (int q = 0; q < 16; ++q) own[16 * k + q] = __uint_as_float(v[q]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->s_free);
-            // exchange the partial scores with the peer CTA: this thread's row
-            // half goes straight into the peer's receive slot i % 2 by
-            // st.async, counted on the peer's barrier.  The slot is free: the
-            // peer sends tile i + 1 only after all of this CTA's tile-i rows
-            // arrived, and each thread sends its tile-i row only after it read
-            // tile i - 2's.
-            const int slot = i & 1;
-            {
-                const uint32_t dst = peer_xbuf + (uint32_t)(slot * kXbufBytes + (8 * g * 128 + h) * 16);
-                const uint32_t xbar = peer_xfull + 8u * (uint32_t)slot;
-#pragma unroll
-                for (int k = 0; k < kHalf / 4; ++k)
-                    st_async_v4(dst + k * 128 * 16,
-                                make_float4(own[4 * k], own[4 * k + 1], own[4 * k + 2], own[4 * k + 3]), xbar);
-            }
-            if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[slot], (i >> 1) & 1, status, kStatusTimeout, abort))) {
+            if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
                 ok = false;
                 break;
             }
-            const float4* xin = xbuf + slot * (kXbufBytes / 16) + 8 * g * 128;
+            const float4* xin = xbuf + u * (kXbufBytes / 16) + 8 * g * 128;
             const int valid = t1 - (t0 + i * kTileTokens) - kHalf * g;  // tokens of this half still in the split
             float s[kHalf];
             float mt = -INFINITY;
@@ -371,9 +413,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                     mt = fmaxf(mt, s[t]);
                 }
             }
-            // re-arm the slot for tile i + 2 (the peer sends it only after
-            // this CTA's tile i + 1, i.e. after this point)
-            if (tid == 0) mbar_arrive_expect_tx(&bar->xfull[slot], kXbufBytes);
             // the row max of the whole tile: this thread's half and the other
             // warpgroup's (through shared memory, written once the other
             // warpgroup has read the previous tile's value)
@@ -389,14 +428,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             }
             const float mt_all = fmaxf(mt, bar->red[g ^ 1][h]);
             mbar_arrive(&bar->red_free);
+            if (tid == 0) {
+                // every softmax thread has read slot u (before its red_full
+                // arrival): re-arm it for tile i + 2 and grant it back to the peer
+                mbar_arrive_expect_tx(&bar->xfull[u], kXbufBytes);
+                st_async_b32(peer_cword + 4u * (uint32_t)u, 1u, peer_credit + 8u * (uint32_t)u);
+            }
             const float m_new = fmaxf(m_used, mt_all);
             const bool move = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
-            // P and O are free once the previous tile's P.V has completed
-            if (i > 0 && !__all_sync(kAll, mbar_wait(&bar->pv_done, (i - 1) & 1, status, kStatusTimeout, abort))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
             if (valid < kHalf) {
                 // rows past the split's last token were loaded from the cache
                 // as they are (stale values, possibly NaN): zero their value
@@ -419,19 +458,30 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             }
             if (i > 0 && __any_sync(kAll, move)) {
                 // rescale this thread's 128 columns of O row h (alpha = 1 for
-                // rows that keep their max)
+                // rows that keep their max) once P.V of tile i - 1 has completed
+                if (!__all_sync(kAll, mbar_wait(&bar->pv_done[u ^ 1], ((i - 1) >> 1) & 1, status, kStatusTimeout,
+                                                abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 for (int k = 0; k < 8; ++k) {
-                    uint32_t u[16];
-                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
+                    uint32_t v[16];
+                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
                     tmem_wait_ld();
-                    pin(u);
+                    pin(v);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) u[q] = __float_as_uint(__uint_as_float(u[q]) * alpha);
-                    tmem_st16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
+                    for (int q = 0; q < 16; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * alpha);
+                    tmem_st16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
                 }
             }
-            // P = 2^(s - m) in the payload type; the row sum in fp32 (a row
-            // whose scores so far are all -inf has m = -inf and p = 0)
+            // P = 2^(s - m) in the payload type into SP[u] columns [16g, 16g +
+            // 16), over scores already read: the other warpgroup's (it passed
+            // red_full) and the exchange warpgroup's (s_read)
+            if (!__all_sync(kAll, mbar_wait(&bar->s_read[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
+                ok = false;
+                break;
+            }
             const float msub = m_used == -INFINITY ? 0.f : m_used;
             {
                 uint32_t w[16];
@@ -442,15 +492,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                     l += pa + pb;
                     w[q] = pack_pair<T>(pa, pb);
                 }
-                tmem_st16(tmem + kColP + 16 * g + lane_off, w);
+                tmem_st16(tmem + kColSP + 64 * u + 16 * g + lane_off, w);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->p_full);
+            if (lane == 0) mbar_arrive(&bar->p_full[u]);
         }
         if (ok && ntiles > 0)
-            ok = __all_sync(kAll, mbar_wait(&bar->pv_done, (ntiles - 1) & 1, status, kStatusTimeout, abort));
+            ok = __all_sync(kAll, mbar_wait(&bar->pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, status,
+                                            kStatusTimeout, abort));
         tc_fence_after();
         // ----------------------------------------------------------- epilogue
         // the row sum is the two warpgroups' partial sums (both relative to
@@ -478,19 +529,19 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             unsigned char* orow =
                 p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + 2 * (256 * c + 128 * g);
             for (int k = 0; k < 8; ++k) {
-                uint32_t u[16];
+                uint32_t v[16];
                 if (have) {
-                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
+                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
                     tmem_wait_ld();
-                    pin(u);
+                    pin(v);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) u[q] = 0u;
+                    for (int q = 0; q < 16; ++q) v[q] = 0u;
                 }
                 uint32_t w[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    w[q] = pack_pair<T>(__uint_as_float(u[2 * q]) * inv, __uint_as_float(u[2 * q + 1]) * inv);
+                    w[q] = pack_pair<T>(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
                 if (live) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
                     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -503,21 +554,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             const int64_t row = (((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split;
             float4* dst = reinterpret_cast<float4*>(p.ws_o + row * 512 + 256 * c + 128 * g);
             for (int k = 0; k < 8; ++k) {
-                uint32_t u[16];
+                uint32_t v[16];
                 if (have) {
-                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, u);
+                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
                     tmem_wait_ld();
-                    pin(u);
+                    pin(v);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) u[q] = 0u;
+                    for (int q = 0; q < 16; ++q) v[q] = 0u;
                 }
                 if (live) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        dst[4 * k + q] = make_float4(__uint_as_float(u[4 * q]) * inv, __uint_as_float(u[4 * q + 1]) * inv,
-                                                     __uint_as_float(u[4 * q + 2]) * inv,
-                                                     __uint_as_float(u[4 * q + 3]) * inv);
+                        dst[4 * k + q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                                     __uint_as_float(v[4 * q + 2]) * inv,
+                                                     __uint_as_float(v[4 * q + 3]) * inv);
                 }
             }
             if (live && c == 0 && g == 0) p.ws_lse[row] = lse2;
@@ -528,7 +579,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         if (lane == 0 && issued_any) {
             // every MMA this CTA issued has completed before its tensor memory goes
             const uint64_t t_start = global_timer_ns();
@@ -614,7 +665,7 @@ EncodeTiledFn encode_fn() {
 }
 
 template <typename T>
-cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, cudaStream_t stream) {
+cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, const CUtensorMap& qmap, cudaStream_t stream) {
     // the shared-memory opt-in is a per-device function attribute
     const cudaError_t attr_err =
         cudaFuncSetAttribute((const void*)mla_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -633,7 +684,7 @@ cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, cudaStream_
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = DCP_PDL ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<T>, map, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<T>, map, qmap, p);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const int64_t rows = (int64_t)p.N * p.B * p.H;
     MlaParams q = p;
@@ -647,18 +698,32 @@ cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, cudaStream_
 cudaError_t launch_mla_decode(const MlaParams& p, int dtype, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    // the latent cache as a 4-D tensor [N][B][Lc][576] (elements, then byte strides)
-    CUtensorMap map;
-    const cuuint64_t dims[4] = {576, (cuuint64_t)(p.lcap > 0 ? p.lcap : 1), (cuuint64_t)p.B, (cuuint64_t)p.N};
-    const cuuint64_t strides[3] = {(cuuint64_t)p.kv_st, (cuuint64_t)p.kv_sb, (cuuint64_t)p.kv_sn};
-    const cuuint32_t box[4] = {64, kTileTokens, 1, 1};
+    const CUtensorMapDataType dt = dtype == DCP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult rc = enc(&map, dtype == DCP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                            4, const_cast<unsigned char*>(p.kv), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // a dimension of extent 1 is never stepped over: give it a nominal stride
+    auto stride = [](int64_t extent, int64_t bytes, int64_t nominal) -> cuuint64_t {
+        return (cuuint64_t)(extent > 1 ? bytes : nominal);
+    };
+    // the latent cache as a 4-D tensor [N][B][Lc][576] (elements, then byte strides)
+    CUtensorMap map, qmap;
+    const int64_t lc = p.lcap > 0 ? p.lcap : 1;
+    const cuuint64_t dims[4] = {576, (cuuint64_t)lc, (cuuint64_t)p.B, (cuuint64_t)p.N};
+    const cuuint64_t strides[3] = {stride(lc, p.kv_st, 1152), stride(p.B, p.kv_sb, 1152), stride(p.N, p.kv_sn, 1152)};
+    const cuuint32_t box[4] = {64, kTileTokens, 1, 1};
+    CUresult rc = enc(&map, dt, 4, const_cast<unsigned char*>(p.kv), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (rc != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    return dtype == DCP_F16 ? launch_mla_t<__half>(p, map, stream) : launch_mla_t<__nv_bfloat16>(p, map, stream);
+    // the absorbed queries as a 3-D tensor [B][H][576]: the rope tile is rows
+    // [0, 128) at column 512 (rows past H read 0)
+    const cuuint64_t qdims[3] = {576, (cuuint64_t)p.H, (cuuint64_t)p.B};
+    const cuuint64_t qstrides[2] = {stride(p.H, p.q_sh, 1152), stride(p.B, p.q_sb, 1152)};
+    const cuuint32_t qbox[3] = {64, 128, 1};
+    rc = enc(&qmap, dt, 3, const_cast<unsigned char*>(p.q), qdims, qstrides, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rc != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    return dtype == DCP_F16 ? launch_mla_t<__half>(p, map, qmap, stream)
+                            : launch_mla_t<__nv_bfloat16>(p, map, qmap, stream);
 }
 
 int mla_device_status(bool clear) {

@@ -107,6 +107,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t* bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_4d(void* dst, const void* map, uint64_t* bar, int x, int y, int z, int w) {
     asm volatile(
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
@@ -239,6 +246,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t dst, float4 v, uint32_t bar
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      dst),
                  "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
+}
+// 4 bytes stored into another CTA's shared memory the same way (a credit or a
+// flag whose arrival is all that matters).
+__device__ __forceinline__ void st_async_b32(uint32_t dst, uint32_t v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst), "r"(v),
+                 "r"(bar)
                  : "memory");
 }
 // Ampere-style asynchronous 16-byte copy global -> this CTA's shared memory.
