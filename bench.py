@@ -476,7 +476,7 @@ def setup_decode_attention(device, split_tokens=1024, batch=None, name="mha_deco
             "bytes": [algo]}
 
 
-def setup_mla_attention(device, split_tokens=1024, batch=None, max_len=None):
+def setup_mla_attention(device, split_tokens=2048, batch=None, max_len=None):
     """Each rank's absorbed-MLA decode attention (the step whose outputs the
     MLA decode merge takes), on the tensor cores."""
     import torch

@@ -722,6 +722,7 @@ dcp_status_t dcp_decode_attention_mla(int dtype, int N, int B, int H, int Dk, in
     const size_t rows = (size_t)N * B * H * nsplit;
     p.ws_o = need ? (float*)workspace : nullptr;
     p.ws_lse = need ? (float*)workspace + rows * Dv : nullptr;
+    p.stall_loads = 0;
     const cudaError_t le = dcp::launch_mla_decode(p, dtype, (cudaStream_t)stream);
     if (le == cudaErrorNotSupported)
         return fail(DCP_ERR_CUDA, "%s: the driver offers no tensor-map encoder (cuTensorMapEncodeTiled)", who);

@@ -40,6 +40,7 @@
 #include <math.h>
 
 #include "dcp_device.cuh"
+#include "dcp_sm100.cuh"
 
 // Tuning knobs (compile-time): use the fixed-shape merge for the common row
 // lengths; use the shifted-chunk merge for 4-byte-aligned rows of those
@@ -55,6 +56,9 @@
 
 #ifndef DCP_COMBINE_STAGED
 #define DCP_COMBINE_STAGED 0
+#endif
+#ifndef DCP_COMBINE_BULK
+#define DCP_COMBINE_BULK 0  // 1: stage 16-byte-aligned rank rows with 1-D cp.async.bulk (an A/B knob)
 #endif
 #ifndef DCP_STAGES
 #define DCP_STAGES 3
@@ -645,6 +649,105 @@ __global__ void __launch_bounds__(kStagedWarps * 32) combine_staged_kernel(const
     pdl_trigger();
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-staged variant (built with -DDCP_COMBINE_BULK=1): each warp keeps a
+// ring of kBulkStages output rows in shared memory; its lane 0 fetches the N
+// rank rows of each (16-byte-aligned rows of 512 x VPL bytes) with one 1-D
+// cp.async.bulk per rank into this CTA's own shared memory, completing on
+// the stage's mbarrier, and the warp merges from shared memory.  The copies
+// occupy no registers and no load slots.  Waits are bounded as everywhere;
+// a wait that runs out makes the warp stop (its rows are then left unwritten).
+// ---------------------------------------------------------------------------
+constexpr int kBulkStages = 3;
+
+template <int NR, int VPL>
+constexpr size_t bulk_smem_bytes() {
+    return (size_t)(kThreads / 32) * (kBulkStages * NR * VPL * 512 + kBulkStages * 8) + 128;
+}
+
+template <typename T, int NR, int VPL, bool SAN>
+__global__ void __launch_bounds__(kThreads, 1) combine_bulk_kernel(const CombineParams p) {
+    pdl_wait();
+    constexpr int ROWB = VPL * 512;
+    constexpr int EPV = 16 / (int)sizeof(T);
+    extern __shared__ uint8_t bsm_raw[];
+    uint8_t* bsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bsm_raw) + 127) & ~uintptr_t(127));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ring = bsm + (size_t)warp * kBulkStages * NR * ROWB;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bsm + (size_t)(kThreads / 32) * kBulkStages * NR * ROWB) +
+                     warp * kBulkStages;
+    if (lane == 0) {
+        for (int s = 0; s < kBulkStages; ++s) sm100::mbar_init(&bars[s], 1);
+        sm100::fence_mbar_init();
+    }
+    __syncwarp();
+    int dummy_status = 0;
+    volatile int stop = 0;
+    const int N = p.N;
+    const bool b2 = p.base2 != 0;
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const int64_t first = (int64_t)blockIdx.x * (kThreads / 32) + warp;
+    RowStep st;
+    st.set(nwarps, p.B, p.Hc);
+    RowCursor icur, ccur;
+    icur.set(first, p.B, p.Hc);
+    ccur = icur;
+    int64_t irow = first;
+    float lq[kBulkStages];
+    auto issue = [&](int slot) {
+        if (irow < p.rows) {
+            const unsigned char* orow = p.o + icur.g * p.o_sg + (int64_t)icur.b * p.o_sb + (int64_t)icur.h * p.o_sh;
+            if (lane == 0) {
+                sm100::mbar_arrive_expect_tx(&bars[slot], (uint32_t)(N * ROWB));
+                for (int j = 0; j < N; ++j)
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            sm100::smem_u32(ring + (slot * NR + j) * ROWB)),
+                        "l"(orow + (int64_t)j * p.o_sn), "r"(ROWB), "r"(sm100::smem_u32(&bars[slot]))
+                        : "memory");
+            }
+            const float* lrow = p.lse + icur.g * p.l_sg + (int64_t)icur.b * p.l_sb + (int64_t)icur.h * p.l_sh;
+            lq[slot] = lane < N ? __ldg(lrow + (int64_t)lane * p.l_sn) : -INFINITY;
+        }
+        irow += nwarps;
+        icur.add(st.dg, st.db, st.dh, p.B, p.Hc);
+    };
+    const LaneGroup lg = lane_group(32);
+#pragma unroll
+    for (int s = 0; s < kBulkStages; ++s) issue(s);
+    for (int64_t row = first, k = 0; row < p.rows; row += nwarps, ++k) {
+        const int slot = (int)(k % kBulkStages);
+        if (!sm100::mbar_wait(&bars[slot], (uint32_t)((k / kBulkStages) & 1), &dummy_status, 1, &stop)) break;
+        float Gl;
+        const float wl = group_weight(lq[slot], lg, 32, b2, Gl);
+        float w[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) w[r] = __shfl_sync(0xffffffffu, wl, r);
+        unsigned char* urow = p.out + ccur.g * p.u_sg + (int64_t)ccur.b * p.u_sb + (int64_t)ccur.h * p.u_sh;
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+            float acc[EPV];
+#pragma unroll
+            for (int i = 0; i < EPV; ++i) acc[i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+                if (j < N)
+                    fma_vec<T, 16, SAN>(acc, *reinterpret_cast<const uint4*>(ring + (slot * NR + j) * ROWB +
+                                                                             (q * 32 + lane) * 16),
+                                        w[j]);
+            st_vec<16>(urow + (int64_t)(q * 32 + lane) * 16, round_vec<T, 16>(acc));
+        }
+        if (p.return_lse && lane == 0)
+            p.out_lse[ccur.g * p.ul_sg + (int64_t)ccur.b * p.ul_sb + (int64_t)ccur.h * p.ul_sh] = Gl;
+        ccur.add(st.dg, st.db, st.dh, p.B, p.Hc);
+        // the merge's reads of this stage come before the next copy into it
+        sm100::fence_proxy_async_smem();
+        __syncwarp();
+        issue(slot);
+    }
+    pdl_trigger();
+}
+
 template <typename T, int NR, bool SAN>
 const void* pick_staged(int vpl, size_t& smem) {
     if (vpl <= 1) {
@@ -658,6 +761,23 @@ const void* pick_staged(int vpl, size_t& smem) {
 template <typename T, int VB, bool SAN>
 cudaError_t launch_combine_vb(const CombineParams& p, cudaStream_t stream) {
     void* args[] = {(void*)&p};
+    if constexpr (VB == 16 && DCP_COMBINE_BULK) {
+        const int rb = p.vec_per_row * 16;
+        if (p.N <= 8 && (rb == 512 || rb == 1024)) {
+            const void* k;
+            size_t smem;
+            if (rb == 512) {
+                k = (const void*)combine_bulk_kernel<T, 8, 1, SAN>;
+                smem = bulk_smem_bytes<8, 1>();
+            } else {
+                k = (const void*)combine_bulk_kernel<T, 8, 2, SAN>;
+                smem = bulk_smem_bytes<8, 2>();
+            }
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            return launch_pdl(k, dim3(device_sm_count()), dim3(kThreads), args, smem, stream);
+        }
+    }
 #if DCP_COMBINE_FIXED
     if constexpr (VB == 4 && DCP_COMBINE_SHIFTED) {
         // 4-byte-aligned rows whose ranks share one misalignment: 16-byte chunks

@@ -103,6 +103,7 @@ struct MlaParams {
     int64_t l_sn, l_sb, l_sh;            // fp32 words
     float* ws_o;                         // [N*B*H*nsplit][512] (nsplit > 1)
     float* ws_lse;                       // [N*B*H*nsplit]
+    int stall_loads;                     // test of the bounded waits: the loads are never issued
 };
 
 // Records `msg` as this host thread's dcp_last_error_message() and returns s.

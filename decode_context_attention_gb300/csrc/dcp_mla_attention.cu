@@ -51,6 +51,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include <mutex>
 #include <type_traits>
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             mbar_arrive_expect_tx(&bar->qrope_full, kQropeBytes);
             tma_load_3d(qrope, &q_map, &bar->qrope_full, 512, 0, b);
             int issued = 0;
-            for (int i = 0; i < ntiles; ++i) {
+            for (int i = 0; i < ntiles && !p.stall_loads; ++i) {
                 const int st = i % kStages, k = i / kStages;
                 if (k > 0 && !mbar_wait(&bar->kv_empty[st], (k - 1) & 1, status, kStatusTimeout, abort)) break;
                 uint8_t* dst = stages + st * kStageBytes;
@@ -695,7 +696,14 @@ cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, const CUten
 
 }  // namespace
 
-cudaError_t launch_mla_decode(const MlaParams& p, int dtype, cudaStream_t stream) {
+cudaError_t launch_mla_decode(const MlaParams& p_in, int dtype, cudaStream_t stream) {
+    MlaParams p = p_in;
+    // DCP_TEST_STALL_LOADS=1 (tests of the failure path only): the kernel
+    // issues none of its latent-row loads, so its first wait on them runs
+    // out; it must then record DCP_ERR_TIMEOUT and end, leaving the context
+    // usable.  Read per call; unset in normal use.
+    const char* stall = getenv("DCP_TEST_STALL_LOADS");
+    p.stall_loads = stall && stall[0] == '1';
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const CUtensorMapDataType dt = dtype == DCP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -230,3 +230,62 @@ def test_mla_refuses_shapes_it_does_not_compile():
     l3 = torch.empty((2, 1, 130), dtype=torch.float32, device=DEV)
     with pytest.raises(binding.DcpError, match="128"):
         binding.decode_attention_mla(q3, kv3, seq3, 10, o3, l3, 0.1)
+
+
+# A process of its own, so that the switch that holds the loads back reaches
+# no other test.
+_STALL_SCRIPT = r'''
+import math, os, sys
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import torch
+import oracle
+from decode_context_attention_gb300 import binding
+
+binding.load()
+dev = "cuda"
+g = torch.Generator(device=dev).manual_seed(5)
+N, B, H, L = 2, 1, 16, 100
+q = torch.randn((B, H, 576), generator=g, device=dev).to(torch.bfloat16)
+kv = torch.randn((N, B, (L + N - 1) // N, 576), generator=g, device=dev).to(torch.bfloat16)
+seq = torch.tensor([L], dtype=torch.int32, device=dev)
+o = torch.empty((N, B, H, 512), dtype=torch.bfloat16, device=dev)
+lse = torch.empty((N, B, H), dtype=torch.float32, device=dev)
+scale = 192 ** -0.5
+# 1: every latent-row load held back, so the first wait on them runs out
+os.environ["DCP_TEST_STALL_LOADS"] = "1"
+binding.decode_attention_mla(q, kv, seq, L, o, lse, scale, base="2")
+torch.cuda.synchronize()
+st = binding.device_status()
+assert st == 7, f"expected DCP_ERR_TIMEOUT, got {st}"
+assert binding.device_status() == 0, "the status must clear once read"
+# 2: the context is still usable and the next call is right
+del os.environ["DCP_TEST_STALL_LOADS"]
+binding.decode_attention_mla(q, kv, seq, L, o, lse, scale, base="2")
+torch.cuda.synchronize()
+assert binding.device_status() == 0
+idx = torch.arange(L, device=dev)
+rows = kv[idx % N, 0, idx // N].double().cpu().numpy()
+want, want_lse = oracle.split_attention_mla(q[0, 3].double().cpu().numpy(), rows, 512, N, scale, base="2")
+got = o[:, 0, 3].double().cpu().numpy()
+assert np.abs(got - want).max() <= 0.02 * np.abs(want).max(), np.abs(got - want).max()
+assert np.abs(lse[:, 0, 3].double().cpu().numpy() - want_lse).max() <= 1e-3
+print("timeout reported, context usable")
+'''
+
+
+def test_mla_wait_that_runs_out_reports_a_timeout_and_leaves_the_context_usable():
+    # every wait of the tensor-core attention is bounded: held-back loads make
+    # the first one run out (after 1 s), which must end the kernel with
+    # DCP_ERR_TIMEOUT in the device status word, not hang it or fault
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    env.pop("DCP_TEST_STALL_LOADS", None)
+    r = subprocess.run([sys.executable, "-c", _STALL_SCRIPT, root], capture_output=True, text=True, timeout=300,
+                       env=env)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "timeout reported, context usable" in r.stdout
