@@ -607,7 +607,11 @@ static dcp_status_t run_attention(const char* who, int dtype, int N, int B, int 
     const size_t rows = (size_t)N * B * H * nsplit;
     p.ws_o = need ? (float*)workspace : nullptr;
     p.ws_lse = need ? (float*)workspace + rows * D : nullptr;
-    return launched(dcp::launch_decode_attention(p, dtype, (cudaStream_t)stream), who);
+    p.stall_loads = 0;
+    cudaError_t le;
+    if (!dcp::launch_decode_attention_tc(p, dtype, (cudaStream_t)stream, &le))
+        le = dcp::launch_decode_attention(p, dtype, (cudaStream_t)stream);
+    return launched(le, who);
 }
 
 dcp_status_t dcp_decode_attention(int dtype, int N, int B, int H, int Hkv, int D,
@@ -730,7 +734,9 @@ dcp_status_t dcp_decode_attention_mla(int dtype, int N, int B, int H, int Dk, in
 }
 
 dcp_status_t dcp_device_status(void) {
-    const int s = dcp::mla_device_status(true);
+    const int s_mla = dcp::mla_device_status(true);
+    const int s_gqa = dcp::attn_tc_device_status(true);
+    const int s = s_mla < 0 || s_gqa < 0 ? -1 : (s_mla ? s_mla : s_gqa);
     if (s < 0) return fail(DCP_ERR_CUDA, "dcp_device_status: the device status word could not be read");
     if (s) return fail((dcp_status_t)s, "dcp_device_status: a tensor-core kernel gave up on a bounded wait");
     return ok();

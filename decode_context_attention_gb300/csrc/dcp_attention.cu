@@ -605,6 +605,16 @@ __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const
     pdl_trigger();
 }
 
+template <typename T, int D>
+static cudaError_t launch_split_merge(const AttnParams& p, cudaStream_t stream) {
+    AttnParams q = p;
+    void* args[] = {(void*)&q};
+    const int64_t rows = (int64_t)p.N * p.B * p.H;
+    const unsigned mgrid = (unsigned)((rows + kAttnThreads / 32 - 1) / (kAttnThreads / 32));
+    return launch_pdl((const void*)decode_merge_splits_kernel<T, D>, dim3(mgrid), dim3(kAttnThreads), args, 0,
+                      stream);
+}
+
 template <typename T, int D, bool PAGED>
 static cudaError_t launch_attention_dp(const AttnParams& p, cudaStream_t stream) {
     const void* k;
@@ -640,10 +650,7 @@ static cudaError_t launch_attention_dp(const AttnParams& p, cudaStream_t stream)
     const dim3 grid((unsigned)((int64_t)p.N * p.B * p.Hkv * p.nsplit));  // split fastest
     cudaError_t e = launch_pdl(k, grid, dim3(kAttnThreads), args, 0, stream);
     if (e != cudaSuccess || p.nsplit == 1) return e;
-    const int64_t rows = (int64_t)p.N * p.B * p.H;
-    const unsigned mgrid = (unsigned)((rows + kAttnThreads / 32 - 1) / (kAttnThreads / 32));
-    return launch_pdl((const void*)decode_merge_splits_kernel<T, D>, dim3(mgrid), dim3(kAttnThreads), args, 0,
-                      stream);
+    return launch_split_merge<T, D>(p, stream);
 }
 
 template <typename T, int D>
@@ -664,6 +671,15 @@ static cudaError_t launch_attention_t(const AttnParams& p, cudaStream_t stream) 
 
 cudaError_t launch_decode_attention(const AttnParams& p, int dtype, cudaStream_t stream) {
     return dtype == 1 ? launch_attention_t<__half>(p, stream) : launch_attention_t<__nv_bfloat16>(p, stream);
+}
+
+cudaError_t launch_attention_split_merge(const AttnParams& p, int dtype, cudaStream_t stream) {
+    switch (p.D) {
+        case 64: return dtype == 1 ? launch_split_merge<__half, 64>(p, stream) : launch_split_merge<__nv_bfloat16, 64>(p, stream);
+        case 128: return dtype == 1 ? launch_split_merge<__half, 128>(p, stream) : launch_split_merge<__nv_bfloat16, 128>(p, stream);
+        case 256: return dtype == 1 ? launch_split_merge<__half, 256>(p, stream) : launch_split_merge<__nv_bfloat16, 256>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace dcp

@@ -80,6 +80,7 @@ struct AttnParams {
     int64_t l_sn, l_sb, l_sh;           // fp32 words
     float* ws_o;                        // [N*B*H*nsplit][D] partial outputs (nsplit > 1)
     float* ws_lse;                      // [N*B*H*nsplit] partial base-2 LSEs
+    int stall_loads;                    // test of the bounded waits (tensor-core path): no loads issued
 };
 
 // Decode attention of every rank over its share of an absorbed-MLA latent
@@ -111,12 +112,22 @@ dcp_status_t set_error(dcp_status_t s, const char* msg);
 
 // Launchers return the launch's cudaGetLastError().
 cudaError_t launch_decode_attention(const AttnParams& p, int dtype, cudaStream_t stream);
+// The tensor-core (tcgen05) path of the same attention, for the shapes it
+// takes (D = 128, 2 to 16 query heads per KV head, split_tokens a multiple of
+// 128, pages of at least 8 tokens, strides a tensor map can describe):
+// returns false without launching anything otherwise, else true with the
+// launches' error in *err.  With splits it also runs the split merge.
+bool launch_decode_attention_tc(const AttnParams& p, int dtype, cudaStream_t stream, cudaError_t* err);
+// The merge of the fp32 split partials into (O, lse) (nsplit > 1).
+cudaError_t launch_attention_split_merge(const AttnParams& p, int dtype, cudaStream_t stream);
 // cudaErrorNotSupported when the driver offers no tensor-map encoder.
 cudaError_t launch_mla_decode(const MlaParams& p, int dtype, cudaStream_t stream);
-// The tensor-core kernels' device status word (0, or the status of the first
-// bounded wait that ran out), read synchronously and optionally cleared;
-// -1 when it cannot be read.
+// The device status words of the tcgen05 kernels (the MLA attention's, the
+// grouped-query attention's): 0, or the status of the first bounded wait
+// that ran out; read synchronously and optionally cleared; -1 when it cannot
+// be read.
 int mla_device_status(bool clear);
+int attn_tc_device_status(bool clear);
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_combine_f32(const CombineParams& p, int vb, cudaStream_t stream);
 cudaError_t launch_combine_f16(const CombineParams& p, int vb, cudaStream_t stream);

@@ -53,7 +53,6 @@
 #include <math.h>
 #include <stdlib.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "dcp_device.cuh"
@@ -645,26 +644,6 @@ __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p
     pdl_trigger();
 }
 
-// cuTensorMapEncodeTiled, looked up from the driver once (no link-time
-// dependency on libcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-std::once_flag g_encode_once;
-EncodeTiledFn g_encode = nullptr;
-
-EncodeTiledFn encode_fn() {
-    std::call_once(g_encode_once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return g_encode;
-}
-
 template <typename T>
 cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, const CUtensorMap& qmap, cudaStream_t stream) {
     // the shared-memory opt-in is a per-device function attribute
@@ -704,7 +683,7 @@ cudaError_t launch_mla_decode(const MlaParams& p_in, int dtype, cudaStream_t str
     // usable.  Read per call; unset in normal use.
     const char* stall = getenv("DCP_TEST_STALL_LOADS");
     p.stall_loads = stall && stall[0] == '1';
-    EncodeTiledFn enc = encode_fn();
+    const EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const CUtensorMapDataType dt = dtype == DCP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint32_t estr[4] = {1, 1, 1, 1};

@@ -1,7 +1,8 @@
 // dcp_sm100.cuh -- thin wrappers over the sm_100-family PTX that the
 // tensor-core attention uses: mbarriers with bounded waits, TMA tile loads,
 // tcgen05 (tensor-memory allocation, MMA, loads and stores, fences) and
-// cluster shared memory.  Header-only, device code only.
+// cluster shared memory; and, for the host, the driver's tensor-map encoder.
+// Header-only.
 //
 // Tensor memory (TMEM) addresses are 32 bits: lane in bits 31..16, column in
 // bits 15..0.  An MMA with M = 128 keeps row i of its fp32 accumulator in lane
@@ -10,8 +11,11 @@
 // reaches lanes [32 (w % 4), 32 (w % 4) + 32) only.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 namespace dcp {
 namespace sm100 {
@@ -119,6 +123,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* map, uint64_t
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
         "%5}], [%6];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* map, uint64_t* bar, int c0, int c1, int c2, int c3,
+                                            int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -271,6 +284,25 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// cuTensorMapEncodeTiled, looked up from the driver once per process (no
+// link-time dependency on libcuda); nullptr when the driver offers none.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+inline EncodeTiledFn tensor_map_encoder() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
 }
 
 }  // namespace sm100
