@@ -115,6 +115,18 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
     }
 }
 
+// A float rounded to the payload type, as its 16 bits; and back.
+template <typename T>
+__device__ __forceinline__ uint32_t to_bits16(float x) {
+    if constexpr (std::is_same<T, __half>::value) return __half_as_ushort(__float2half_rn(x));
+    else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <typename T>
+__device__ __forceinline__ float from_bits16(uint32_t b) {
+    if constexpr (std::is_same<T, __half>::value) return __half2float(__ushort_as_half((unsigned short)b));
+    else return __bfloat162float(__ushort_as_bfloat16((unsigned short)b));
+}
+
 // An int whose signed order is the float order (for -inf and finite values):
 // the warp's maximum then takes one redux instruction.
 __device__ __forceinline__ int order_key(float f) {
@@ -167,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int rb = item / p.Hkv;
     const int b = rb % p.B;
     const int r = rb / p.B;
+#if !DCP_PDL
+    const int Lraw = p.seq_lens[b];  // in flight during the set-up below
+#endif
 
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
@@ -197,8 +212,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     tc_fence_after();
     pdl_wait();
-    int L = p.seq_lens[b];
-    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+#if DCP_PDL
+    const int Lraw = p.seq_lens[b];
+#endif
+    const int L = Lraw < 0 ? 0 : (Lraw > p.max_seq_len ? p.max_seq_len : Lraw);
     const int Ll = L / p.N + (r < L % p.N ? 1 : 0);
     const int t0 = split * p.split_tokens;
     const int t1 = min(t0 + p.split_tokens, Ll);
@@ -377,24 +394,32 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld16(tmem + kColS + kN * u + lane_off, v);
             tmem_wait_ld();
             pin(v);
+            // the tile's maximum of each head: over the warp, then lane h < G
+            // takes head h over the four warps and hands it to every lane
             float s[GQ];
+            float wmax = -INFINITY;  // lane h: this warp's maximum of head h
 #pragma unroll
             for (int h = 0; h < GQ; ++h) {
                 s[h] = valid ? __uint_as_float(v[h]) * qscale : -INFINITY;
                 const int key = __reduce_max_sync(kAll, order_key(s[h]));
-                if (lane == 0) bar->red[u][wq][h] = from_order_key(key);
+                if (lane == h) wmax = from_order_key(key);
             }
+            if (lane < GQ) bar->red[u][wq][lane] = wmax;
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar->red_full[u]);
             if (!__all_sync(kAll, mbar_wait(&bar->red_full[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
                 ok = false;
                 break;
             }
+            float m4 = -INFINITY;
+            if (lane < GQ)
+                m4 = fmaxf(fmaxf(bar->red[u][0][lane], bar->red[u][1][lane]),
+                           fmaxf(bar->red[u][2][lane], bar->red[u][3][lane]));
             float mt[GQ];
             bool grow = false;
 #pragma unroll
             for (int h = 0; h < GQ; ++h) {
-                mt[h] = fmaxf(fmaxf(bar->red[u][0][h], bar->red[u][1][h]), fmaxf(bar->red[u][2][h], bar->red[u][3][h]));
+                mt[h] = __shfl_sync(kAll, m4, h);
                 grow |= mt[h] > m_run[h] + kRescaleLog2;
             }
             if (grow) {  // every thread takes this branch together (same maxima)
@@ -441,21 +466,28 @@ __global__ void __launch_bounds__(kThreads, 2)
                 ok = false;
                 break;
             }
-            // lanes 2x and 2x + 1 hold neighbouring tokens: each writes the
-            // 4-byte pairs of the two (P_hi, then P_lo) for every other head
+            // this token's P^T column as 16-bit terms: row h < G is P_hi of
+            // head h, row G + h its P_lo
+            uint32_t t16[2 * GQ];
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) {
+                t16[h] = to_bits16<T>(pr[h]);
+                t16[GQ + h] = to_bits16<T>(pr[h] - from_bits16<T>(t16[h]));
+            }
+            // lanes 2x and 2x + 1 hold neighbouring tokens; per store the even
+            // lane writes the pair's 4 bytes of row n, the odd lane those of
+            // row n ^ 4 (n ^ 1 at G = 2): under the 128-byte swizzle the two
+            // rows of 32 tokens then fall in disjoint halves of the banks
             uint8_t* pbuf = ps + (NPBUF == 2 ? u : 0) * PBYTES;
             const int ke = kk & ~1;
+            constexpr int kPair = GQ >= 4 ? 4 : 1;
 #pragma unroll
-            for (int hp = 0; hp < GQ / 2; ++hp) {
-                const float send = (lane & 1) ? pr[2 * hp] : pr[2 * hp + 1];
-                const float recv = __shfl_xor_sync(kAll, send, 1);
-                const int n = 2 * hp + (lane & 1);
-                const float pa = (lane & 1) ? recv : pr[2 * hp];      // token ke
-                const float pb = (lane & 1) ? pr[2 * hp + 1] : recv;  // token ke + 1
-                const uint32_t whi = pack_pair<T>(pa, pb);
-                const float2 hi = unpack2(word_to_pair<T>(whi));
-                *reinterpret_cast<uint32_t*>(pbuf + op_offset(n, ke, PCHUNK)) = whi;
-                *reinterpret_cast<uint32_t*>(pbuf + op_offset(GQ + n, ke, PCHUNK)) = pack_pair<T>(pa - hi.x, pb - hi.y);
+            for (int n = 0; n < 2 * GQ; ++n) {
+                if (n & kPair) continue;
+                const int m = n | kPair;
+                const uint32_t recv = __shfl_xor_sync(kAll, (lane & 1) ? t16[n] : t16[m], 1);
+                const uint32_t w = (lane & 1) ? (recv | (t16[m] << 16)) : (t16[n] | (recv << 16));
+                *reinterpret_cast<uint32_t*>(pbuf + op_offset((lane & 1) ? m : n, ke, PCHUNK)) = w;
             }
             if (tb + kTT > t1) {
                 // the split's last tile: V rows past its end hold other tokens
@@ -512,14 +544,29 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int c = 0; c < 16; ++c) o[16 * g + c] = w[c];
             }
         }
+        // lane h < G: head h's row sum, its reciprocal and base-2 LSE, then
+        // handed to every lane (one reciprocal and logarithm per head)
+        float inv_l = 0.f, lse2 = -INFINITY;
+        int mass_l = 0;
+        if (have && lane < GQ) {
+            float mh = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < GQ; ++h)
+                if (lane == h) mh = m_run[h];
+            const float l = bar->sum[0][lane] + bar->sum[1][lane] + bar->sum[2][lane] + bar->sum[3][lane];
+            if (l > 0.f) {
+                mass_l = 1;
+                inv_l = 1.f / l;
+                lse2 = mh + log2f(l);
+            }
+        }
         const int d = kk;
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
-            const float l = have ? bar->sum[0][h] + bar->sum[1][h] + bar->sum[2][h] + bar->sum[3][h] : 0.f;
-            const bool mass = l > 0.f;
+            const float inv = __shfl_sync(kAll, inv_l, h);
+            const bool mass = __shfl_sync(kAll, mass_l, h) != 0;
             const float acc = __uint_as_float(o[h]) + __uint_as_float(o[GQ + h]);
-            const float val = mass ? acc * (1.f / l) : 0.f;
-            const float lse2 = mass ? m_run[h] + log2f(l) : -INFINITY;
+            const float val = mass ? acc * inv : 0.f;
             const int head = hkv * GQ + h;
             if (p.nsplit == 1) {
                 T* orow = reinterpret_cast<T*>(p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)head * p.o_sh);
