@@ -288,6 +288,14 @@ def unpack_combine(recv, D, out, out_lse=None, base="e", sanitize=False, stream=
     prepare_unpack_combine(recv, D, out, out_lse, base, sanitize, stream)()
 
 
+def _default_workspace(workspace, device, N, B, H, D, max_seq_len, split_tokens):
+    """The caller's workspace, else a fresh one of the size the call needs."""
+    if workspace is not None:
+        return workspace
+    nbytes = dcp_decode_attention_workspace_size(N, B, H, D, int(max_seq_len), int(split_tokens))
+    return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes else None
+
+
 def prepare_decode_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
                              max_seq_len: int, o: torch.Tensor, lse: torch.Tensor, sm_scale: float,
                              base: str = "e", split_tokens: int = 1024,
@@ -296,8 +304,8 @@ def prepare_decode_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
 
     q [B,H,D]; k, v [N,B,Lc,Hkv,D] local caches (token i of rank r = global
     token i*N + r); seq_lens [B] int32 global lengths; o [N,B,H,D], lse [N,B,H].
-    `workspace` (uint8, device) is needed when the local lengths span more than
-    one split; see workspace_bytes()."""
+    `workspace` (uint8, device, workspace_bytes() long): the split partials and
+    the work counters; allocated here when not given."""
     _need_cuda(q, k, v, seq_lens, o, lse, workspace)
     if seq_lens.dtype != torch.int32:
         raise ValueError("seq_lens must be int32")
@@ -305,6 +313,7 @@ def prepare_decode_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
         _inner_ok(t)
     B, H, D = q.shape
     N, _, _, Hkv, _ = k.shape
+    workspace = _default_workspace(workspace, q.device, N, B, H, D, max_seq_len, split_tokens)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = (_dtype_code(q), N, B, H, Hkv, D,
             q.data_ptr(), q.stride(0), q.stride(1),
@@ -336,6 +345,7 @@ def prepare_decode_attention_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pag
         _inner_ok(t)
     B, H, D = q.shape
     N, num_pages, page_size, Hkv, _ = k_pages.shape
+    workspace = _default_workspace(workspace, q.device, N, B, H, D, max_seq_len, split_tokens)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = (_dtype_code(q), N, B, H, Hkv, D,
             q.data_ptr(), q.stride(0), q.stride(1),

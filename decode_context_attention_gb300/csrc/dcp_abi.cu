@@ -608,6 +608,7 @@ static dcp_status_t run_attention(const char* who, int dtype, int N, int B, int 
     p.ws_o = need ? (float*)workspace : nullptr;
     p.ws_lse = need ? (float*)workspace + rows * D : nullptr;
     p.stall_loads = 0;
+    p.merge_multi_only = 0;
     cudaError_t le;
     if (!dcp::launch_decode_attention_tc(p, dtype, (cudaStream_t)stream, &le))
         le = dcp::launch_decode_attention(p, dtype, (cudaStream_t)stream);

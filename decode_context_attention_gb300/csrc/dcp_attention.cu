@@ -573,8 +573,19 @@ __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const
     const int64_t rows = (int64_t)p.N * p.B * p.H;
     const int64_t row = (int64_t)blockIdx.x * (kAttnThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
-    const int S = p.nsplit;
-    const float* lrow = p.ws_lse + row * S;
+    const int h = (int)(row % p.H);
+    const int64_t rb = row / p.H;
+    const int b = (int)(rb % p.B);
+    const int r = (int)(rb / p.B);
+    // only the splits that hold tokens of the row (the others are (0, -inf)
+    // and would drop out; the tensor-core kernel does not write them, and it
+    // writes the result of a row with at most one such split itself)
+    int L = p.seq_lens[b];
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+    const int Ll = local_len(L, p.N, r);
+    const int S = min(p.nsplit, (Ll + p.split_tokens - 1) / p.split_tokens);
+    if (p.merge_multi_only && S <= 1) return;
+    const float* lrow = p.ws_lse + row * p.nsplit;
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) M = fmaxf(M, lrow[s]);
     float Ls = 0.f;
@@ -585,15 +596,11 @@ __global__ void __launch_bounds__(kAttnThreads) decode_merge_splits_kernel(const
         for (int s = 0; s < S; ++s) {
             const float w = exp2f(lrow[s] - M);
             Ls += w;
-            const float* orow = p.ws_o + (row * S + s) * D;
+            const float* orow = p.ws_o + (row * p.nsplit + s) * D;
 #pragma unroll
             for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(w, orow[lane + 32 * i], acc[i]);
         }
     }
-    const int h = (int)(row % p.H);
-    const int64_t rb = row / p.H;
-    const int b = (int)(rb % p.B);
-    const int r = (int)(rb / p.B);
     T* orow = reinterpret_cast<T*>(p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh);
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll

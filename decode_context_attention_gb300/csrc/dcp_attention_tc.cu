@@ -220,6 +220,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int t0 = split * p.split_tokens;
     const int t1 = min(t0 + p.split_tokens, Ll);
     const int ntiles = t1 > t0 ? (t1 - t0 + kTT - 1) / kTT : 0;
+    // splits of this (rank, request) that hold tokens: with at most one the
+    // result goes straight to the outputs (from split 0), else fp32 partials
+    // of the non-empty splits go to the workspace for the split merge
+    const int nse = (Ll + p.split_tokens - 1) / p.split_tokens;
+    const bool direct = p.nsplit == 1 || nse <= 1;
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort = &bar->abort;
     int* status = &g_tc_status;
@@ -568,13 +573,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float acc = __uint_as_float(o[h]) + __uint_as_float(o[GQ + h]);
             const float val = mass ? acc * inv : 0.f;
             const int head = hkv * GQ + h;
-            if (p.nsplit == 1) {
+            if (direct) {
+                if (split > 0) break;  // nothing to write: this split holds no token
                 T* orow = reinterpret_cast<T*>(p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)head * p.o_sh);
                 orow[d] = from_f32<T>(val);
                 if (st == h)
                     p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)head * p.l_sh] =
                         p.base2 ? lse2 : lse2 * kLn2F;
             } else {
+                if (split >= nse) break;  // an empty split: the merge skips it
                 const int64_t row = (((int64_t)r * p.B + b) * p.H + head) * p.nsplit + split;
                 p.ws_o[row * kD + d] = val;
                 if (st == h) p.ws_lse[row] = lse2;
@@ -668,7 +675,11 @@ bool launch_decode_attention_tc(const AttnParams& p, int dtype, cudaStream_t str
     else
         e = paged ? launch_tc_t<__nv_bfloat16, true>(p, maps[0], maps[1], stream)
                   : launch_tc_t<__nv_bfloat16, false>(p, maps[0], maps[1], stream);
-    if (e == cudaSuccess && p.nsplit > 1) e = launch_attention_split_merge(p, dtype, stream);
+    if (e == cudaSuccess && p.nsplit > 1) {
+        AttnParams m = p;
+        m.merge_multi_only = 1;  // rows with one non-empty split were written above
+        e = launch_attention_split_merge(m, dtype, stream);
+    }
     *err = e;
     return true;
 }

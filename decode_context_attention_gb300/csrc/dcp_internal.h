@@ -81,6 +81,7 @@ struct AttnParams {
     float* ws_o;                        // [N*B*H*nsplit][D] partial outputs (nsplit > 1)
     float* ws_lse;                      // [N*B*H*nsplit] partial base-2 LSEs
     int stall_loads;                    // test of the bounded waits (tensor-core path): no loads issued
+    int merge_multi_only;               // split merge: only rows with two or more non-empty splits
 };
 
 // Decode attention of every rank over its share of an absorbed-MLA latent
