@@ -325,6 +325,7 @@ KERNEL_SOURCES = {
     "combine_kernel": ("dcp_combine.cuh", "dcp_combine_bf16.cu", "dcp_device.cuh"),
     "decode_partial_kernel": ("dcp_attention.cu", "dcp_device.cuh"),
     "decode_partial_mma_kernel": ("dcp_attention.cu", "dcp_device.cuh"),
+    "gqa_decode_tc_kernel": ("dcp_attention_tc.cu", "dcp_device.cuh", "dcp_sm100.cuh"),
 }
 
 
