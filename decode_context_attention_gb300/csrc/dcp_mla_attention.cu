@@ -92,7 +92,7 @@ __device__ int g_mla_status;  // first bounded wait that ran out (0 if none)
 
 struct Barriers {
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t q_full, qrope_full, mma_done;
+    uint64_t q_full, qrope_full, qlat_full, mma_done;
     uint64_t s_full[2], s_read[2], p_full[2], pv_done[2];  // per score / probability buffer
     uint64_t xfull[2];   // receive slot: the peer's partial scores arrived (st.async bytes)
     uint64_t credit[2];  // send slot: the peer has freed its receive slot (a st.async credit)
@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         }
         mbar_init(&bar->q_full, 128);
         mbar_init(&bar->qrope_full, 1);
+        mbar_init(&bar->qlat_full, 1);
         mbar_init(&bar->mma_done, 1);
         for (int u = 0; u < 2; ++u) {
             mbar_init(&bar->s_full[u], 1);
@@ -198,7 +199,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     if (warp == 12) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            // the query's rope columns, [128 heads x 64], once (heads past H read 0)
+            // the query's latent columns [256c, 256c + 256) as four [128 heads x
+            // 64] boxes into the receive slots (staging for tensor memory), and
+            // its rope columns, once (heads past H read 0)
+            mbar_arrive_expect_tx(&bar->qlat_full, 4 * 128 * 128);
+            for (int j = 0; j < 4; ++j)
+                tma_load_3d(slots + j * 128 * 128, &q_map, &bar->qlat_full, 256 * (int)c + 64 * j, 0, b);
             mbar_arrive_expect_tx(&bar->qrope_full, kQropeBytes);
             tma_load_3d(qrope, &q_map, &bar->qrope_full, 512, 0, b);
             int issued = 0;
@@ -216,6 +222,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             // copies still in flight (only after an abort) land before the CTA ends
             const uint64_t t_start = global_timer_ns();
             while (!mbar_try_wait(&bar->qrope_full, 0) && global_timer_ns() - t_start < kWaitLimitNs) {
+            }
+            while (!mbar_try_wait(&bar->qlat_full, 0) && global_timer_ns() - t_start < kWaitLimitNs) {
             }
             for (int i = max(0, issued - kStages); i < issued; ++i) {
                 uint64_t* fb = &bar->kv_full[i % kStages];
@@ -328,30 +336,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t peer_credit = map_to_cta(&bar->credit[0], peer);   // slot u's is 8u bytes further
         const uint32_t peer_cword = map_to_cta(&bar->credit_word[0], peer);
-        if (g == 0) {
+        if (g == 0 && __all_sync(kAll, mbar_wait(&bar->qlat_full, 0, status, kStatusTimeout, abort))) {
             // Q_c's latent columns [256c, 256c + 256) into tensor memory,
-            // staged through the receive slots (the peer may send only once
-            // they are granted, below): each warp copies its 32 rows with
-            // coalesced 16-byte cp.async (row h at h*512, 16-byte chunk k at
-            // position k ^ (h % 32): no bank conflicts on either side), then
-            // every thread moves its row into its lane.
-            const unsigned char* qbase = p.q + (int64_t)b * p.q_sb + 512 * (int64_t)c;
-            for (int j = 0; j < 32; ++j) {
-                const int row = 32 * warp + j;
-                uint4* dst = reinterpret_cast<uint4*>(slots + row * 512 + 16 * (lane ^ (row & 31)));
-                if (row < p.H)
-                    cp_async_cg16(dst, qbase + (int64_t)row * p.q_sh + 16 * lane);
-                else
-                    *dst = make_uint4(0u, 0u, 0u, 0u);
-            }
-            cp_async_wait_all();
-            __syncwarp();
+            // staged through the receive slots by TMA (the peer may send only
+            // once they are granted, below): four 128-byte-swizzled boxes of
+            // [128 heads x 64 columns], row h of box j at j*16384 + h*128
+            // with 16-byte chunk k at position k ^ (h % 8); every thread moves
+            // its row into its lane, TMEM columns [16gq, 16gq + 16) being
+            // chunks 4gq .. 4gq + 3 of the row.
 #pragma unroll
             for (int gq = 0; gq < 8; ++gq) {
                 uint32_t w[16];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(slots + h * 512 + 16 * ((4 * gq + v) ^ (h & 31)));
+                    const uint4 x = *reinterpret_cast<const uint4*>(slots + (gq >> 1) * 128 * 128 + h * 128 +
+                                                                    (((4 * (gq & 1) + v) ^ (h & 7)) << 4));
                     w[4 * v] = x.x;
                     w[4 * v + 1] = x.y;
                     w[4 * v + 2] = x.z;
@@ -525,53 +524,82 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         const float inv = mass ? 1.f / l_all : 0.f;
         const float lse2 = mass ? m_used + log2f(l_all) : -INFINITY;
         const bool live = h < p.H;
+        // O columns [128g + 16k0, 128g + 16k0 + 64) of this thread's row (zeros when there is none)
+        auto load_o4 = [&](int k0, uint32_t (&v)[4][16]) {
+            if (have) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * (k0 + q4), v[q4]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) pin(v[q4]);
+            } else {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q4][q] = 0u;
+            }
+        };
+        // The rows go out through shared memory: a thread holds one head's
+        // row, so its own stores would put each warp store across 32 rows;
+        // each softmax warp instead writes its 32 rows' 64-column chunk into
+        // 8 KB of the ring (idle once the last P.V has completed: no copy is
+        // in flight then), and stores them back row by row, coalesced.
+        // 16-byte chunk ch of row rr sits at rr * rowb + ((ch ^ (rr % 8)) * 16).
+        uint8_t* stg = stages + warp * 8192;
+        const int h0 = 32 * (warp & 3);  // the warp's first head
         if (p.nsplit == 1) {
-            unsigned char* orow =
-                p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + 2 * (256 * c + 128 * g);
-            for (int k = 0; k < 8; ++k) {
-                uint32_t v[16];
-                if (have) {
-                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
-                    tmem_wait_ld();
-                    pin(v);
-                } else {
+            for (int k0 = 0; k0 < 8; k0 += 4) {  // 64 columns a pass, four loads in flight per wait
+                uint32_t v[4][16];
+                load_o4(k0, v);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = 0u;
-                }
-                uint32_t w[8];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t w[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    w[q] = pack_pair<T>(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
-                if (live) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int q = 0; q < 8; ++q)
+                        w[q] = pack_pair<T>(__uint_as_float(v[q4][2 * q]) * inv, __uint_as_float(v[q4][2 * q + 1]) * inv);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        *reinterpret_cast<uint4*>(stg + lane * 128 + (((2 * q4 + e) ^ (lane & 7)) << 4)) =
+                            make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
                 }
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {  // 4 rows of 128 bytes a store
+                    const int rr = 4 * j + (lane >> 3), cc = lane & 7;
+                    const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
+                    if (h0 + rr < p.H)
+                        *reinterpret_cast<uint4*>(p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb +
+                                                  (int64_t)(h0 + rr) * p.o_sh + 2 * (256 * c + 128 * g + 16 * k0) +
+                                                  16 * cc) = x;
+                }
+                __syncwarp();
             }
             if (live && c == 0 && g == 0)
                 p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] = p.base2 ? lse2 : lse2 * kLn2F;
         } else {
-            const int64_t row = (((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split;
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + row * 512 + 256 * c + 128 * g);
-            for (int k = 0; k < 8; ++k) {
-                uint32_t v[16];
-                if (have) {
-                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
-                    tmem_wait_ld();
-                    pin(v);
-                } else {
+            const int64_t row0 = (((int64_t)r * p.B + b) * p.H + h0) * p.nsplit + split;  // the warp's first head
+            for (int k0 = 0; k0 < 8; k0 += 4) {
+                uint32_t v[4][16];
+                load_o4(k0, v);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = 0u;
-                }
-                if (live) {
+                for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[4 * k + q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                                     __uint_as_float(v[4 * q + 2]) * inv,
-                                                     __uint_as_float(v[4 * q + 3]) * inv);
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<float4*>(stg + lane * 256 + (((4 * q4 + e) ^ (lane & 7)) << 4)) =
+                            make_float4(__uint_as_float(v[q4][4 * e]) * inv, __uint_as_float(v[q4][4 * e + 1]) * inv,
+                                        __uint_as_float(v[q4][4 * e + 2]) * inv, __uint_as_float(v[q4][4 * e + 3]) * inv);
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {  // 2 rows of 256 bytes a store
+                    const int rr = 2 * j + (lane >> 4), cc = lane & 15;
+                    const float4 x = *reinterpret_cast<const float4*>(stg + rr * 256 + ((cc ^ (rr & 7)) << 4));
+                    if (h0 + rr < p.H)
+                        *reinterpret_cast<float4*>(p.ws_o + (row0 + (int64_t)rr * p.nsplit) * 512 + 256 * c + 128 * g +
+                                                   16 * k0 + 4 * cc) = x;
                 }
+                __syncwarp();
             }
-            if (live && c == 0 && g == 0) p.ws_lse[row] = lse2;
+            if (live && c == 0 && g == 0) p.ws_lse[(((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split] = lse2;
         }
     }
 
