@@ -301,16 +301,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             const int u = i & 1;
             if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (i >> 1) & 1, status, kStatusTimeout, abort))) break;
             tc_fence_after();
-            uint32_t row[64];
+            uint32_t row[4][16];  // the four loads in flight together, one wait
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t v[16];
-                tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * k, v);
-                tmem_wait_ld();
-                pin(v);
+            for (int k = 0; k < 4; ++k) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * k, row[k]);
+            tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 16; ++q) row[16 * k + q] = v[q];
-            }
+            for (int k = 0; k < 4; ++k) pin(row[k]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar->s_read[u]);
@@ -323,8 +319,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
 #pragma unroll
             for (int k = 0; k < 16; ++k)
                 st_async_v4(dst + k * 128 * 16,
-                            make_float4(__uint_as_float(row[4 * k]), __uint_as_float(row[4 * k + 1]),
-                                        __uint_as_float(row[4 * k + 2]), __uint_as_float(row[4 * k + 3])),
+                            make_float4(__uint_as_float(row[k >> 2][4 * (k & 3)]),
+                                        __uint_as_float(row[k >> 2][4 * (k & 3) + 1]),
+                                        __uint_as_float(row[k >> 2][4 * (k & 3) + 2]),
+                                        __uint_as_float(row[k >> 2][4 * (k & 3) + 3])),
                             xb);
         }
     } else {
@@ -382,14 +380,17 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             }
             tc_fence_after();
             float own[kHalf];
+            {
+                uint32_t v[2][16];  // both loads in flight, one wait
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                uint32_t v[16];
-                tmem_ld16(tmem + kColSP + 64 * u + kHalf * g + lane_off + 16 * k, v);
+                for (int k = 0; k < 2; ++k) tmem_ld16(tmem + kColSP + 64 * u + kHalf * g + lane_off + 16 * k, v[k]);
                 tmem_wait_ld();
-                pin(v);
 #pragma unroll
-                for (int q = 0; q < 16; ++q) own[16 * k + q] = __uint_as_float(v[q]);
+                for (int k = 0; k < 2; ++k) {
+                    pin(v[k]);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) own[16 * k + q] = __uint_as_float(v[k][q]);
+                }
             }
             if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
                 ok = false;
