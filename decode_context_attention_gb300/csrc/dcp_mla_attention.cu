@@ -29,13 +29,16 @@
 //     columns an A operand in shared memory (a TMA tile), the latent rows the
 //     K-major B operand;
 //   * an exchange warpgroup reads S_c as soon as it is ready and sends it to
-//     the peer CTA with st.async stores that count their bytes on the peer's
-//     mbarrier (no fence); a 4-byte st.async credit from the peer frees each
-//     of its two receive slots again.  Scores are double-buffered in TMEM,
-//     so the exchange of tile i + 1 overlaps the softmax of tile i;
+//     the peer CTA, in log2 units rounded to fp16 (half the bytes of fp32 on
+//     the distributed-shared-memory path that bounds the tile), with st.async
+//     stores that count their bytes on the peer's mbarrier (no fence); a
+//     4-byte st.async credit from the peer frees each of its two receive
+//     slots again.  Scores are double-buffered in TMEM, so the exchange of
+//     tile i + 1 overlaps the softmax of tile i;
 //   * two softmax warpgroups (thread (h, g) = head h = TMEM lane h, tokens
-//     [32g, 32g + 32) of the tile) add the peer's half as S_0 + S_1 in that
-//     order (the same bits in both CTAs) and run an online softmax in base 2
+//     [32g, 32g + 32) of the tile) round their own partial the same way and
+//     add the peer's as S_0 + S_1 in that order (the same bits in both CTAs:
+//     one probability for both halves of the output) and run an online softmax in base 2
 //     with a lazily moved reference max (the output is rescaled only when the
 //     max grows by more than 2^8, so most tiles skip it); P goes to tensor
 //     memory as bf16/fp16, over its tile's consumed scores;
@@ -68,14 +71,18 @@ constexpr int kMlaThreads = 448;   // warps 0-7 softmax, 8-11 exchange, 12 TMA, 
 constexpr int kSoftmaxThreads = 256;
 constexpr int kTileTokens = 64;    // tokens per tile (one ring stage)
 constexpr int kHalf = 32;          // tokens of a tile per softmax warpgroup
-constexpr int kStages = 3;         // shared-memory ring depth
+#ifndef DCP_MLA_STAGES
+#define DCP_MLA_STAGES 3
+#endif
+constexpr int kStages = DCP_MLA_STAGES;  // shared-memory ring depth
 constexpr int kChunkBytes = kTileTokens * 128;      // 64 tokens x 64 columns x 2 bytes
 constexpr int kStageBytes = 5 * kChunkBytes;        // 4 latent chunks + the rope chunk
-constexpr int kXbufBytes = kTileTokens * 128 * 4;   // fp32 partial scores of a tile, 64 tokens x 128 heads
+constexpr int kXbufBytes = kTileTokens * 128 * 2;   // fp16 partial scores of a tile (log2 units), 64 tokens x 128 heads
 constexpr int kQropeBytes = 128 * 128;              // [128 heads x 64 rope columns], 128-byte swizzled
 constexpr int kMiscBytes = 2048;                    // barriers, the warpgroups' row values, credit words
-// the ring, the two receive slots (first the query's staging area), the
-// query's rope tile, the small things
+// the ring, the two receive slots, the query's rope tile, the small things
+// (the query's latent part is staged in the receive slots and the last ring
+// stage before any of them is used)
 constexpr int kSmemBytes = kStages * kStageBytes + 2 * kXbufBytes + kQropeBytes + kMiscBytes + 1024 /* align */;
 // tensor-memory columns
 constexpr uint32_t kColO = 0;      // O_c: 256 fp32 columns
@@ -104,6 +111,19 @@ struct Barriers {
 };
 static_assert(sizeof(Barriers) <= kMiscBytes, "misc region too small");
 
+// Two floats to fp16 (round to nearest, values past the fp16 range to its
+// largest finite, NaN kept), lo in the low half; and back.
+__device__ __forceinline__ uint32_t f16x2_satfinite(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, sizeof(h));
+    return __half22float2(h);
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
     if constexpr (std::is_same<T, __half>::value) {
@@ -131,9 +151,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    uint8_t* slots = smem + kStages * kStageBytes;                           // 2 x [16][128] float4
-    float4* xbuf = reinterpret_cast<float4*>(slots);
+    uint8_t* slots = smem + kStages * kStageBytes;  // 2 x [8 token groups][128 heads] x 8 halves
     uint8_t* qrope = slots + 2 * kXbufBytes;
+    // staging box j of the query's latent columns
+    auto q_stage = [&](int j) -> uint8_t* {
+        return j < 2 ? slots + j * 128 * 128 : stages + (kStages - 1) * kStageBytes + (j - 2) * 128 * 128;
+    };
     Barriers* bar = reinterpret_cast<Barriers*>(qrope + kQropeBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -200,17 +223,20 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             // the query's latent columns [256c, 256c + 256) as four [128 heads x
-            // 64] boxes into the receive slots (staging for tensor memory), and
-            // its rope columns, once (heads past H read 0)
+            // 64] boxes (staging for tensor memory: two in the receive slots,
+            // two in the last ring stage), and its rope columns, once (heads
+            // past H read 0)
             mbar_arrive_expect_tx(&bar->qlat_full, 4 * 128 * 128);
             for (int j = 0; j < 4; ++j)
-                tma_load_3d(slots + j * 128 * 128, &q_map, &bar->qlat_full, 256 * (int)c + 64 * j, 0, b);
+                tma_load_3d(q_stage(j), &q_map, &bar->qlat_full, 256 * (int)c + 64 * j, 0, b);
             mbar_arrive_expect_tx(&bar->qrope_full, kQropeBytes);
             tma_load_3d(qrope, &q_map, &bar->qrope_full, 512, 0, b);
             int issued = 0;
             for (int i = 0; i < ntiles && !p.stall_loads; ++i) {
                 const int st = i % kStages, k = i / kStages;
                 if (k > 0 && !mbar_wait(&bar->kv_empty[st], (k - 1) & 1, status, kStatusTimeout, abort)) break;
+                // the last stage's first tile waits until the query has left it
+                if (k == 0 && st == kStages - 1 && !mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort)) break;
                 uint8_t* dst = stages + st * kStageBytes;
                 mbar_arrive_expect_tx(&bar->kv_full[st], kStageBytes);
                 const int y = t0 + i * kTileTokens;
@@ -295,6 +321,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         // Thread h: row h of S_c of every tile, to the peer's receive slot.
         const int h = tid - 256;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const float scale2x = p.sm_scale * kLog2eF;
         const uint32_t peer_slots = map_to_cta(slots, peer);
         const uint32_t peer_xfull = map_to_cta(&bar->xfull[0], peer);  // slot u's barrier is 8u bytes further
         for (int i = 0; i < ntiles; ++i) {
@@ -314,15 +341,20 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             if (!__all_sync(kAll, mbar_wait<true>(&bar->credit[u], (i >> 1) & 1, status, kStatusTimeout, abort)))
                 break;
             if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
+            // the row in log2 units, rounded to fp16 (saturating, NaN kept) in
+            // token pairs: group k of 8 tokens to slot offset (k * 128 + h) * 16
+            uint32_t hv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                hv[j] = f16x2_satfinite(__uint_as_float(row[(2 * j) >> 4][(2 * j) & 15]) * scale2x,
+                                        __uint_as_float(row[(2 * j + 1) >> 4][(2 * j + 1) & 15]) * scale2x);
             const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
             const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
+            for (int k = 0; k < 8; ++k)
                 st_async_v4(dst + k * 128 * 16,
-                            make_float4(__uint_as_float(row[k >> 2][4 * (k & 3)]),
-                                        __uint_as_float(row[k >> 2][4 * (k & 3) + 1]),
-                                        __uint_as_float(row[k >> 2][4 * (k & 3) + 2]),
-                                        __uint_as_float(row[k >> 2][4 * (k & 3) + 3])),
+                            make_float4(__uint_as_float(hv[4 * k]), __uint_as_float(hv[4 * k + 1]),
+                                        __uint_as_float(hv[4 * k + 2]), __uint_as_float(hv[4 * k + 3])),
                             xb);
         }
     } else {
@@ -336,10 +368,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         const uint32_t peer_cword = map_to_cta(&bar->credit_word[0], peer);
         if (g == 0 && __all_sync(kAll, mbar_wait(&bar->qlat_full, 0, status, kStatusTimeout, abort))) {
             // Q_c's latent columns [256c, 256c + 256) into tensor memory,
-            // staged through the receive slots by TMA (the peer may send only
-            // once they are granted, below): four 128-byte-swizzled boxes of
-            // [128 heads x 64 columns], row h of box j at j*16384 + h*128
-            // with 16-byte chunk k at position k ^ (h % 8); every thread moves
+            // staged by TMA in the receive slots and the last ring stage (the
+            // peer may send only once the slots are granted, below, and the
+            // stage's first tile waits for q_full): four 128-byte-swizzled
+            // boxes of [128 heads x 64 columns], row h of box j at
+            // q_stage(j) + h*128 with 16-byte chunk k at position k ^ (h % 8); every thread moves
             // its row into its lane, TMEM columns [16gq, 16gq + 16) being
             // chunks 4gq .. 4gq + 3 of the row.
 #pragma unroll
@@ -347,7 +380,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 uint32_t w[16];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(slots + (gq >> 1) * 128 * 128 + h * 128 +
+                    const uint4 x = *reinterpret_cast<const uint4*>(q_stage(gq >> 1) + h * 128 +
                                                                     (((4 * (gq & 1) + v) ^ (h & 7)) << 4));
                     w[4 * v] = x.x;
                     w[4 * v + 1] = x.y;
@@ -396,21 +429,28 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 ok = false;
                 break;
             }
-            const float4* xin = xbuf + u * (kXbufBytes / 16) + 8 * g * 128;
+            // the peer's half of this thread's tokens: groups 4g .. 4g + 3 of 8
+            const uint4* xin = reinterpret_cast<const uint4*>(slots + u * kXbufBytes) + 4 * g * 128;
             const int valid = t1 - (t0 + i * kTileTokens) - kHalf * g;  // tokens of this half still in the split
             float s[kHalf];
             float mt = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < kHalf / 4; ++k) {
-                const float4 o4 = xin[k * 128 + h];
-                const float other[4] = {o4.x, o4.y, o4.z, o4.w};
+            for (int k = 0; k < kHalf / 8; ++k) {
+                const uint4 o4 = xin[k * 128 + h];
+                const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int t = 4 * k + q;
-                    // S_0 + S_1 in that order in both CTAs: the same bits on both sides
-                    const float x = (c == 0 ? own[t] + other[q] : other[q] + own[t]) * scale2;
-                    s[t] = t < valid ? x : -INFINITY;
-                    mt = fmaxf(mt, s[t]);
+                    const int t = 8 * k + 2 * q;
+                    // both partial scores in log2 units rounded to fp16 alike,
+                    // then S_0 + S_1 in that order in both CTAs: the same bits
+                    // on both sides
+                    const float2 other = f16x2_to_float2(ow[q]);
+                    const float2 mine = f16x2_to_float2(f16x2_satfinite(own[t] * scale2, own[t + 1] * scale2));
+                    const float x0 = c == 0 ? mine.x + other.x : other.x + mine.x;
+                    const float x1 = c == 0 ? mine.y + other.y : other.y + mine.y;
+                    s[t] = t < valid ? x0 : -INFINITY;
+                    s[t + 1] = t + 1 < valid ? x1 : -INFINITY;
+                    mt = fmaxf(mt, fmaxf(s[t], s[t + 1]));
                 }
             }
             // the row max of the whole tile: this thread's half and the other

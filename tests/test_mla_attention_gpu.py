@@ -13,10 +13,14 @@ probability once to the payload type before the value product (relative
 error <= u, u = 2^-9 for bf16, 2^-12 for fp16), normalises by the fp32 sum
 of the unrounded probabilities, and rounds the output once (<= u relative).
 So |O - O*|_d <= u sum_t w_t |v_td| + u |O*_d| + the effect of score errors.
-The scores are fp32 sums of 576 products: |ds_t| <= 576 * 2^-24 *
-sum_i |q_i kv_ti| * sm_scale =: E (natural-log units), which moves lse by at
-most E and every weight by a factor within exp(+-2E).  The bounds below take
-twice each term.
+The scores are fp32 sums of 576 products, and each of the two CTAs' partial
+scores (latent columns [256c, 256c + 256) plus rope columns [512 + 32c,
+544 + 32c)) crosses to the other CTA rounded to fp16 in log2 units, both
+CTAs rounding alike (relative error <= 2^-11, absolute <= 2^-25 below the
+normal range): |ds_t| <= (576 * 2^-24 * sum_i |q_i kv_ti| + 2^-11 (|S_0t| +
+|S_1t|)) * sm_scale + 2^-24 ln 2, maximised over t =: E (natural-log units),
+which moves lse by at most E and every weight by a factor within
+exp(+-2E).  The bounds below take twice each term.
 """
 import math
 
@@ -60,7 +64,9 @@ def check_row(got_o, got_lse, q, rows_global, r, N, scale, base, u, what, want=N
     conv = math.log(2.0) if base == "2" else 1.0
     own = rows_global[r::N]
     s = own @ q * scale                                     # natural-log units
-    E = DK * 2.0 ** -24 * float((np.abs(own) @ np.abs(q)).max()) * scale
+    part = [np.r_[256 * cc:256 * cc + 256, 512 + 32 * cc:544 + 32 * cc] for cc in (0, 1)]
+    s_half = sum(np.abs(own[:, cols] @ q[cols]) for cols in part)
+    E = float((DK * 2.0 ** -24 * (np.abs(own) @ np.abs(q)) + 2.0 ** -11 * s_half).max()) * scale + 2.0 ** -24 * math.log(2.0)
     w = np.exp(s - want_lse * conv)
     A = w @ np.abs(own[:, :DV])
     tol_o = 2 * (u * A + u * np.abs(want_o) + 2 * E * A) + 1e-6
