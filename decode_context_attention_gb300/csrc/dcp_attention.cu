@@ -22,9 +22,11 @@
 //  * each lane group keeps an online softmax in base 2 (scores pre-scaled by
 //    log2 e, exp2f) per query head, rescaled once per block of 4 tokens whose
 //    K and V loads are all issued first;
-//  * grouped-query heads (2..8 per KV head) instead run the score and output
-//    products on the tensor cores (decode_partial_mma_kernel below), since
-//    their multiply-adds per byte outrun the CUDA cores;
+//  * grouped-query heads (2..16 per KV head) instead run the score and
+//    output products on the tensor cores, since their multiply-adds per byte
+//    outrun the CUDA cores: at D = 128 (split_tokens a multiple of 128,
+//    pages of 8 tokens or more) the tcgen05 kernel of dcp_attention_tc.cu,
+//    otherwise decode_partial_mma_kernel below (warp-level mma.sync);
 //  * the CTA's lane groups merge their states through shared memory; with one
 //    split the CTA writes (O_r, lse_r) directly, otherwise an fp32 partial
 //    (O, lse) per split goes to the caller's workspace and a second kernel

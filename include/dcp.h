@@ -14,7 +14,8 @@
  *                       receive rows in one pass;
  *   dcp_decode_attention  the step before the merge: each rank's decode
  *                       attention over its round-robin share of the KV cache
- *                       (dcp_decode_attention_mla: over an absorbed-MLA
+ *                       (grouped-query heads at D = 128 on the tcgen05 tensor
+ *                       cores; dcp_decode_attention_mla: over an absorbed-MLA
  *                       latent cache, on the tcgen05 tensor cores).
  *
  * The cross-rank exchange itself (NCCL all-to-all, MNNVL, all-gather /
