@@ -22,7 +22,9 @@ Also measured in the same run and reported under "secondary":
   * the MLA decode shape with fp8 e4m3 payloads through the interleaved pack
     (lpd = 4) and the fused unpack+combine;
   * the decode attention that produces the merge's inputs (N = 4 ranks,
-    B = 64 requests, H = 32, D = 128, bf16, lengths up to 16384; ~9 GB of K/V);
+    B = 64 requests, H = 32, D = 128, bf16, lengths up to 16384): one query
+    head per KV head (MHA, ~9 GB of K/V, CUDA cores), and 8 per KV head (GQA,
+    ~1.1 GB, tcgen05), the latter also over 64-token pages;
   * the absorbed-MLA decode attention whose outputs the headline merge takes
     (N = 8, B = 128, H = 128, 576-wide latent rows, 512-wide values, bf16, on
     the tcgen05 tensor cores), in TFLOP/s and GB/s;
