@@ -16,8 +16,9 @@
 //
 // Design.  128 query heads x 512 output columns of fp32 accumulators are
 // 256 KB: all of one SM's tensor memory, with no room left for the scores.
-// So a pair of CTAs (a thread-block cluster of 2) takes one (rank, request,
-// split): CTA c owns output columns [256c, 256c + 256) and, for the scores,
+// So a pair of CTAs (a thread-block cluster of 2) works on one (rank,
+// request, split) item at a time: CTA c owns output columns [256c, 256c +
+// 256) and, for the scores,
 // latent columns [256c, 256c + 256) plus rope columns [512 + 32c, 544 + 32c)
 // -- exactly the columns it loads, so the pair reads every latent byte once
 // and does every multiply-add once.  Per tile of 64 tokens:
@@ -46,7 +47,15 @@
 //     TMEM A operand and V_c read MN-major from the same shared-memory tile.
 // With one split the softmax warps normalise O and write (O_r, lse_r);
 // otherwise fp32 partials go to the workspace and a second kernel merges the
-// splits with the combine's LSE rule.  Every barrier wait is bounded (1 s):
+// splits with the combine's LSE rule.
+//
+// The pairs are persistent: as many as fit on the device at once, each
+// taking its share of the items, longest first, one after the other.  The
+// pipeline runs on across an item boundary -- the next item's query is
+// staged (TMA into a shared-memory area, then into tensor memory) and its
+// first tiles are loaded and scored while the current item's last tiles and
+// its epilogue finish -- so the per-item set-up (barriers, tensor memory,
+// the query, the first tile's latency) is paid once per pair, not per item.  Every barrier wait is bounded (1 s):
 // a wait that runs out records DCP_ERR_TIMEOUT in a device status word and
 // the kernel winds down (its copies and MMAs in flight are waited for, its
 // tensor memory freed) instead of hanging.
@@ -79,11 +88,17 @@ constexpr int kChunkBytes = kTileTokens * 128;      // 64 tokens x 64 columns x 
 constexpr int kStageBytes = 5 * kChunkBytes;        // 4 latent chunks + the rope chunk
 constexpr int kXbufBytes = kTileTokens * 128 * 2;   // fp16 partial scores of a tile (log2 units), 64 tokens x 128 heads
 constexpr int kQropeBytes = 128 * 128;              // [128 heads x 64 rope columns], 128-byte swizzled
+constexpr int kQStageBytes = 2 * 128 * 128;         // half the query's latent columns: two [128 heads x 64] boxes
 constexpr int kMiscBytes = 2048;                    // barriers, the warpgroups' row values, credit words
-// the ring, the two receive slots, the query's rope tile, the small things
-// (the query's latent part is staged in the receive slots and the last ring
-// stage before any of them is used)
-constexpr int kSmemBytes = kStages * kStageBytes + 2 * kXbufBytes + kQropeBytes + kMiscBytes + 1024 /* align */;
+constexpr int kSeqMax = 2048;                       // items a pair takes in sorted order, at most
+constexpr int kSortMax = 8192;                      // items put in order (in the ring), at most
+constexpr int kSortBins = 512;                      // tile counts told apart by that order
+// the ring, the two receive slots, the query's rope tile, the query staging
+// area, the small things, the pair's item list
+constexpr int kSmemBytes =
+    kStages * kStageBytes + 2 * kXbufBytes + kQropeBytes + kQStageBytes + kMiscBytes + 8 * kSeqMax + 1024 /* align */;
+static_assert(6 * kSortMax + 4 * (kMlaThreads / 32 + 1) * kSortBins <= kStages * kStageBytes,
+              "the sort's scratch lives in the ring");
 // tensor-memory columns
 constexpr uint32_t kColO = 0;      // O_c: 256 fp32 columns
 constexpr uint32_t kColQ = 256;    // Q_c latent part: 256 16-bit elements = 128 columns
@@ -99,7 +114,14 @@ __device__ int g_mla_status;  // first bounded wait that ran out (0 if none)
 
 struct Barriers {
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t q_full, qrope_full, qlat_full, mma_done;
+    uint64_t q_full;       // the item's latent query is in tensor memory (exchange warpgroup)
+    uint64_t q_empty;      // the item's last score product has run (MMA commit)
+    uint64_t qrope_full;   // the item's rope tile landed (TMA)
+    uint64_t qstage_full;  // a query half landed in the staging area (TMA)
+    uint64_t qstage_free;  // the staging area's half has moved to tensor memory
+    uint64_t o_free;       // the item's O has been read out (softmax threads)
+    uint64_t stg_free;     // the epilogue is done with the staging area (softmax warps)
+    uint64_t mma_done;
     uint64_t s_full[2], s_read[2], p_full[2], pv_done[2];  // per score / probability buffer
     uint64_t xfull[2];   // receive slot: the peer's partial scores arrived (st.async bytes)
     uint64_t credit[2];  // send slot: the peer has freed its receive slot (a st.async credit)
@@ -135,15 +157,28 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
     }
 }
 
-// Roles and the flow of one tile i (buffer u = i % 2, slot u, stage i % 3):
-//   TMA      kv_full[stage] <- 5 chunks of the tile's latent rows
-//   MMA      QK(i) -> S in SP[u] (s_full[u]); after P(i): PV(i) (pv_done[u],
-//            kv_empty[stage]); then QK(i + 2) into SP[u] (in issue order after PV(i))
-//   exchange S(i) from SP[u] (s_read[u]) -> the peer's receive slot u by
-//            st.async, once the peer granted that slot (credit[u])
-//   softmax  the peer's S(i) from slot u (xfull[u]) + the own S(i) from
-//            SP[u]; then re-arm xfull[u] and grant the slot back to the peer;
-//            P(i) into SP[u] columns [0, 32) (p_full[u])
+// Roles, for the pair's items in turn (global tile index gi over all of
+// them: score buffer and receive slot u = gi % 2, ring stage gi % 3; the
+// pair's n-th item with tokens is "item n"):
+//   TMA      item n's query: its two latent halves through the staging area
+//            (qstage_full; the first once the area is free of item n-2's
+//            epilogue and of the last half, the second once the first has
+//            moved on: qstage_free), its rope tile once item n-1's last score
+//            product has run (q_empty); kv_full[stage] <- each tile's 5 chunks
+//   exchange item n's latent query from the staging area into tensor memory
+//            once item n-1's last score product has run (q_full); then S(gi)
+//            from SP[u] (s_read[u]) -> the peer's receive slot u by st.async
+//            once the peer granted it (credit[u])
+//   MMA      the scores run two tiles ahead of the value products, across
+//            items: PV(gi) after P(gi) (pv_done[u], kv_empty[stage]; an
+//            item's first once the previous item's O has been read: o_free),
+//            then QK(gi + 2) into SP[u] (s_full[u]; an item's last also
+//            q_empty)
+//   softmax  the peer's S(gi) from slot u (xfull[u]) + the own S(gi) from
+//            SP[u]; re-arm xfull[u] and grant the slot back to the peer;
+//            P(gi) into SP[u] columns [0, 32) (p_full[u]); after an item's
+//            last PV its O goes out (o_free once read) through the staging
+//            area, once the next item's query has left it (stg_free after)
 template <typename T>
 __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map,
                                                                    const __grid_constant__ CUtensorMap q_map,
@@ -153,20 +188,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     uint8_t* stages = smem;
     uint8_t* slots = smem + kStages * kStageBytes;  // 2 x [8 token groups][128 heads] x 8 halves
     uint8_t* qrope = slots + 2 * kXbufBytes;
-    // staging box j of the query's latent columns
-    auto q_stage = [&](int j) -> uint8_t* {
-        return j < 2 ? slots + j * 128 * 128 : stages + (kStages - 1) * kStageBytes + (j - 2) * 128 * 128;
-    };
-    Barriers* bar = reinterpret_cast<Barriers*>(qrope + kQropeBytes);
+    uint8_t* qstage = qrope + kQropeBytes;  // half the query's latent columns, or the epilogue's rows
+    Barriers* bar = reinterpret_cast<Barriers*>(qstage + kQStageBytes);
+    int* seq = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bar) + kMiscBytes);  // the pair's items
+    int* spn = seq + kSeqMax;                                                           // and their tokens
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t c = cluster_ctarank();  // which half of the columns
     const uint32_t peer = c ^ 1u;
-    const int item = (int)(blockIdx.x >> 1);
-    const int split = item % p.nsplit;
-    const int rb = item / p.nsplit;
-    const int b = rb % p.B;
-    const int r = rb / p.B;
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+    const int nitems = p.N * p.B * p.nsplit;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -174,8 +205,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             mbar_init(&bar->kv_empty[s], 1);
         }
         mbar_init(&bar->q_full, 128);
+        mbar_init(&bar->q_empty, 1);
         mbar_init(&bar->qrope_full, 1);
-        mbar_init(&bar->qlat_full, 1);
+        mbar_init(&bar->qstage_full, 1);
+        mbar_init(&bar->qstage_free, 128);
+        mbar_init(&bar->o_free, kSoftmaxThreads);
+        mbar_init(&bar->stg_free, kSoftmaxThreads / 32);
         mbar_init(&bar->mma_done, 1);
         for (int u = 0; u < 2; ++u) {
             mbar_init(&bar->s_full[u], 1);
@@ -207,55 +242,204 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     tc_fence_after();
     cluster_sync();  // the peer's barriers are initialised before any remote arrival
     pdl_wait();      // the set-up above overlapped the previous kernel's tail
-    int L = p.seq_lens[b];
-    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
-    const int Ll = L / p.N + (r < L % p.N ? 1 : 0);
-    const int t0 = split * p.split_tokens;
-    const int t1 = min(t0 + p.split_tokens, Ll);
-    const int ntiles = t1 > t0 ? (t1 - t0 + kTileTokens - 1) / kTileTokens : 0;
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort = &bar->abort;
     int* status = &g_mla_status;
     bool issued_any = false;  // the MMA thread issued at least one MMA
     const unsigned kAll = 0xffffffffu;
 
+    // Item idx = (rank r, request b, split): its first local token t0, and
+    // its number of local tokens (from the request's length), in tiles
+    struct Item {
+        int r, b, split, t0;
+    };
+    auto item_of = [&](int idx) {
+        Item it;
+        it.split = idx % p.nsplit;
+        const int rb = idx / p.nsplit;
+        it.b = rb % p.B;
+        it.r = rb / p.B;
+        it.t0 = it.split * p.split_tokens;
+        return it;
+    };
+    auto span_of = [&](int idx) {
+        const Item it = item_of(idx);
+        int L = p.seq_lens[it.b];
+        L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+        const int Ll = L / p.N + (it.r < L % p.N ? 1 : 0);
+        return max(0, min(it.t0 + p.split_tokens, Ll) - it.t0);
+    };
+    auto tiles_of = [](int span) { return (span + kTileTokens - 1) / kTileTokens; };
+    // The pair's items.  Every CTA puts all items in order of their number of
+    // tiles, most first, ties by index (a stable counting sort in the ring,
+    // before any copy lands there); pair q then takes positions q, 2P - 1 -
+    // q, 2P + q, 4P - 1 - q, ... (P pairs), so the longest items start first
+    // and the pairs' totals come out close.  Both CTAs of a pair compute the
+    // same list.  Past kSortMax items (or kSeqMax a pair), pair q takes q,
+    // q + P, q + 2P, ...
+    const bool sorted = nitems <= kSortMax && (nitems + npairs - 1) / npairs <= kSeqMax;
+    if (sorted) {
+        constexpr int kWarps = kMlaThreads / 32;
+        uint16_t* bin_of = reinterpret_cast<uint16_t*>(stages);         // [item]
+        int* order = reinterpret_cast<int*>(stages + 2 * kSortMax);     // [position]
+        int* hist = order + kSortMax;                                   // [warp][bin]
+        int* start = hist + kWarps * kSortBins;                         // [bin]
+        // bin 0 holds the items with the most tiles (nbins - 1 or more)
+        const int nbins = min(kSortBins, (p.split_tokens + kTileTokens - 1) / kTileTokens + 1);
+        for (int i = tid; i < nitems; i += kMlaThreads)
+            bin_of[i] = (uint16_t)(nbins - 1 - min(tiles_of(span_of(i)), nbins - 1));
+        for (int i = tid; i < kWarps * nbins; i += kMlaThreads) hist[i] = 0;
+        __syncthreads();
+        // warp w takes the items [w * seg, (w + 1) * seg): first the count of
+        // each bin among them
+        const int seg = (nitems + kWarps - 1) / kWarps;
+        const int s0 = min(warp * seg, nitems), s1 = min(s0 + seg, nitems);
+        for (int i0 = s0; i0 < s1; i0 += 32) {
+            const int i = i0 + lane;
+            const unsigned act = __ballot_sync(kAll, i < s1);
+            if (i < s1) {
+                const int bn = bin_of[i];
+                const unsigned peers = __match_any_sync(act, bn);
+                if (lane == __ffs(peers) - 1) hist[warp * nbins + bn] += __popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        // per bin: the items of the warps before (exclusive), and the total
+        for (int bn = tid; bn < nbins; bn += kMlaThreads) {
+            int run = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                const int cnt = hist[w * nbins + bn];
+                hist[w * nbins + bn] = run;
+                run += cnt;
+            }
+            start[bn] = run;
+        }
+        __syncthreads();
+        if (warp == 0) {  // the bins' first positions: an exclusive scan of the totals
+            int carry = 0;
+            for (int b0 = 0; b0 < nbins; b0 += 32) {
+                const int bn = b0 + lane;
+                const int tot = bn < nbins ? start[bn] : 0;
+                int incl = tot;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(kAll, incl, d);
+                    if (lane >= d) incl += y;
+                }
+                if (bn < nbins) start[bn] = carry + incl - tot;
+                carry += __shfl_sync(kAll, incl, 31);
+            }
+        }
+        __syncthreads();
+        // each item's position: its bin's first, plus the bin's items in the
+        // warps before, in this warp's earlier chunks and at lower lanes
+        for (int i0 = s0; i0 < s1; i0 += 32) {
+            const int i = i0 + lane;
+            const unsigned act = __ballot_sync(kAll, i < s1);
+            if (i < s1) {
+                const int bn = bin_of[i];
+                const unsigned peers = __match_any_sync(act, bn);
+                order[start[bn] + hist[warp * nbins + bn] + __popc(peers & ((1u << lane) - 1u))] = i;
+                __syncwarp(act);
+                if (lane == __ffs(peers) - 1) hist[warp * nbins + bn] += __popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        for (int k = tid; k * npairs < nitems; k += kMlaThreads) {
+            const int pos = k * npairs + ((k & 1) ? npairs - 1 - pair : pair);
+            const int idx = pos < nitems ? order[pos] : -1;
+            seq[k] = idx;
+            spn[k] = idx >= 0 ? span_of(idx) : 0;
+        }
+        __syncthreads();  // the ring is free for copies again
+    }
+    // the pair's k-th item and its local tokens (idx -1: none, -2: past the
+    // list's end)
+    struct Work {
+        int idx, span;
+    };
+    auto work_at = [&](int k) -> Work {
+        if (sorted) {
+            if (k * npairs >= nitems) return {-2, 0};
+            return {seq[k], spn[k]};
+        }
+        const int idx = pair + k * npairs;
+        if (idx >= nitems) return {-2, 0};
+        return {idx, span_of(idx)};
+    };
+
     if (warp == 12) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            // the query's latent columns [256c, 256c + 256) as four [128 heads x
-            // 64] boxes (staging for tensor memory: two in the receive slots,
-            // two in the last ring stage), and its rope columns, once (heads
-            // past H read 0)
-            mbar_arrive_expect_tx(&bar->qlat_full, 4 * 128 * 128);
-            for (int j = 0; j < 4; ++j)
-                tma_load_3d(q_stage(j), &q_map, &bar->qlat_full, 256 * (int)c + 64 * j, 0, b);
-            mbar_arrive_expect_tx(&bar->qrope_full, kQropeBytes);
-            tma_load_3d(qrope, &q_map, &bar->qrope_full, 512, 0, b);
-            int issued = 0;
-            for (int i = 0; i < ntiles && !p.stall_loads; ++i) {
-                const int st = i % kStages, k = i / kStages;
-                if (k > 0 && !mbar_wait(&bar->kv_empty[st], (k - 1) & 1, status, kStatusTimeout, abort)) break;
-                // the last stage's first tile waits until the query has left it
-                if (k == 0 && st == kStages - 1 && !mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort)) break;
+            int gt = 0;      // tiles of the items before
+            int nq = 0;      // items with tokens before
+            int nbox = 0;    // query halves staged
+            int nrope = 0;   // rope tiles loaded
+            int issued = 0;  // tiles loaded
+            bool ok = true;
+            // half `half` of the query's latent columns [256c, 256c + 256) of
+            // request b: two [128 heads x 64] boxes (heads past H read 0)
+            auto stage_half = [&](int half, int b) {
+                mbar_arrive_expect_tx(&bar->qstage_full, kQStageBytes);
+                for (int jj = 0; jj < 2; ++jj)
+                    tma_load_3d(qstage + jj * 128 * 128, &q_map, &bar->qstage_full, 256 * (int)c + 64 * (2 * half + jj),
+                                0, b);
+                ++nbox;
+            };
+            // the tile i of item `it` (global index gi) into its ring stage
+            auto load_tile = [&](const Item& it, int i, int gi) -> bool {
+                const int st = gi % kStages, kk = gi / kStages;
+                if (kk > 0 && !mbar_wait(&bar->kv_empty[st], (kk - 1) & 1, status, kStatusTimeout, abort)) return false;
                 uint8_t* dst = stages + st * kStageBytes;
                 mbar_arrive_expect_tx(&bar->kv_full[st], kStageBytes);
-                const int y = t0 + i * kTileTokens;
+                const int y = it.t0 + i * kTileTokens;
                 for (int j = 0; j < 4; ++j)
-                    tma_load_4d(dst + j * kChunkBytes, &kv_map, &bar->kv_full[st], 256 * (int)c + 64 * j, y, b, r);
-                tma_load_4d(dst + 4 * kChunkBytes, &kv_map, &bar->kv_full[st], 512, y, b, r);
-                issued = i + 1;
+                    tma_load_4d(dst + j * kChunkBytes, &kv_map, &bar->kv_full[st], 256 * (int)c + 64 * j, y, it.b, it.r);
+                tma_load_4d(dst + 4 * kChunkBytes, &kv_map, &bar->kv_full[st], 512, y, it.b, it.r);
+                issued = gi + 1;
+                return true;
+            };
+            for (int k = 0; ok; ++k) {
+                const Work w = work_at(k);
+                if (w.idx == -2) break;
+                const int ntiles = tiles_of(w.span);
+                if (w.idx < 0 || ntiles == 0) continue;
+                const Item it = item_of(w.idx);
+                // in the order they can go (every wait blocks): the query's
+                // first half (once item n-2's epilogue and the last half have
+                // left the staging area), the first tile, the rope tile (once
+                // item n-1's last score product has run), the second half
+                // (once the first has moved on), the other tiles
+                ok = (nq < 2 || mbar_wait(&bar->stg_free, (nq - 2) & 1, status, kStatusTimeout, abort)) &&
+                     (nbox == 0 || mbar_wait(&bar->qstage_free, (nbox - 1) & 1, status, kStatusTimeout, abort));
+                if (!ok) break;
+                stage_half(0, it.b);
+                if (!p.stall_loads && !load_tile(it, 0, gt)) break;
+                if (nq > 0 && !mbar_wait(&bar->q_empty, (nq - 1) & 1, status, kStatusTimeout, abort)) break;
+                mbar_arrive_expect_tx(&bar->qrope_full, kQropeBytes);
+                tma_load_3d(qrope, &q_map, &bar->qrope_full, 512, 0, it.b);
+                ++nrope;
+                if (!mbar_wait(&bar->qstage_free, (nbox - 1) & 1, status, kStatusTimeout, abort)) break;
+                stage_half(1, it.b);
+                if (p.stall_loads) break;
+                for (int i = 1; ok && i < ntiles; ++i) ok = load_tile(it, i, gt + i);
+                gt += ntiles;
+                ++nq;
             }
             // copies still in flight (only after an abort) land before the CTA ends
             const uint64_t t_start = global_timer_ns();
-            while (!mbar_try_wait(&bar->qrope_full, 0) && global_timer_ns() - t_start < kWaitLimitNs) {
-            }
-            while (!mbar_try_wait(&bar->qlat_full, 0) && global_timer_ns() - t_start < kWaitLimitNs) {
-            }
-            for (int i = max(0, issued - kStages); i < issued; ++i) {
-                uint64_t* fb = &bar->kv_full[i % kStages];
-                const uint32_t par = (i / kStages) & 1;
+            if (nrope > 0)
+                while (!mbar_try_wait(&bar->qrope_full, (nrope - 1) & 1) && global_timer_ns() - t_start < kWaitLimitNs) {
+                }
+            if (nbox > 0)
+                while (!mbar_try_wait(&bar->qstage_full, (nbox - 1) & 1) && global_timer_ns() - t_start < kWaitLimitNs) {
+                }
+            for (int gi = max(0, issued - kStages); gi < issued; ++gi) {
                 const uint64_t t1w = global_timer_ns();
-                while (!mbar_try_wait(fb, par) && global_timer_ns() - t1w < kWaitLimitNs) {
+                while (!mbar_try_wait(&bar->kv_full[gi % kStages], (gi / kStages) & 1) &&
+                       global_timer_ns() - t1w < kWaitLimitNs) {
                 }
             }
         }
@@ -267,14 +451,33 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             const uint32_t idesc_pv = idesc_f16(128, 256, kBf16, 0, 1);
             const uint32_t tQ = tmem + kColQ, tO = tmem + kColO;
             const uint64_t dq = smem_desc(smem_u32(qrope), 16, 1024, kSwizzle128B);
-            // S(i) = Q_c . KV_c(i)^T into buffer i % 2.  The descriptor's
-            // address field is bits 0-13 in 16-byte units: offsets are added
-            // to it directly.
-            auto issue_qk = [&](int i) -> bool {
-                const int st = i % kStages;
-                if (!mbar_wait(&bar->kv_full[st], (i / kStages) & 1, status, kStatusTimeout, abort)) return false;
+            // the score stream: the next tile whose S is computed (tile qi of
+            // the pair's qk-th item, the qn-th with tokens; global tile qg)
+            int qk = -1, qi = 0, qn = -1, qg = 0, qnt = 0;
+            auto next_tile = [&]() -> bool {
+                if (qk >= 0 && ++qi < qnt) return true;
+                for (;;) {
+                    const Work w = work_at(++qk);
+                    if (w.idx == -2) return false;
+                    qnt = w.idx >= 0 ? tiles_of(w.span) : 0;
+                    if (qnt > 0) break;
+                }
+                qi = 0;
+                ++qn;
+                return true;
+            };
+            bool qmore = next_tile();
+            // S(qg) = Q_c . KV_c(qg)^T into buffer qg % 2, then the stream
+            // moves on.  The descriptor's address field is bits 0-13 in
+            // 16-byte units: offsets are added to it directly.
+            auto issue_qk = [&]() -> bool {
+                if (qi == 0 && (!mbar_wait(&bar->q_full, qn & 1, status, kStatusTimeout, abort) ||
+                                !mbar_wait(&bar->qrope_full, qn & 1, status, kStatusTimeout, abort)))
+                    return false;
+                const int st = qg % kStages;
+                if (!mbar_wait(&bar->kv_full[st], (qg / kStages) & 1, status, kStatusTimeout, abort)) return false;
                 tc_fence_after();
-                const uint32_t tS = tmem + kColSP + 64 * (i & 1);
+                const uint32_t tS = tmem + kColSP + 64 * (qg & 1);
                 const uint64_t d0 = smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kSwizzle128B);
 #pragma unroll
                 for (int s = 0; s < 16; ++s)  // latent columns: 4 chunks x 4 steps of 16, A in TMEM
@@ -284,78 +487,141 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 for (int s = 0; s < 2; ++s)  // this CTA's 32 rope columns: bytes [64c, 64c + 64) of each row
                     mma_ss(tS, dq + (uint64_t)((64 * c + 32 * s) >> 4),
                            d0 + (uint64_t)((4 * kChunkBytes + 64 * c + 32 * s) >> 4), idesc_qk, 1u);
-                mma_commit(&bar->s_full[i & 1]);
+                mma_commit(&bar->s_full[qg & 1]);
+                if (qi == qnt - 1) mma_commit(&bar->q_empty);  // the item's last read of its query
                 issued_any = true;
+                ++qg;
+                qmore = next_tile();
                 return true;
             };
-            bool ok = mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort) &&
-                      mbar_wait(&bar->qrope_full, 0, status, kStatusTimeout, abort);
-            for (int i = 0; ok && i < ntiles && i < 2; ++i) ok = issue_qk(i);
-            for (int i = 0; ok && i < ntiles; ++i) {
-                // O += P(i) . V(i): P from TMEM (the first 32 columns of SP[i % 2]),
-                // V read MN-major from tile i's stage
-                const int u = i & 1;
-                if (!mbar_wait(&bar->p_full[u], (i >> 1) & 1, status, kStatusTimeout, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t dv =
-                    smem_desc(smem_u32(stages + (i % kStages) * kStageBytes), kChunkBytes, 1024, kSwizzle128B);
-                const uint32_t tP = tmem + kColSP + 64 * u;
+            bool ok = true;
+            for (int j = 0; ok && qmore && j < 2; ++j) ok = issue_qk();
+            int gt = 0, nq = 0;
+            for (int k = 0; ok; ++k) {
+                const Work w = work_at(k);
+                if (w.idx == -2) break;
+                const int ntiles = w.idx >= 0 ? tiles_of(w.span) : 0;
+                if (ntiles == 0) continue;
+                for (int i = 0; i < ntiles; ++i) {
+                    // O += P(gi) . V(gi): P from TMEM (the first 32 columns of
+                    // SP[gi % 2]), V read MN-major from the tile's stage
+                    const int gi = gt + i, u = gi & 1;
+                    if (!mbar_wait(&bar->p_full[u], (gi >> 1) & 1, status, kStatusTimeout, abort) ||
+                        (i == 0 && nq > 0 && !mbar_wait(&bar->o_free, (nq - 1) & 1, status, kStatusTimeout, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t dv = smem_desc(smem_u32(stages + (gi % kStages) * kStageBytes), kChunkBytes, 1024,
+                                                  kSwizzle128B);
+                    const uint32_t tP = tmem + kColSP + 64 * u;
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_ts(tO, tP + 8 * s, dv + (uint64_t)((2048 * s) >> 4), idesc_pv, (i > 0 || s > 0) ? 1u : 0u);
-                mma_commit(&bar->pv_done[u]);
-                mma_commit(&bar->kv_empty[i % kStages]);
-                // the MMAs run in issue order: QK(i + 2) overwrites SP[u] after PV(i) has read P(i)
-                if (i + 2 < ntiles && !issue_qk(i + 2)) {
-                    ok = false;
-                    break;
+                    for (int s = 0; s < 4; ++s)
+                        mma_ts(tO, tP + 8 * s, dv + (uint64_t)((2048 * s) >> 4), idesc_pv, (i > 0 || s > 0) ? 1u : 0u);
+                    mma_commit(&bar->pv_done[u]);
+                    mma_commit(&bar->kv_empty[gi % kStages]);
+                    // in issue order: QK(gi + 2) overwrites SP[u] after PV(gi) has read P(gi)
+                    if (qmore && !issue_qk()) {
+                        ok = false;
+                        break;
+                    }
                 }
+                gt += ntiles;
+                ++nq;
             }
             if (issued_any) mma_commit(&bar->mma_done);
         }
     } else if (warp >= 8) {
         // ------------------------------------------------- exchange warpgroup
-        // Thread h: row h of S_c of every tile, to the peer's receive slot.
+        // Thread h: row h of each item's latent query into its TMEM lane, then
+        // row h of S_c of every tile to the peer's receive slot.
         const int h = tid - 256;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const float scale2x = p.sm_scale * kLog2eF;
         const uint32_t peer_slots = map_to_cta(slots, peer);
         const uint32_t peer_xfull = map_to_cta(&bar->xfull[0], peer);  // slot u's barrier is 8u bytes further
-        for (int i = 0; i < ntiles; ++i) {
-            const int u = i & 1;
-            if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (i >> 1) & 1, status, kStatusTimeout, abort))) break;
-            tc_fence_after();
-            uint32_t row[4][16];  // the four loads in flight together, one wait
-#pragma unroll
-            for (int k = 0; k < 4; ++k) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * k, row[k]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) pin(row[k]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->s_read[u]);
-            // the peer grants slot u once it has consumed the message before
-            if (!__all_sync(kAll, mbar_wait<true>(&bar->credit[u], (i >> 1) & 1, status, kStatusTimeout, abort)))
+        int gt = 0, nq = 0, nbox = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const Work w = work_at(k);
+            if (w.idx == -2) break;
+            const int ntiles = w.idx >= 0 ? tiles_of(w.span) : 0;
+            if (ntiles == 0) continue;
+            // Q_c's latent columns [256c, 256c + 256) into tensor memory once
+            // the previous item's last score product has read the old ones, a
+            // half at a time from the staging area: two 128-byte-swizzled
+            // boxes of [128 heads x 64 columns] (row h of box jj at qstage +
+            // jj*16384 + h*128, 16-byte chunk k at position k ^ (h % 8)); TMEM
+            // columns [16gq, 16gq + 16) are chunks 4gq .. 4gq + 3 of the row
+            if (nq > 0 && !__all_sync(kAll, mbar_wait(&bar->q_empty, (nq - 1) & 1, status, kStatusTimeout, abort)))
                 break;
-            if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
-            // the row in log2 units, rounded to fp16 (saturating, NaN kept) in
-            // token pairs: group k of 8 tokens to slot offset (k * 128 + h) * 16
-            uint32_t hv[32];
+            for (int half = 0; half < 2; ++half) {
+                if (!__all_sync(kAll, mbar_wait(&bar->qstage_full, nbox & 1, status, kStatusTimeout, abort))) {
+                    ok = false;
+                    break;
+                }
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                hv[j] = f16x2_satfinite(__uint_as_float(row[(2 * j) >> 4][(2 * j) & 15]) * scale2x,
-                                        __uint_as_float(row[(2 * j + 1) >> 4][(2 * j + 1) & 15]) * scale2x);
-            const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
-            const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t w[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                st_async_v4(dst + k * 128 * 16,
-                            make_float4(__uint_as_float(hv[4 * k]), __uint_as_float(hv[4 * k + 1]),
-                                        __uint_as_float(hv[4 * k + 2]), __uint_as_float(hv[4 * k + 3])),
-                            xb);
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(qstage + (j >> 1) * 128 * 128 + h * 128 +
+                                                                        (((4 * (j & 1) + v) ^ (h & 7)) << 4));
+                        w[4 * v] = x.x;
+                        w[4 * v + 1] = x.y;
+                        w[4 * v + 2] = x.z;
+                        w[4 * v + 3] = x.w;
+                    }
+                    tmem_st16(tmem + kColQ + lane_off + 16 * (4 * half + j), w);
+                }
+                fence_proxy_async_smem();  // the staging reads come before the next copy into the area
+                mbar_arrive(&bar->qstage_free);
+                ++nbox;
+            }
+            if (!ok) break;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar->q_full);
+            for (int i = 0; i < ntiles; ++i) {
+                const int gi = gt + i, u = gi & 1;
+                if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t row[4][16];  // the four loads in flight together, one wait
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * q4, row[q4]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) pin(row[q4]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->s_read[u]);
+                // the peer grants slot u once it has consumed the message before
+                if (!__all_sync(kAll, mbar_wait<true>(&bar->credit[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                    ok = false;
+                    break;
+                }
+                if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
+                // the row in log2 units, rounded to fp16 (saturating, NaN kept) in
+                // token pairs: group q of 8 tokens to slot offset (q * 128 + h) * 16
+                uint32_t hv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    hv[j] = f16x2_satfinite(__uint_as_float(row[(2 * j) >> 4][(2 * j) & 15]) * scale2x,
+                                            __uint_as_float(row[(2 * j + 1) >> 4][(2 * j + 1) & 15]) * scale2x);
+                const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
+                const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_async_v4(dst + q * 128 * 16,
+                                make_float4(__uint_as_float(hv[4 * q]), __uint_as_float(hv[4 * q + 1]),
+                                            __uint_as_float(hv[4 * q + 2]), __uint_as_float(hv[4 * q + 3])),
+                                xb);
+            }
+            gt += ntiles;
+            ++nq;
         }
     } else {
         // ------------------------------------------- softmax, two warpgroups
@@ -366,281 +632,294 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t peer_credit = map_to_cta(&bar->credit[0], peer);   // slot u's is 8u bytes further
         const uint32_t peer_cword = map_to_cta(&bar->credit_word[0], peer);
-        if (g == 0 && __all_sync(kAll, mbar_wait(&bar->qlat_full, 0, status, kStatusTimeout, abort))) {
-            // Q_c's latent columns [256c, 256c + 256) into tensor memory,
-            // staged by TMA in the receive slots and the last ring stage (the
-            // peer may send only once the slots are granted, below, and the
-            // stage's first tile waits for q_full): four 128-byte-swizzled
-            // boxes of [128 heads x 64 columns], row h of box j at
-            // q_stage(j) + h*128 with 16-byte chunk k at position k ^ (h % 8); every thread moves
-            // its row into its lane, TMEM columns [16gq, 16gq + 16) being
-            // chunks 4gq .. 4gq + 3 of the row.
-#pragma unroll
-            for (int gq = 0; gq < 8; ++gq) {
-                uint32_t w[16];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(q_stage(gq >> 1) + h * 128 +
-                                                                    (((4 * (gq & 1) + v) ^ (h & 7)) << 4));
-                    w[4 * v] = x.x;
-                    w[4 * v + 1] = x.y;
-                    w[4 * v + 2] = x.z;
-                    w[4 * v + 3] = x.w;
-                }
-                tmem_st16(tmem + kColQ + lane_off + 16 * gq, w);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            fence_proxy_async_smem();  // the staging reads come before the peer's writes into the slots
-            mbar_arrive(&bar->q_full);
-            if (tid == 0 &&
-                mbar_wait(&bar->q_full, 0, status, kStatusTimeout, abort)) {  // every row read: grant both slots
-                st_async_b32(peer_cword, 1u, peer_credit);
-                st_async_b32(peer_cword + 4u, 1u, peer_credit + 8u);
-            }
+        if (tid == 0) {  // both receive slots start free: grant them to the peer
+            st_async_b32(peer_cword, 1u, peer_credit);
+            st_async_b32(peer_cword + 4u, 1u, peer_credit + 8u);
         }
         const float scale2 = p.sm_scale * kLog2eF;
-        float m_used = -INFINITY, l = 0.f;
-        // tcgen05.ld / st are warp-collective: every wait's outcome is made
-        // warp-uniform so that the lanes of a warp leave the loop together
-        bool ok = true;
-        for (int i = 0; i < ntiles && ok; ++i) {
-            const int u = i & 1;
-            // the own half of S(i) from tensor memory, the peer's from slot u
-            if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float own[kHalf];
-            {
-                uint32_t v[2][16];  // both loads in flight, one wait
-#pragma unroll
-                for (int k = 0; k < 2; ++k) tmem_ld16(tmem + kColSP + 64 * u + kHalf * g + lane_off + 16 * k, v[k]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    pin(v[k]);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) own[16 * k + q] = __uint_as_float(v[k][q]);
-                }
-            }
-            if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
-                ok = false;
-                break;
-            }
-            // the peer's half of this thread's tokens: groups 4g .. 4g + 3 of 8
-            const uint4* xin = reinterpret_cast<const uint4*>(slots + u * kXbufBytes) + 4 * g * 128;
-            const int valid = t1 - (t0 + i * kTileTokens) - kHalf * g;  // tokens of this half still in the split
-            float s[kHalf];
-            float mt = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < kHalf / 8; ++k) {
-                const uint4 o4 = xin[k * 128 + h];
-                const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int t = 8 * k + 2 * q;
-                    // both partial scores in log2 units rounded to fp16 alike,
-                    // then S_0 + S_1 in that order in both CTAs: the same bits
-                    // on both sides
-                    const float2 other = f16x2_to_float2(ow[q]);
-                    const float2 mine = f16x2_to_float2(f16x2_satfinite(own[t] * scale2, own[t + 1] * scale2));
-                    const float x0 = c == 0 ? mine.x + other.x : other.x + mine.x;
-                    const float x1 = c == 0 ? mine.y + other.y : other.y + mine.y;
-                    s[t] = t < valid ? x0 : -INFINITY;
-                    s[t + 1] = t + 1 < valid ? x1 : -INFINITY;
-                    mt = fmaxf(mt, fmaxf(s[t], s[t + 1]));
-                }
-            }
-            // the row max of the whole tile: this thread's half and the other
-            // warpgroup's (through shared memory, written once the other
-            // warpgroup has read the previous tile's value)
-            if (i > 0 && !__all_sync(kAll, mbar_wait(&bar->red_free, (i - 1) & 1, status, kStatusTimeout, abort))) {
-                ok = false;
-                break;
-            }
-            bar->red[g][h] = mt;
+        const bool live = h < p.H;
+        int nfull = 0;  // the pair's items with tokens
+        for (int k = 0;; ++k) {
+            const Work w = work_at(k);
+            if (w.idx == -2) break;
+            if (w.idx >= 0 && w.span > 0) ++nfull;
+        }
+        int gt = 0, gr = 0, nq = 0;  // tiles, uses of the row exchange, items with tokens: before
+        // one use of the row exchange between the two warpgroups: this
+        // thread's value in, the other warpgroup's for the same head out
+        auto exchange_row = [&](float mine, float& other) -> bool {
+            if (gr > 0 && !__all_sync(kAll, mbar_wait(&bar->red_free, (gr - 1) & 1, status, kStatusTimeout, abort)))
+                return false;
+            bar->red[g][h] = mine;
             mbar_arrive(&bar->red_full);
-            if (!__all_sync(kAll, mbar_wait(&bar->red_full, i & 1, status, kStatusTimeout, abort))) {
-                ok = false;
-                break;
-            }
-            const float mt_all = fmaxf(mt, bar->red[g ^ 1][h]);
+            if (!__all_sync(kAll, mbar_wait(&bar->red_full, gr & 1, status, kStatusTimeout, abort))) return false;
+            other = bar->red[g ^ 1][h];
             mbar_arrive(&bar->red_free);
-            if (tid == 0) {
-                // every softmax thread has read slot u (before its red_full
-                // arrival): re-arm it for tile i + 2 and grant it back to the peer
-                mbar_arrive_expect_tx(&bar->xfull[u], kXbufBytes);
-                st_async_b32(peer_cword + 4u * (uint32_t)u, 1u, peer_credit + 8u * (uint32_t)u);
-            }
-            const float m_new = fmaxf(m_used, mt_all);
-            const bool move = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
-            if (valid < kHalf) {
-                // rows past the split's last token were loaded from the cache
-                // as they are (stale values, possibly NaN): zero their value
-                // columns so that 0-probability rows add exactly 0
-                uint8_t* rows0 = stages + (i % kStages) * kStageBytes + kHalf * g * 128;
-                const int first = valid < 0 ? 0 : valid, rows = kHalf - first;
-                for (int e = h; e < 4 * rows * 8; e += 128) {
-                    const int chunk = e / (rows * 8), rem = e % (rows * 8);
-                    const int row = first + rem / 8, v16 = rem % 8;
-                    *reinterpret_cast<uint4*>(rows0 + chunk * kChunkBytes + row * 128 + v16 * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+            ++gr;
+            return true;
+        };
+        // tcgen05.ld / st are warp-collective: every wait's outcome is made
+        // warp-uniform so that the lanes of a warp leave the loops together
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const Work w = work_at(k);
+            if (w.idx == -2) break;
+            if (w.idx < 0) continue;
+            const int ntiles = tiles_of(w.span), span = w.span;
+            const Item it = item_of(w.idx);
+            if (ntiles == 0) {
+                // no token of this item: a single split writes the neutral
+                // (0, -inf) for its rows; with several splits the merge never
+                // reads an empty split's rows
+                if (p.nsplit == 1 && live) {
+                    uint4* orow = reinterpret_cast<uint4*>(p.o + (int64_t)it.r * p.o_sn + (int64_t)it.b * p.o_sb +
+                                                           (int64_t)h * p.o_sh + 2 * (256 * c + 128 * g));
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) orow[e] = make_uint4(0u, 0u, 0u, 0u);
+                    if (c == 0 && g == 0)
+                        p.lse[(int64_t)it.r * p.l_sn + (int64_t)it.b * p.l_sb + (int64_t)h * p.l_sh] = -INFINITY;
                 }
-                fence_proxy_async_smem();
+                continue;
             }
-            float alpha = 1.f;
-            if (move) {
-                alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - m_new);
-                l *= alpha;
-                m_used = m_new;
-            }
-            if (i > 0 && __any_sync(kAll, move)) {
-                // rescale this thread's 128 columns of O row h (alpha = 1 for
-                // rows that keep their max) once P.V of tile i - 1 has completed
-                if (!__all_sync(kAll, mbar_wait(&bar->pv_done[u ^ 1], ((i - 1) >> 1) & 1, status, kStatusTimeout,
-                                                abort))) {
+            float m_used = -INFINITY, l = 0.f;
+            for (int i = 0; i < ntiles; ++i) {
+                const int gi = gt + i, u = gi & 1;
+                // the own half of S(gi) from tensor memory, the peer's from slot u
+                if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int k = 0; k < 8; ++k) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
+                float own[kHalf];
+                {
+                    uint32_t v[2][16];  // both loads in flight, one wait
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2)
+                        tmem_ld16(tmem + kColSP + 64 * u + kHalf * g + lane_off + 16 * q2, v[q2]);
                     tmem_wait_ld();
-                    pin(v);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * alpha);
-                    tmem_st16(tmem + kColO + 128 * g + lane_off + 16 * k, v);
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        pin(v[q2]);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) own[16 * q2 + q] = __uint_as_float(v[q2][q]);
+                    }
                 }
+                if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                    ok = false;
+                    break;
+                }
+                // the peer's half of this thread's tokens: groups 4g .. 4g + 3 of 8
+                const uint4* xin = reinterpret_cast<const uint4*>(slots + u * kXbufBytes) + 4 * g * 128;
+                const int valid = span - i * kTileTokens - kHalf * g;  // tokens of this half in the split
+                float s[kHalf];
+                float mt = -INFINITY;
+#pragma unroll
+                for (int q8 = 0; q8 < kHalf / 8; ++q8) {
+                    const uint4 o4 = xin[q8 * 128 + h];
+                    const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int t = 8 * q8 + 2 * q;
+                        // both partial scores in log2 units rounded to fp16
+                        // alike, then S_0 + S_1 in that order in both CTAs:
+                        // the same bits on both sides
+                        const float2 other = f16x2_to_float2(ow[q]);
+                        const float2 mine = f16x2_to_float2(f16x2_satfinite(own[t] * scale2, own[t + 1] * scale2));
+                        const float x0 = c == 0 ? mine.x + other.x : other.x + mine.x;
+                        const float x1 = c == 0 ? mine.y + other.y : other.y + mine.y;
+                        s[t] = t < valid ? x0 : -INFINITY;
+                        s[t + 1] = t + 1 < valid ? x1 : -INFINITY;
+                        mt = fmaxf(mt, fmaxf(s[t], s[t + 1]));
+                    }
+                }
+                // the row max of the whole tile: this thread's half and the
+                // other warpgroup's
+                float mt_other;
+                if (!exchange_row(mt, mt_other)) {
+                    ok = false;
+                    break;
+                }
+                const float mt_all = fmaxf(mt, mt_other);
+                if (tid == 0) {
+                    // every softmax thread has read slot u (before its red_full
+                    // arrival): re-arm it for tile gi + 2 and grant it back to the peer
+                    mbar_arrive_expect_tx(&bar->xfull[u], kXbufBytes);
+                    st_async_b32(peer_cword + 4u * (uint32_t)u, 1u, peer_credit + 8u * (uint32_t)u);
+                }
+                const float m_new = fmaxf(m_used, mt_all);
+                const bool move = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
+                if (valid < kHalf) {
+                    // rows past the split's last token were loaded from the cache
+                    // as they are (stale values, possibly NaN): zero their value
+                    // columns so that 0-probability rows add exactly 0
+                    uint8_t* rows0 = stages + (gi % kStages) * kStageBytes + kHalf * g * 128;
+                    const int first = valid < 0 ? 0 : valid, rows = kHalf - first;
+                    for (int e = h; e < 4 * rows * 8; e += 128) {
+                        const int chunk = e / (rows * 8), rem = e % (rows * 8);
+                        const int row = first + rem / 8, v16 = rem % 8;
+                        *reinterpret_cast<uint4*>(rows0 + chunk * kChunkBytes + row * 128 + v16 * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                float alpha = 1.f;
+                if (move) {
+                    alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - m_new);
+                    l *= alpha;
+                    m_used = m_new;
+                }
+                if (i > 0 && __any_sync(kAll, move)) {
+                    // rescale this thread's 128 columns of O row h (alpha = 1 for
+                    // rows that keep their max) once P.V of tile gi - 1 has completed
+                    if (!__all_sync(kAll, mbar_wait(&bar->pv_done[u ^ 1], ((gi - 1) >> 1) & 1, status, kStatusTimeout,
+                                                    abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int q16 = 0; q16 < 8; ++q16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * q16, v);
+                        tmem_wait_ld();
+                        pin(v);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * alpha);
+                        tmem_st16(tmem + kColO + 128 * g + lane_off + 16 * q16, v);
+                    }
+                }
+                // P = 2^(s - m) in the payload type into SP[u] columns [16g, 16g +
+                // 16), over scores already read: the other warpgroup's (it passed
+                // red_full) and the exchange warpgroup's (s_read)
+                if (!__all_sync(kAll, mbar_wait(&bar->s_read[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                    ok = false;
+                    break;
+                }
+                const float msub = m_used == -INFINITY ? 0.f : m_used;
+                {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float pa = exp2f(s[2 * q] - msub);
+                        const float pb = exp2f(s[2 * q + 1] - msub);
+                        l += pa + pb;
+                        w[q] = pack_pair<T>(pa, pb);
+                    }
+                    tmem_st16(tmem + kColSP + 64 * u + 16 * g + lane_off, w);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->p_full[u]);
             }
-            // P = 2^(s - m) in the payload type into SP[u] columns [16g, 16g +
-            // 16), over scores already read: the other warpgroup's (it passed
-            // red_full) and the exchange warpgroup's (s_read)
-            if (!__all_sync(kAll, mbar_wait(&bar->s_read[u], (i >> 1) & 1, status, kStatusTimeout, abort))) {
-                ok = false;
+            if (!ok) break;
+            // ------------------------------------------------------- epilogue
+            // the row sum is the two warpgroups' partial sums (both relative
+            // to the same reference max), added in a fixed order
+            const int glast = gt + ntiles - 1;
+            float l_other;
+            if (!__all_sync(kAll, mbar_wait(&bar->pv_done[glast & 1], (glast >> 1) & 1, status, kStatusTimeout,
+                                            abort)) ||
+                !exchange_row(l, l_other))
                 break;
-            }
-            const float msub = m_used == -INFINITY ? 0.f : m_used;
-            {
-                uint32_t w[16];
+            tc_fence_after();
+            const float l_all = g == 0 ? l + l_other : l_other + l;
+            // a row with no probability mass writes 0
+            const bool mass = l_all > 0.f;
+            const float inv = mass ? 1.f / l_all : 0.f;
+            const float lse2 = mass ? m_used + log2f(l_all) : -INFINITY;
+            // the staging area holds the next item's query until that has
+            // moved to tensor memory
+            const bool more = nq + 1 < nfull;
+            if (more && !__all_sync(kAll, mbar_wait(&bar->q_full, (nq + 1) & 1, status, kStatusTimeout, abort))) break;
+            // O columns [128g + 16k0, 128g + 16k0 + 32) of this thread's row
+            auto load_o2 = [&](int k0, uint32_t (&v)[2][16]) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float pa = exp2f(s[2 * q] - msub);
-                    const float pb = exp2f(s[2 * q + 1] - msub);
-                    l += pa + pb;
-                    w[q] = pack_pair<T>(pa, pb);
-                }
-                tmem_st16(tmem + kColSP + 64 * u + 16 * g + lane_off, w);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->p_full[u]);
-        }
-        if (ok && ntiles > 0)
-            ok = __all_sync(kAll, mbar_wait(&bar->pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, status,
-                                            kStatusTimeout, abort));
-        tc_fence_after();
-        // ----------------------------------------------------------- epilogue
-        // the row sum is the two warpgroups' partial sums (both relative to
-        // the same reference max)
-        if (ok && ntiles > 0 &&
-            !__all_sync(kAll, mbar_wait(&bar->red_free, (ntiles - 1) & 1, status, kStatusTimeout, abort)))
-            ok = false;
-        float l_all = 0.f;
-        if (ok) {
-            bar->red[g][h] = l;
-            mbar_arrive(&bar->red_full);
-            if (__all_sync(kAll, mbar_wait(&bar->red_full, ntiles & 1, status, kStatusTimeout, abort)))
-                l_all = g == 0 ? l + bar->red[1][h] : bar->red[0][h] + l;
-            else
-                ok = false;
-        }
-        // `have` is warp-uniform (it decides the warp-collective loads of O);
-        // a row with no probability mass still reads O but writes 0
-        const bool have = ok && ntiles > 0;
-        const bool mass = have && l_all > 0.f;
-        const float inv = mass ? 1.f / l_all : 0.f;
-        const float lse2 = mass ? m_used + log2f(l_all) : -INFINITY;
-        const bool live = h < p.H;
-        // O columns [128g + 16k0, 128g + 16k0 + 64) of this thread's row (zeros when there is none)
-        auto load_o4 = [&](int k0, uint32_t (&v)[4][16]) {
-            if (have) {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * (k0 + q4), v[q4]);
+                for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(tmem + kColO + 128 * g + lane_off + 16 * (k0 + q2), v[q2]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) pin(v[q4]);
-            } else {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q4][q] = 0u;
-            }
-        };
-        // The rows go out through shared memory: a thread holds one head's
-        // row, so its own stores would put each warp store across 32 rows;
-        // each softmax warp instead writes its 32 rows' 64-column chunk into
-        // 8 KB of the ring (idle once the last P.V has completed: no copy is
-        // in flight then), and stores them back row by row, coalesced.
-        // 16-byte chunk ch of row rr sits at rr * rowb + ((ch ^ (rr % 8)) * 16).
-        uint8_t* stg = stages + warp * 8192;
-        const int h0 = 32 * (warp & 3);  // the warp's first head
-        if (p.nsplit == 1) {
-            for (int k0 = 0; k0 < 8; k0 += 4) {  // 64 columns a pass, four loads in flight per wait
-                uint32_t v[4][16];
-                load_o4(k0, v);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t w[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        w[q] = pack_pair<T>(__uint_as_float(v[q4][2 * q]) * inv, __uint_as_float(v[q4][2 * q + 1]) * inv);
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        *reinterpret_cast<uint4*>(stg + lane * 128 + (((2 * q4 + e) ^ (lane & 7)) << 4)) =
-                            make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-                }
+                for (int q2 = 0; q2 < 2; ++q2) pin(v[q2]);
+            };
+            // every column of O read: the next item's P.V may start
+            auto release_o = [&]() {
+                tc_fence_before();
+                mbar_arrive(&bar->o_free);
+            };
+            // The rows go out through the staging area: a thread holds one
+            // head's row, so its own stores would put each warp store across
+            // 32 rows; each softmax warp instead writes 128 bytes of each of
+            // its 32 rows (64 payload columns, or 32 fp32 partials) into its 4
+            // KB and stores them back row by row, coalesced.  16-byte piece cc
+            // of row rr sits at rr * 128 + ((cc ^ (rr % 8)) * 16).
+            uint8_t* stg = qstage + warp * 4096;
+            const int h0 = 32 * (warp & 3);  // the warp's first head
+            // 128-byte piece x of each of the warp's rows to row0 + x * 128,
+            // row0 being this lane's first row (head h0 + lane / 8), rows
+            // rstride bytes apart
+            auto flush = [&](unsigned char* row0, int64_t rstride, int x) {
                 __syncwarp();
-#pragma unroll
+#pragma unroll 2
                 for (int j = 0; j < 8; ++j) {  // 4 rows of 128 bytes a store
                     const int rr = 4 * j + (lane >> 3), cc = lane & 7;
-                    const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
-                    if (h0 + rr < p.H)
-                        *reinterpret_cast<uint4*>(p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb +
-                                                  (int64_t)(h0 + rr) * p.o_sh + 2 * (256 * c + 128 * g + 16 * k0) +
-                                                  16 * cc) = x;
+                    const uint4 xv = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
+                    if (h0 + rr < p.H) *reinterpret_cast<uint4*>(row0 + 4 * j * rstride + x * 128 + 16 * cc) = xv;
                 }
                 __syncwarp();
-            }
-            if (live && c == 0 && g == 0)
-                p.lse[(int64_t)r * p.l_sn + (int64_t)b * p.l_sb + (int64_t)h * p.l_sh] = p.base2 ? lse2 : lse2 * kLn2F;
-        } else {
-            const int64_t row0 = (((int64_t)r * p.B + b) * p.H + h0) * p.nsplit + split;  // the warp's first head
-            for (int k0 = 0; k0 < 8; k0 += 4) {
-                uint32_t v[4][16];
-                load_o4(k0, v);
+            };
+            if (p.nsplit == 1) {
+                unsigned char* orow = p.o + (int64_t)it.r * p.o_sn + (int64_t)it.b * p.o_sb +
+                                      (int64_t)(h0 + (lane >> 3)) * p.o_sh + 2 * (256 * c + 128 * g);
+                for (int x = 0; x < 2; ++x) {  // 64 columns a pass, in two loads of 32
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[2][16];
+                        load_o2(4 * x + 2 * hh, v);
+                        if (x == 1 && hh == 1) release_o();
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        *reinterpret_cast<float4*>(stg + lane * 256 + (((4 * q4 + e) ^ (lane & 7)) << 4)) =
-                            make_float4(__uint_as_float(v[q4][4 * e]) * inv, __uint_as_float(v[q4][4 * e + 1]) * inv,
-                                        __uint_as_float(v[q4][4 * e + 2]) * inv, __uint_as_float(v[q4][4 * e + 3]) * inv);
-                __syncwarp();
+                        for (int q2 = 0; q2 < 2; ++q2) {
+                            uint32_t w[8];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {  // 2 rows of 256 bytes a store
-                    const int rr = 2 * j + (lane >> 4), cc = lane & 15;
-                    const float4 x = *reinterpret_cast<const float4*>(stg + rr * 256 + ((cc ^ (rr & 7)) << 4));
-                    if (h0 + rr < p.H)
-                        *reinterpret_cast<float4*>(p.ws_o + (row0 + (int64_t)rr * p.nsplit) * 512 + 256 * c + 128 * g +
-                                                   16 * k0 + 4 * cc) = x;
+                            for (int q = 0; q < 8; ++q)
+                                w[q] = pack_pair<T>(__uint_as_float(v[q2][2 * q]) * inv,
+                                                    __uint_as_float(v[q2][2 * q + 1]) * inv);
+#pragma unroll
+                            for (int e = 0; e < 2; ++e)
+                                *reinterpret_cast<uint4*>(stg + lane * 128 +
+                                                          (((2 * (2 * hh + q2) + e) ^ (lane & 7)) << 4)) =
+                                    make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                        }
+                    }
+                    flush(orow, p.o_sh, x);
                 }
-                __syncwarp();
+                if (live && c == 0 && g == 0)
+                    p.lse[(int64_t)it.r * p.l_sn + (int64_t)it.b * p.l_sb + (int64_t)h * p.l_sh] =
+                        p.base2 ? lse2 : lse2 * kLn2F;
+            } else {
+                unsigned char* wrow = reinterpret_cast<unsigned char*>(
+                    p.ws_o + ((((int64_t)it.r * p.B + it.b) * p.H + h0 + (lane >> 3)) * p.nsplit + it.split) * 512 +
+                    256 * c + 128 * g);
+                for (int x = 0; x < 4; ++x) {  // 32 fp32 columns (128 bytes) a pass
+                    uint32_t v[2][16];
+                    load_o2(2 * x, v);
+                    if (x == 3) release_o();
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<float4*>(stg + lane * 128 + (((4 * q2 + e) ^ (lane & 7)) << 4)) =
+                                make_float4(__uint_as_float(v[q2][4 * e]) * inv, __uint_as_float(v[q2][4 * e + 1]) * inv,
+                                            __uint_as_float(v[q2][4 * e + 2]) * inv,
+                                            __uint_as_float(v[q2][4 * e + 3]) * inv);
+                    flush(wrow, (int64_t)p.nsplit * 512 * 4, x);
+                }
+                if (live && c == 0 && g == 0)
+                    p.ws_lse[(((int64_t)it.r * p.B + it.b) * p.H + h) * p.nsplit + it.split] = lse2;
             }
-            if (live && c == 0 && g == 0) p.ws_lse[(((int64_t)r * p.B + b) * p.H + h) * p.nsplit + split] = lse2;
+            // the staging area is free again for the query after next
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->stg_free);
+            gt += ntiles;
+            ++nq;
         }
     }
 
@@ -663,8 +942,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
 }
 
 // Merge of the split partials (fp32, normalised, base-2 LSE) of every
-// (rank, request, head): one warp per row, with the combine's LSE rule
-// (empty splits are (0, -inf) and drop out).
+// (rank, request, head): one warp per row, with the combine's LSE rule.  Only
+// the splits that hold tokens of the rank were written; the empty ones are
+// the neutral (0, -inf) and drop out, so they are not read.
 template <typename T>
 __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p) {
     pdl_wait();
@@ -672,8 +952,15 @@ __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p
     const int64_t rows = (int64_t)p.N * p.B * p.H;
     const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (row >= rows) return;
-    const int S = p.nsplit;
-    const float* lrow = p.ws_lse + row * S;
+    const int h = (int)(row % p.H);
+    const int64_t rbq = row / p.H;
+    const int b = (int)(rbq % p.B);
+    const int r = (int)(rbq / p.B);
+    int L = p.seq_lens[b];
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+    const int Ll = L / p.N + (r < L % p.N ? 1 : 0);
+    const int S = min(p.nsplit, (Ll + p.split_tokens - 1) / p.split_tokens);
+    const float* lrow = p.ws_lse + row * p.nsplit;
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) M = fmaxf(M, lrow[s]);
     float Ls = 0.f;
@@ -684,7 +971,7 @@ __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p
         for (int s = 0; s < S; ++s) {
             const float w = exp2f(lrow[s] - M);
             Ls += w;
-            const float4* orow = reinterpret_cast<const float4*>(p.ws_o + (row * S + s) * 512);
+            const float4* orow = reinterpret_cast<const float4*>(p.ws_o + (row * p.nsplit + s) * 512);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float4 v = orow[lane + 32 * k];
@@ -695,10 +982,6 @@ __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p
             }
         }
     }
-    const int h = (int)(row % p.H);
-    const int64_t rbq = row / p.H;
-    const int b = (int)(rbq % p.B);
-    const int r = (int)(rbq / p.B);
     unsigned char* orow = p.o + (int64_t)r * p.o_sn + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh;
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll
@@ -713,14 +996,49 @@ __global__ void __launch_bounds__(128) mla_merge_splits_kernel(const MlaParams p
     pdl_trigger();
 }
 
+// CTA pairs of the kernel that fit on the device at once (one per two SMs),
+// per device; 0 if the occupancy query fails
+template <typename T>
+int resident_pairs() {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kMlaThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)mla_decode_kernel<T>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
 template <typename T>
 cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, const CUtensorMap& qmap, cudaStream_t stream) {
     // the shared-memory opt-in is a per-device function attribute
     const cudaError_t attr_err =
         cudaFuncSetAttribute((const void*)mla_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
+    const int64_t items = (int64_t)p.N * p.B * p.nsplit;
+    if (items <= 0) return cudaSuccess;
+    // persistent: as many CTA pairs as fit at once (each takes its share of
+    // the items in turn), never more than there are items
+    const int fit = resident_pairs<T>();
+    if (fit <= 0) return cudaErrorLaunchOutOfResources;
+    const int64_t pairs = items < fit ? items : fit;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * (int64_t)p.N * p.B * p.nsplit));
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
     cfg.blockDim = dim3(kMlaThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

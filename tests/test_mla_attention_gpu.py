@@ -4,7 +4,8 @@ Every rank's partial (O_r, lse_r) from dcp_decode_attention_mla is compared,
 element by element, with oracle.split_attention_mla on the same seeded
 inputs: small cases on every row (ragged tails, ranks owning nothing, one
 split and many, both LSE bases, bf16 and fp16, fewer than 128 heads, strided
-operands), the full-size workload on sampled rows, and the whole one-GPU DCP
+operands), the full-size workload on sampled rows, a request's rows under
+both work orders of the persistent kernel, and the whole one-GPU DCP
 decode of the MLA merge's shape (attention -> peer-inside pack -> combine)
 against unsplit attention.
 
@@ -185,6 +186,31 @@ def test_mla_full_size_workload_sampled_rows():
         rows = global_rows(kv, b, lens[b], N)
         check_row(o[r, b, h].double().cpu().numpy(), float(lse[r, b, h]), qn[b, h], rows, r, N,
                   c["sm_scale"], c["base"], U[q.dtype], f"full size b={b} r={r} h={h}")
+
+
+def test_mla_schedule_leaves_every_item_bit_identical():
+    """The CTA pairs are persistent and each takes its share of the (rank,
+    request, split) items in turn: longest first while there are at most
+    8192 items, in launch order beyond.  An item's arithmetic does not depend
+    on which pair takes it or when, so a request's rows are bit for bit the
+    same in a batch of 10240 items (launch order) and in a batch of that
+    request alone (128 items, sorted), and they match the oracle."""
+    N, H, max_len, split, B = 8, 128, 8192, 64, 80   # 8 ranks x 80 requests x 16 splits
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(0, max_len + 1, size=B)]
+    lens[:3] = [0, max_len, 1]
+    q, kv, seq = draw(N, B, H, lens, max_len, torch.bfloat16, seed=17)
+    scale = 192 ** -0.5
+    o, lse = run(q, kv, seq, max_len, scale, "2", split)
+    for b in (0, 1, 2, 37, 79):
+        o1, lse1 = run(q[b:b + 1], kv[:, b:b + 1], seq[b:b + 1], max_len, scale, "2", split)
+        assert torch.equal(o1.view(torch.int16), o[:, b:b + 1].view(torch.int16)), f"request {b}: O differs"
+        assert torch.equal(lse1.view(torch.int32), lse[:, b:b + 1].view(torch.int32)), f"request {b}: lse differs"
+    qn = q.double().cpu().numpy()
+    for b, h, r in ((1, 0, 0), (1, 127, 7), (37, 5, 3), (79, 64, 1), (2, 9, 0), (2, 9, 1)):
+        rows = global_rows(kv, b, lens[b], N)
+        check_row(o[r, b, h].double().cpu().numpy(), float(lse[r, b, h]), qn[b, h], rows, r, N, scale, "2",
+                  U[q.dtype], f"b={b} r={r} h={h}")
 
 
 def test_whole_mla_dcp_decode_equals_unsplit_attention():
