@@ -29,20 +29,21 @@
 //     256 latent columns are the A operand in tensor memory, its 32 rope
 //     columns an A operand in shared memory (a TMA tile), the latent rows the
 //     K-major B operand;
-//   * an exchange warpgroup reads S_c as soon as it is ready and sends it to
-//     the peer CTA, in log2 units rounded to fp16 (half the bytes of fp32 on
-//     the distributed-shared-memory path that bounds the tile), with st.async
-//     stores that count their bytes on the peer's mbarrier (no fence); a
-//     4-byte st.async credit from the peer frees each of its two receive
-//     slots again.  Scores are double-buffered in TMEM, so the exchange of
-//     tile i + 1 overlaps the softmax of tile i;
+//   * an exchange warpgroup reads S_c as soon as it is ready, rounds it to
+//     fp16 in log2 units (half the bytes of fp32 on the
+//     distributed-shared-memory path), and sends it to the peer CTA with
+//     st.async stores that count their bytes on the peer's mbarrier (no
+//     fence) -- a 4-byte st.async credit from the peer frees each of its two
+//     receive slots again -- and puts the same fp16 pairs back into tensor
+//     memory for its own CTA's softmax.  Scores are double-buffered in TMEM,
+//     so the exchange of tile i + 1 overlaps the softmax of tile i;
 //   * two softmax warpgroups (thread (h, g) = head h = TMEM lane h, tokens
-//     [32g, 32g + 32) of the tile) round their own partial the same way and
-//     add the peer's as S_0 + S_1 in that order (the same bits in both CTAs:
-//     one probability for both halves of the output) and run an online softmax in base 2
-//     with a lazily moved reference max (the output is rescaled only when the
-//     max grows by more than 2^8, so most tiles skip it); P goes to tensor
-//     memory as bf16/fp16, over its tile's consumed scores;
+//     [32g, 32g + 32) of the tile) add the two fp16 partials in fp32 (the
+//     same bits in both CTAs: one probability for both halves of the
+//     output) and run an online softmax in base 2 with a lazily moved
+//     reference max (the output is rescaled only when the max grows by more
+//     than 2^8, so most tiles skip it); P goes to tensor memory as
+//     bf16/fp16, over its tile's consumed scores;
 //   * the MMA thread accumulates O_c [128 x 256] += P . V_c with P as the
 //     TMEM A operand and V_c read MN-major from the same shared-memory tile.
 // With one split the softmax warps normalise O and write (O_r, lse_r);
@@ -122,7 +123,7 @@ struct Barriers {
     uint64_t o_free;       // the item's O has been read out (softmax threads)
     uint64_t stg_free;     // the epilogue is done with the staging area (softmax warps)
     uint64_t mma_done;
-    uint64_t s_full[2], s_read[2], p_full[2], pv_done[2];  // per score / probability buffer
+    uint64_t s_full[2], own_full[2], p_full[2], pv_done[2];  // per score / probability buffer
     uint64_t xfull[2];   // receive slot: the peer's partial scores arrived (st.async bytes)
     uint64_t credit[2];  // send slot: the peer has freed its receive slot (a st.async credit)
     uint64_t red_full, red_free;  // the softmax warpgroups' per-row values: written / read
@@ -146,6 +147,15 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
     return __half22float2(h);
 }
 
+// 2^x by the ex2.approx instruction (the PTX ISA puts its relative error
+// near 2^-22, far below the 2^-9 / 2^-12 rounding of P to bf16 / fp16;
+// results below the normal range flush to 0, 2^-inf = 0).
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
     if constexpr (std::is_same<T, __half>::value) {
@@ -167,15 +177,16 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 //            product has run (q_empty); kv_full[stage] <- each tile's 5 chunks
 //   exchange item n's latent query from the staging area into tensor memory
 //            once item n-1's last score product has run (q_full); then S(gi)
-//            from SP[u] (s_read[u]) -> the peer's receive slot u by st.async
-//            once the peer granted it (credit[u])
+//            from SP[u] as fp16 pairs -> the peer's receive slot u by
+//            st.async once the peer granted it (credit[u]), and into SP[u]
+//            columns [32, 64) (own_full[u])
 //   MMA      the scores run two tiles ahead of the value products, across
 //            items: PV(gi) after P(gi) (pv_done[u], kv_empty[stage]; an
 //            item's first once the previous item's O has been read: o_free),
 //            then QK(gi + 2) into SP[u] (s_full[u]; an item's last also
 //            q_empty)
-//   softmax  the peer's S(gi) from slot u (xfull[u]) + the own S(gi) from
-//            SP[u]; re-arm xfull[u] and grant the slot back to the peer;
+//   softmax  the peer's S(gi) from slot u (xfull[u]) + the own from SP[u]
+//            (own_full[u]); re-arm xfull[u] and grant the slot back to the peer;
 //            P(gi) into SP[u] columns [0, 32) (p_full[u]); after an item's
 //            last PV its O goes out (o_free once read) through the staging
 //            area, once the next item's query has left it (stg_free after)
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         mbar_init(&bar->mma_done, 1);
         for (int u = 0; u < 2; ++u) {
             mbar_init(&bar->s_full[u], 1);
-            mbar_init(&bar->s_read[u], 4);
+            mbar_init(&bar->own_full[u], 4);
             mbar_init(&bar->p_full[u], 8);
             mbar_init(&bar->pv_done[u], 1);
             // the peer's bytes complete these; this CTA's expect_tx is the one
@@ -595,30 +606,44 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 tmem_wait_ld();
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) pin(row[q4]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar->s_read[u]);
                 // the peer grants slot u once it has consumed the message before
                 if (!__all_sync(kAll, mbar_wait<true>(&bar->credit[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
                     ok = false;
                     break;
                 }
                 if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
-                // the row in log2 units, rounded to fp16 (saturating, NaN kept) in
-                // token pairs: group q of 8 tokens to slot offset (q * 128 + h) * 16
-                uint32_t hv[32];
+                // the row in log2 units, rounded to fp16 (saturating, NaN kept)
+                // in token pairs, once for both CTAs' softmaxes: group q of 8
+                // tokens to the peer's slot u at offset (q * 128 + h) * 16, and
+                // pairs [16g, 16g + 16) (tokens [32g, 32g + 32)) into SP[u]
+                // columns [32 + 16g, 48 + 16g) for this CTA's warpgroup g, over
+                // scores this thread has read
+                uint32_t hv[2][16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    hv[j] = f16x2_satfinite(__uint_as_float(row[(2 * j) >> 4][(2 * j) & 15]) * scale2x,
-                                            __uint_as_float(row[(2 * j + 1) >> 4][(2 * j + 1) & 15]) * scale2x);
+                for (int g2 = 0; g2 < 2; ++g2)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        hv[g2][j] = f16x2_satfinite(__uint_as_float(row[2 * g2][2 * j]) * scale2x,
+                                                    __uint_as_float(row[2 * g2][2 * j + 1]) * scale2x);
+                        hv[g2][8 + j] = f16x2_satfinite(__uint_as_float(row[2 * g2 + 1][2 * j]) * scale2x,
+                                                        __uint_as_float(row[2 * g2 + 1][2 * j + 1]) * scale2x);
+                    }
                 const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
                 const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     st_async_v4(dst + q * 128 * 16,
-                                make_float4(__uint_as_float(hv[4 * q]), __uint_as_float(hv[4 * q + 1]),
-                                            __uint_as_float(hv[4 * q + 2]), __uint_as_float(hv[4 * q + 3])),
+                                make_float4(__uint_as_float(hv[q >> 2][4 * (q & 3)]),
+                                            __uint_as_float(hv[q >> 2][4 * (q & 3) + 1]),
+                                            __uint_as_float(hv[q >> 2][4 * (q & 3) + 2]),
+                                            __uint_as_float(hv[q >> 2][4 * (q & 3) + 3])),
                                 xb);
+#pragma unroll
+                for (int g2 = 0; g2 < 2; ++g2) tmem_st16(tmem + kColSP + 64 * u + 32 + 16 * g2 + lane_off, hv[g2]);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->own_full[u]);
             }
             gt += ntiles;
             ++nq;
@@ -636,7 +661,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             st_async_b32(peer_cword, 1u, peer_credit);
             st_async_b32(peer_cword + 4u, 1u, peer_credit + 8u);
         }
-        const float scale2 = p.sm_scale * kLog2eF;
         const bool live = h < p.H;
         int nfull = 0;  // the pair's items with tokens
         for (int k = 0;; ++k) {
@@ -684,26 +708,18 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             float m_used = -INFINITY, l = 0.f;
             for (int i = 0; i < ntiles; ++i) {
                 const int gi = gt + i, u = gi & 1;
-                // the own half of S(gi) from tensor memory, the peer's from slot u
-                if (!__all_sync(kAll, mbar_wait(&bar->s_full[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                // the own partial scores of this thread's tokens, as the
+                // exchange warpgroup rounded them (fp16 pairs in SP[u]
+                // columns [32 + 16g, 48 + 16g)), the peer's from slot u
+                if (!__all_sync(kAll, mbar_wait(&bar->own_full[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                float own[kHalf];
-                {
-                    uint32_t v[2][16];  // both loads in flight, one wait
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2)
-                        tmem_ld16(tmem + kColSP + 64 * u + kHalf * g + lane_off + 16 * q2, v[q2]);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        pin(v[q2]);
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) own[16 * q2 + q] = __uint_as_float(v[q2][q]);
-                    }
-                }
+                uint32_t own[16];
+                tmem_ld16(tmem + kColSP + 64 * u + 32 + 16 * g + lane_off, own);
+                tmem_wait_ld();
+                pin(own);
                 if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
                     ok = false;
                     break;
@@ -721,12 +737,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                     for (int q = 0; q < 4; ++q) {
                         const int t = 8 * q8 + 2 * q;
                         // both partial scores in log2 units rounded to fp16
-                        // alike, then S_0 + S_1 in that order in both CTAs:
-                        // the same bits on both sides
+                        // alike, added in fp32 (commutative): the same bits
+                        // in both CTAs
                         const float2 other = f16x2_to_float2(ow[q]);
-                        const float2 mine = f16x2_to_float2(f16x2_satfinite(own[t] * scale2, own[t + 1] * scale2));
-                        const float x0 = c == 0 ? mine.x + other.x : other.x + mine.x;
-                        const float x1 = c == 0 ? mine.y + other.y : other.y + mine.y;
+                        const float2 mine = f16x2_to_float2(own[4 * q8 + q]);
+                        const float x0 = mine.x + other.x;
+                        const float x1 = mine.y + other.y;
                         s[t] = t < valid ? x0 : -INFINITY;
                         s[t + 1] = t + 1 < valid ? x1 : -INFINITY;
                         mt = fmaxf(mt, fmaxf(s[t], s[t + 1]));
@@ -788,19 +804,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                     }
                 }
                 // P = 2^(s - m) in the payload type into SP[u] columns [16g, 16g +
-                // 16), over scores already read: the other warpgroup's (it passed
-                // red_full) and the exchange warpgroup's (s_read)
-                if (!__all_sync(kAll, mbar_wait(&bar->s_read[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
-                    ok = false;
-                    break;
-                }
+                // 16), over scores the exchange warpgroup has read (own_full)
                 const float msub = m_used == -INFINITY ? 0.f : m_used;
                 {
                     uint32_t w[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        const float pa = exp2f(s[2 * q] - msub);
-                        const float pb = exp2f(s[2 * q + 1] - msub);
+                        const float pa = exp2_approx(s[2 * q] - msub);
+                        const float pb = exp2_approx(s[2 * q + 1] - msub);
                         l += pa + pb;
                         w[q] = pack_pair<T>(pa, pb);
                     }
