@@ -135,16 +135,39 @@ struct Barriers {
 static_assert(sizeof(Barriers) <= kMiscBytes, "misc region too small");
 
 // Two floats to fp16 (round to nearest, values past the fp16 range to its
-// largest finite, NaN kept), lo in the low half; and back.
+// largest finite, NaN kept), lo in the low half.
 __device__ __forceinline__ uint32_t f16x2_satfinite(float lo, float hi) {
     uint32_t d;
     asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
 }
-__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
-    __half2 h;
-    memcpy(&h, &w, sizeof(h));
-    return __half22float2(h);
+
+// (a + b, c + d) with one instruction (packed fp32 add, round to nearest)
+__device__ __forceinline__ float2 add_f32x2(float2 x, float2 y) {
+    uint64_t a, b, d;
+    memcpy(&a, &x, 8);
+    memcpy(&b, &y, 8);
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    float2 r;
+    memcpy(&r, &d, 8);
+    return r;
+}
+// The sums of two pairs of fp16 values (lo halves, hi halves) rounded once
+// to fp32: x's halves enter the mixed-precision add as fp16, y's exactly
+// widened to fp32 first.
+__device__ __forceinline__ float2 add_f16x2_exact(uint32_t x, uint32_t y) {
+    float2 r;
+    asm("{\n .reg .b16 a0, a1, b0, b1;\n .reg .f32 f0, f1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %3;\n"
+        " cvt.f32.f16 f0, b0;\n cvt.f32.f16 f1, b1;\n add.rn.f32.f16 %0, a0, f0;\n add.rn.f32.f16 %1, a1, f1;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "r"(y));
+    return r;
+}
+// max(a, b, c) with one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // 2^x by the ex2.approx instruction (the PTX ISA puts its relative error
@@ -728,26 +751,27 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 const uint4* xin = reinterpret_cast<const uint4*>(slots + u * kXbufBytes) + 4 * g * 128;
                 const int valid = span - i * kTileTokens - kHalf * g;  // tokens of this half in the split
                 float s[kHalf];
-                float mt = -INFINITY;
 #pragma unroll
                 for (int q8 = 0; q8 < kHalf / 8; ++q8) {
                     const uint4 o4 = xin[q8 * 128 + h];
                     const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int t = 8 * q8 + 2 * q;
                         // both partial scores in log2 units rounded to fp16
-                        // alike, added in fp32 (commutative): the same bits
-                        // in both CTAs
-                        const float2 other = f16x2_to_float2(ow[q]);
-                        const float2 mine = f16x2_to_float2(own[4 * q8 + q]);
-                        const float x0 = mine.x + other.x;
-                        const float x1 = mine.y + other.y;
-                        s[t] = t < valid ? x0 : -INFINITY;
-                        s[t + 1] = t + 1 < valid ? x1 : -INFINITY;
-                        mt = fmaxf(mt, fmaxf(s[t], s[t + 1]));
+                        // alike, added with one rounding to fp32 (commutative:
+                        // the same bits in both CTAs)
+                        const float2 sum = add_f16x2_exact(own[4 * q8 + q], ow[q]);
+                        s[8 * q8 + 2 * q] = sum.x;
+                        s[8 * q8 + 2 * q + 1] = sum.y;
                     }
                 }
+                if (valid < kHalf) {  // the split ends inside this half
+#pragma unroll
+                    for (int t = 0; t < kHalf; ++t) s[t] = t < valid ? s[t] : -INFINITY;
+                }
+                float mt = -INFINITY;
+#pragma unroll
+                for (int t = 0; t < kHalf; t += 2) mt = fmax3(mt, s[t], s[t + 1]);
                 // the row max of the whole tile: this thread's half and the
                 // other warpgroup's
                 float mt_other;
@@ -807,14 +831,17 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 // 16), over scores the exchange warpgroup has read (own_full)
                 const float msub = m_used == -INFINITY ? 0.f : m_used;
                 {
+                    // in pairs: s - m and the running sum two lanes wide
                     uint32_t w[16];
+                    float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        const float pa = exp2_approx(s[2 * q] - msub);
-                        const float pb = exp2_approx(s[2 * q + 1] - msub);
-                        l += pa + pb;
-                        w[q] = pack_pair<T>(pa, pb);
+                        const float2 x = add_f32x2(make_float2(s[2 * q], s[2 * q + 1]), make_float2(-msub, -msub));
+                        const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                        l2 = add_f32x2(l2, pp);
+                        w[q] = pack_pair<T>(pp.x, pp.y);
                     }
+                    l += l2.x + l2.y;
                     tmem_st16(tmem + kColSP + 64 * u + 16 * g + lane_off, w);
                 }
                 tmem_wait_st();
