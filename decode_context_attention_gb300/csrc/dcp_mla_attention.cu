@@ -22,8 +22,11 @@
 // latent columns [256c, 256c + 256) plus rope columns [512 + 32c, 544 + 32c)
 // -- exactly the columns it loads, so the pair reads every latent byte once
 // and does every multiply-add once.  Per tile of 64 tokens:
-//   * TMA (one thread) loads the CTA's four 64-column latent chunks and the
-//     rope chunk of the 64 tokens, 128-byte swizzled, into a 3-stage ring;
+//   * TMA (one thread) loads the CTA's four 64-column latent chunks of the
+//     64 tokens (128-byte swizzled) and its 32 rope columns (64-byte
+//     swizzled) into a 4-stage ring (36 KB a stage: the loads of a tile are
+//     issued about three tiles ahead, which the memory latency under full
+//     load needs);
 //   * the MMA thread computes the partial scores S_c [128 heads x 64 tokens]
 //     = Q_c . KV_c^T with tcgen05.mma, fp32 in tensor memory: the query's
 //     256 latent columns are the A operand in tensor memory, its 32 rope
@@ -82,22 +85,25 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kTileTokens = 64;    // tokens per tile (one ring stage)
 constexpr int kHalf = 32;          // tokens of a tile per softmax warpgroup
 #ifndef DCP_MLA_STAGES
-#define DCP_MLA_STAGES 3
+#define DCP_MLA_STAGES 4
 #endif
 constexpr int kStages = DCP_MLA_STAGES;  // shared-memory ring depth
 constexpr int kChunkBytes = kTileTokens * 128;      // 64 tokens x 64 columns x 2 bytes
-constexpr int kStageBytes = 5 * kChunkBytes;        // 4 latent chunks + the rope chunk
+constexpr int kRopeChunkBytes = kTileTokens * 64;   // the CTA's 32 rope columns of 64 tokens
+constexpr int kStageBytes = 4 * kChunkBytes + kRopeChunkBytes;  // 4 latent chunks + the rope chunk
 constexpr int kXbufBytes = kTileTokens * 128 * 2;   // fp16 partial scores of a tile (log2 units), 64 tokens x 128 heads
-constexpr int kQropeBytes = 128 * 128;              // [128 heads x 64 rope columns], 128-byte swizzled
+constexpr int kQropeBytes = 128 * 64;               // [128 heads x the CTA's 32 rope columns], 64-byte swizzled
 constexpr int kQStageBytes = 2 * 128 * 128;         // half the query's latent columns: two [128 heads x 64] boxes
 constexpr int kMiscBytes = 2048;                    // barriers, the warpgroups' row values, credit words
-constexpr int kSeqMax = 2048;                       // items a pair takes in sorted order, at most
+constexpr int kSeqMax = 512;                        // items a pair takes in sorted order, at most
 constexpr int kSortMax = 8192;                      // items put in order (in the ring), at most
 constexpr int kSortBins = 512;                      // tile counts told apart by that order
 // the ring, the two receive slots, the query's rope tile, the query staging
 // area, the small things, the pair's item list
 constexpr int kSmemBytes =
     kStages * kStageBytes + 2 * kXbufBytes + kQropeBytes + kQStageBytes + kMiscBytes + 8 * kSeqMax + 1024 /* align */;
+static_assert(kSmemBytes <= 232448, "more than a CTA's shared memory");
+static_assert(kStageBytes % 1024 == 0 && kQropeBytes % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
 static_assert(6 * kSortMax + 4 * (kMlaThreads / 32 + 1) * kSortBins <= kStages * kStageBytes,
               "the sort's scratch lives in the ring");
 // tensor-memory columns
@@ -191,7 +197,7 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 }
 
 // Roles, for the pair's items in turn (global tile index gi over all of
-// them: score buffer and receive slot u = gi % 2, ring stage gi % 3; the
+// them: score buffer and receive slot u = gi % 2, ring stage gi % 4; the
 // pair's n-th item with tokens is "item n"):
 //   TMA      item n's query: its two latent halves through the staging area
 //            (qstage_full; the first once the area is free of item n-2's
@@ -215,7 +221,9 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 //            area, once the next item's query has left it (stg_free after)
 template <typename T>
 __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map,
+                                                                   const __grid_constant__ CUtensorMap kv_rope_map,
                                                                    const __grid_constant__ CUtensorMap q_map,
+                                                                   const __grid_constant__ CUtensorMap q_rope_map,
                                                                    const MlaParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,7 +277,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
     }
     if (warp == 12 && lane == 0) {
         tma_prefetch_map(&kv_map);
+        tma_prefetch_map(&kv_rope_map);
         tma_prefetch_map(&q_map);
+        tma_prefetch_map(&q_rope_map);
     }
     tc_fence_before();
     __syncthreads();
@@ -431,7 +441,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 const int y = it.t0 + i * kTileTokens;
                 for (int j = 0; j < 4; ++j)
                     tma_load_4d(dst + j * kChunkBytes, &kv_map, &bar->kv_full[st], 256 * (int)c + 64 * j, y, it.b, it.r);
-                tma_load_4d(dst + 4 * kChunkBytes, &kv_map, &bar->kv_full[st], 512, y, it.b, it.r);
+                tma_load_4d(dst + 4 * kChunkBytes, &kv_rope_map, &bar->kv_full[st], 512 + 32 * (int)c, y, it.b, it.r);
                 issued = gi + 1;
                 return true;
             };
@@ -453,7 +463,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 if (!p.stall_loads && !load_tile(it, 0, gt)) break;
                 if (nq > 0 && !mbar_wait(&bar->q_empty, (nq - 1) & 1, status, kStatusTimeout, abort)) break;
                 mbar_arrive_expect_tx(&bar->qrope_full, kQropeBytes);
-                tma_load_3d(qrope, &q_map, &bar->qrope_full, 512, 0, it.b);
+                tma_load_3d(qrope, &q_rope_map, &bar->qrope_full, 512 + 32 * (int)c, 0, it.b);
                 ++nrope;
                 if (!mbar_wait(&bar->qstage_free, (nbox - 1) & 1, status, kStatusTimeout, abort)) break;
                 stage_half(1, it.b);
@@ -484,7 +494,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             const uint32_t idesc_qk = idesc_f16(128, kTileTokens, kBf16, 0, 0);
             const uint32_t idesc_pv = idesc_f16(128, 256, kBf16, 0, 1);
             const uint32_t tQ = tmem + kColQ, tO = tmem + kColO;
-            const uint64_t dq = smem_desc(smem_u32(qrope), 16, 1024, kSwizzle128B);
+            const uint64_t dq = smem_desc(smem_u32(qrope), 16, 512, kSwizzle64B);
             // the score stream: the next tile whose S is computed (tile qi of
             // the pair's qk-th item, the qn-th with tokens; global tile qg)
             int qk = -1, qi = 0, qn = -1, qg = 0, qnt = 0;
@@ -513,14 +523,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 tc_fence_after();
                 const uint32_t tS = tmem + kColSP + 64 * (qg & 1);
                 const uint64_t d0 = smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kSwizzle128B);
+                const uint64_t dr = smem_desc(smem_u32(stages + st * kStageBytes + 4 * kChunkBytes), 16, 512, kSwizzle64B);
 #pragma unroll
                 for (int s = 0; s < 16; ++s)  // latent columns: 4 chunks x 4 steps of 16, A in TMEM
                     mma_ts(tS, tQ + 8 * s, d0 + (uint64_t)(((s >> 2) * kChunkBytes + (s & 3) * 32) >> 4), idesc_qk,
                            s > 0 ? 1u : 0u);
 #pragma unroll
-                for (int s = 0; s < 2; ++s)  // this CTA's 32 rope columns: bytes [64c, 64c + 64) of each row
-                    mma_ss(tS, dq + (uint64_t)((64 * c + 32 * s) >> 4),
-                           d0 + (uint64_t)((4 * kChunkBytes + 64 * c + 32 * s) >> 4), idesc_qk, 1u);
+                for (int s = 0; s < 2; ++s)  // this CTA's 32 rope columns: the 64-byte rows of both tiles
+                    mma_ss(tS, dq + (uint64_t)((32 * s) >> 4), dr + (uint64_t)((32 * s) >> 4), idesc_qk, 1u);
                 mma_commit(&bar->s_full[qg & 1]);
                 if (qi == qnt - 1) mma_commit(&bar->q_empty);  // the item's last read of its query
                 issued_any = true;
@@ -1063,7 +1073,7 @@ int resident_pairs() {
 }
 
 template <typename T>
-cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, const CUtensorMap& qmap, cudaStream_t stream) {
+cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     // the shared-memory opt-in is a per-device function attribute
     const cudaError_t attr_err =
         cudaFuncSetAttribute((const void*)mla_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1089,7 +1099,7 @@ cudaError_t launch_mla_t(const MlaParams& p, const CUtensorMap& map, const CUten
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = DCP_PDL ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<T>, map, qmap, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<T>, maps[0], maps[1], maps[2], maps[3], p);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const int64_t rows = (int64_t)p.N * p.B * p.H;
     MlaParams q = p;
@@ -1116,26 +1126,35 @@ cudaError_t launch_mla_decode(const MlaParams& p_in, int dtype, cudaStream_t str
     auto stride = [](int64_t extent, int64_t bytes, int64_t nominal) -> cuuint64_t {
         return (cuuint64_t)(extent > 1 ? bytes : nominal);
     };
-    // the latent cache as a 4-D tensor [N][B][Lc][576] (elements, then byte strides)
-    CUtensorMap map, qmap;
+    // the latent cache as a 4-D tensor [N][B][Lc][576] (elements, then byte
+    // strides): latent boxes of [64 tokens x 64 columns], 128-byte swizzled,
+    // and rope boxes of [64 tokens x 32 columns], 64-byte swizzled
+    CUtensorMap maps[4];  // latent rows, rope columns of the rows, query, rope columns of the query
     const int64_t lc = p.lcap > 0 ? p.lcap : 1;
     const cuuint64_t dims[4] = {576, (cuuint64_t)lc, (cuuint64_t)p.B, (cuuint64_t)p.N};
     const cuuint64_t strides[3] = {stride(lc, p.kv_st, 1152), stride(p.B, p.kv_sb, 1152), stride(p.N, p.kv_sn, 1152)};
     const cuuint32_t box[4] = {64, kTileTokens, 1, 1};
-    CUresult rc = enc(&map, dt, 4, const_cast<unsigned char*>(p.kv), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (rc != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    // the absorbed queries as a 3-D tensor [B][H][576]: the rope tile is rows
-    // [0, 128) at column 512 (rows past H read 0)
+    const cuuint32_t rbox[4] = {32, kTileTokens, 1, 1};
+    // the absorbed queries as a 3-D tensor [B][H][576]: boxes of 128 heads
+    // (rows past H read 0) by 64 latent / 32 rope columns
     const cuuint64_t qdims[3] = {576, (cuuint64_t)p.H, (cuuint64_t)p.B};
     const cuuint64_t qstrides[2] = {stride(p.H, p.q_sh, 1152), stride(p.B, p.q_sb, 1152)};
     const cuuint32_t qbox[3] = {64, 128, 1};
-    rc = enc(&qmap, dt, 3, const_cast<unsigned char*>(p.q), qdims, qstrides, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (rc != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    return dtype == DCP_F16 ? launch_mla_t<__half>(p, map, qmap, stream)
-                            : launch_mla_t<__nv_bfloat16>(p, map, qmap, stream);
+    const cuuint32_t qrbox[3] = {32, 128, 1};
+    void* kv = const_cast<unsigned char*>(p.kv);
+    void* q = const_cast<unsigned char*>(p.q);
+    const CUresult rc[4] = {
+        enc(&maps[0], dt, 4, kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+        enc(&maps[1], dt, 4, kv, dims, strides, rbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+        enc(&maps[2], dt, 3, q, qdims, qstrides, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+        enc(&maps[3], dt, 3, q, qdims, qstrides, qrbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)};
+    for (const CUresult r : rc)
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    return dtype == DCP_F16 ? launch_mla_t<__half>(p, maps, stream) : launch_mla_t<__nv_bfloat16>(p, maps, stream);
 }
 
 int mla_device_status(bool clear) {

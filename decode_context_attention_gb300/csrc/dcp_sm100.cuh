@@ -162,6 +162,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            (static_cast<uint64_t>(swizzle & 7u) << 61);
 }
 constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle64B = 4;
 
 // Instruction descriptor of kind::f16 with fp32 accumulation: A and B both
 // bf16 (bf16 = true) or both fp16, each K-major (0) or MN-major (1).
