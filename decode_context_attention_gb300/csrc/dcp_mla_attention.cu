@@ -158,6 +158,16 @@ __device__ __forceinline__ float2 add_f32x2(float2 x, float2 y) {
     memcpy(&r, &d, 8);
     return r;
 }
+// (a * b, c * d) with one instruction (packed fp32 multiply, round to nearest)
+__device__ __forceinline__ float2 mul_f32x2(float2 x, float2 y) {
+    uint64_t a, b, d;
+    memcpy(&a, &x, 8);
+    memcpy(&b, &y, 8);
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    float2 r;
+    memcpy(&r, &d, 8);
+    return r;
+}
 // The sums of two pairs of fp16 values (lo halves, hi halves) rounded once
 // to fp32: x's halves enter the mixed-precision add as fp16, y's exactly
 // widened to fp32 first.
@@ -633,34 +643,45 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                     break;
                 }
                 tc_fence_after();
-                uint32_t row[4][16];  // the four loads in flight together, one wait
+                // the row in log2 units, rounded to fp16 (saturating, NaN kept)
+                // in token pairs, once for both CTAs' softmaxes: the second
+                // half's loads are in flight while the first half converts
+                uint32_t hv[2][16];
+                {
+                    uint32_t ra[2][16], rb[2][16];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * q4, row[q4]);
-                tmem_wait_ld();
+                    for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * q2, ra[q2]);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) pin(row[q4]);
+                    for (int q2 = 0; q2 < 2; ++q2) pin(ra[q2]);
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 32 + 16 * q2, rb[q2]);
+                    auto convert = [&](const uint32_t (&r)[2][16], uint32_t (&out)[16]) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float2 x = mul_f32x2(
+                                make_float2(__uint_as_float(r[j >> 3][2 * (j & 7)]),
+                                            __uint_as_float(r[j >> 3][2 * (j & 7) + 1])),
+                                make_float2(scale2x, scale2x));
+                            out[j] = f16x2_satfinite(x.x, x.y);
+                        }
+                    };
+                    convert(ra, hv[0]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) pin(rb[q2]);
+                    convert(rb, hv[1]);
+                }
                 // the peer grants slot u once it has consumed the message before
                 if (!__all_sync(kAll, mbar_wait<true>(&bar->credit[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
                     ok = false;
                     break;
                 }
                 if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
-                // the row in log2 units, rounded to fp16 (saturating, NaN kept)
-                // in token pairs, once for both CTAs' softmaxes: group q of 8
-                // tokens to the peer's slot u at offset (q * 128 + h) * 16, and
-                // pairs [16g, 16g + 16) (tokens [32g, 32g + 32)) into SP[u]
-                // columns [32 + 16g, 48 + 16g) for this CTA's warpgroup g, over
-                // scores this thread has read
-                uint32_t hv[2][16];
-#pragma unroll
-                for (int g2 = 0; g2 < 2; ++g2)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        hv[g2][j] = f16x2_satfinite(__uint_as_float(row[2 * g2][2 * j]) * scale2x,
-                                                    __uint_as_float(row[2 * g2][2 * j + 1]) * scale2x);
-                        hv[g2][8 + j] = f16x2_satfinite(__uint_as_float(row[2 * g2 + 1][2 * j]) * scale2x,
-                                                        __uint_as_float(row[2 * g2 + 1][2 * j + 1]) * scale2x);
-                    }
+                // group q of 8 tokens to the peer's slot u at offset (q * 128 +
+                // h) * 16; pairs [16g, 16g + 16) (tokens [32g, 32g + 32)) into
+                // SP[u] columns [32 + 16g, 48 + 16g) for this CTA's warpgroup g,
+                // over scores this thread has read
                 const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
                 const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
 #pragma unroll
