@@ -328,6 +328,7 @@ KERNEL_SOURCES = {
     "decode_partial_kernel": ("dcp_attention.cu", "dcp_device.cuh"),
     "decode_partial_mma_kernel": ("dcp_attention.cu", "dcp_device.cuh"),
     "gqa_decode_tc_kernel": ("dcp_attention_tc.cu", "dcp_device.cuh", "dcp_sm100.cuh"),
+    "mla_decode_kernel": ("dcp_mla_attention.cu", "dcp_device.cuh", "dcp_sm100.cuh"),
 }
 
 
