@@ -18,10 +18,10 @@
 // 256 KB: all of one SM's tensor memory, with no room left for the scores.
 // So a pair of CTAs (a thread-block cluster of 2) works on one (rank,
 // request, split) item at a time: CTA c owns output columns [256c, 256c +
-// 256) and, for the scores,
-// latent columns [256c, 256c + 256) plus rope columns [512 + 32c, 544 + 32c)
-// -- exactly the columns it loads, so the pair reads every latent byte once
-// and does every multiply-add once.  Per tile of 64 tokens:
+// 256) and, for the scores, latent columns [256c, 256c + 256) plus rope
+// columns [512 + 32c, 544 + 32c) -- exactly the columns it loads, so the
+// pair reads every latent byte once and does every multiply-add once.  Per
+// tile of 64 tokens:
 //   * TMA (one thread) loads the CTA's four 64-column latent chunks of the
 //     64 tokens (128-byte swizzled) and its 32 rope columns (64-byte
 //     swizzled) into a 4-stage ring (36 KB a stage: the loads of a tile are
@@ -41,12 +41,12 @@
 //     memory for its own CTA's softmax.  Scores are double-buffered in TMEM,
 //     so the exchange of tile i + 1 overlaps the softmax of tile i;
 //   * two softmax warpgroups (thread (h, g) = head h = TMEM lane h, tokens
-//     [32g, 32g + 32) of the tile) add the two fp16 partials in fp32 (the
-//     same bits in both CTAs: one probability for both halves of the
-//     output) and run an online softmax in base 2 with a lazily moved
-//     reference max (the output is rescaled only when the max grows by more
-//     than 2^8, so most tiles skip it); P goes to tensor memory as
-//     bf16/fp16, over its tile's consumed scores;
+//     [32g, 32g + 32) of the tile) add the two fp16 partials with one
+//     rounding to fp32 (the same bits in both CTAs: one probability for both
+//     halves of the output) and run an online softmax in base 2 with a
+//     lazily moved reference max (the output is rescaled only when the max
+//     grows by more than 2^8, so most tiles skip it); P goes to tensor
+//     memory as bf16/fp16, over its tile's consumed scores;
 //   * the MMA thread accumulates O_c [128 x 256] += P . V_c with P as the
 //     TMEM A operand and V_c read MN-major from the same shared-memory tile.
 // With one split the softmax warps normalise O and write (O_r, lse_r);
@@ -59,10 +59,12 @@
 // staged (TMA into a shared-memory area, then into tensor memory) and its
 // first tiles are loaded and scored while the current item's last tiles and
 // its epilogue finish -- so the per-item set-up (barriers, tensor memory,
-// the query, the first tile's latency) is paid once per pair, not per item.  Every barrier wait is bounded (1 s):
-// a wait that runs out records DCP_ERR_TIMEOUT in a device status word and
-// the kernel winds down (its copies and MMAs in flight are waited for, its
-// tensor memory freed) instead of hanging.
+// the query, the first tile's latency) is paid once per pair, not per item.
+//
+// Every barrier wait is bounded (1 s): a wait that runs out records
+// DCP_ERR_TIMEOUT in a device status word and the kernel winds down (its
+// copies and MMAs in flight are waited for, its tensor memory freed)
+// instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
