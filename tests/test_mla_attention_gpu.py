@@ -4,8 +4,9 @@ Every rank's partial (O_r, lse_r) from dcp_decode_attention_mla is compared,
 element by element, with oracle.split_attention_mla on the same seeded
 inputs: small cases on every row (ragged tails, ranks owning nothing, one
 split and many, both LSE bases, bf16 and fp16, fewer than 128 heads, strided
-operands), the full-size workload on sampled rows, a request's rows under
-both work orders of the persistent kernel, and the whole one-GPU DCP
+operands), seeded random shapes on sampled rows, the full-size workload on
+sampled rows, a request's rows under both work orders of the persistent
+kernel, and the whole one-GPU DCP
 decode of the MLA merge's shape (attention -> peer-inside pack -> combine)
 against unsplit attention.
 
@@ -211,6 +212,43 @@ def test_mla_schedule_leaves_every_item_bit_identical():
         rows = global_rows(kv, b, lens[b], N)
         check_row(o[r, b, h].double().cpu().numpy(), float(lse[r, b, h]), qn[b, h], rows, r, N, scale, "2",
                   U[q.dtype], f"b={b} r={r} h={h}")
+
+
+RANDOM_SEEDS = list(range(8))
+
+
+@pytest.mark.parametrize("seed", RANDOM_SEEDS)
+def test_mla_random_shapes_match_oracle_on_sampled_rows(seed):
+    """Seeded random shapes for the persistent kernel: 1-8 ranks, 1-40
+    requests (some empty, some at the cache's end), 16-128 heads, splits of
+    64 tokens to whole ranks, either payload type and LSE base; every
+    request's rows for a few heads and every rank against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(1, 9))
+    B = int(rng.integers(1, 41))
+    H = int(rng.choice([16, 48, 64, 96, 128]))
+    max_len = int(rng.integers(1, 6001))
+    split = int(rng.choice([64, 128, 512, 2048]))
+    dtype = torch.bfloat16 if rng.integers(2) else torch.float16
+    base = "2" if rng.integers(2) else "e"
+    lens = [int(x) for x in rng.integers(0, max_len + 1, size=B)]
+    lens[int(rng.integers(B))] = max_len
+    if B > 2:
+        lens[int(rng.integers(B))] = 0
+    q, kv, seq = draw(N, B, H, lens, max_len, dtype, seed=2000 + seed)
+    scale = 192 ** -0.5
+    o, lse = run(q, kv, seq, max_len, scale, base, split)
+    qn = q.double().cpu().numpy()
+    on = o.double().cpu().numpy()
+    ln = lse.double().cpu().numpy()
+    heads = sorted({0, H - 1, int(rng.integers(H))})
+    for b, L in enumerate(lens):
+        rows = global_rows(kv, b, L, N)
+        for h in heads:
+            want = oracle.split_attention_mla(qn[b, h], rows, DV, N, scale, base=base)
+            for r in range(N):
+                check_row(on[r, b, h], ln[r, b, h], qn[b, h], rows, r, N, scale, base, U[dtype],
+                          f"seed={seed} N={N} B={B} H={H} split={split} b={b} r={r} h={h}", want)
 
 
 def test_whole_mla_dcp_decode_equals_unsplit_attention():
