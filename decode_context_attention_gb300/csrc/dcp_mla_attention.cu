@@ -647,53 +647,54 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 tc_fence_after();
                 // the row in log2 units, rounded to fp16 (saturating, NaN kept)
                 // in token pairs, once for both CTAs' softmaxes: the second
-                // half's loads are in flight while the first half converts
+                // half's loads are in flight while the first half converts and
+                // goes to the peer (group q of 8 tokens to the peer's slot u at
+                // offset (q * 128 + h) * 16)
                 uint32_t hv[2][16];
-                {
-                    uint32_t ra[2][16], rb[2][16];
+                uint32_t ra[2][16], rb[2][16];
 #pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * q2, ra[q2]);
-                    tmem_wait_ld();
+                for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 16 * q2, ra[q2]);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) pin(ra[q2]);
+                for (int q2 = 0; q2 < 2; ++q2) pin(ra[q2]);
 #pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 32 + 16 * q2, rb[q2]);
-                    auto convert = [&](const uint32_t (&r)[2][16], uint32_t (&out)[16]) {
+                for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(tmem + kColSP + 64 * u + lane_off + 32 + 16 * q2, rb[q2]);
+                auto convert = [&](const uint32_t (&r)[2][16], uint32_t (&out)[16]) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float2 x = mul_f32x2(
-                                make_float2(__uint_as_float(r[j >> 3][2 * (j & 7)]),
-                                            __uint_as_float(r[j >> 3][2 * (j & 7) + 1])),
-                                make_float2(scale2x, scale2x));
-                            out[j] = f16x2_satfinite(x.x, x.y);
-                        }
-                    };
-                    convert(ra, hv[0]);
-                    tmem_wait_ld();
+                    for (int j = 0; j < 16; ++j) {
+                        const float2 x = mul_f32x2(make_float2(__uint_as_float(r[j >> 3][2 * (j & 7)]),
+                                                               __uint_as_float(r[j >> 3][2 * (j & 7) + 1])),
+                                                   make_float2(scale2x, scale2x));
+                        out[j] = f16x2_satfinite(x.x, x.y);
+                    }
+                };
+                const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
+                const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
+                auto send = [&](int g2) {  // token groups 4 g2 .. 4 g2 + 3
 #pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) pin(rb[q2]);
-                    convert(rb, hv[1]);
-                }
+                    for (int q = 0; q < 4; ++q)
+                        st_async_v4(dst + (4 * g2 + q) * 128 * 16,
+                                    make_float4(__uint_as_float(hv[g2][4 * q]), __uint_as_float(hv[g2][4 * q + 1]),
+                                                __uint_as_float(hv[g2][4 * q + 2]), __uint_as_float(hv[g2][4 * q + 3])),
+                                    xb);
+                };
+                convert(ra, hv[0]);
                 // the peer grants slot u once it has consumed the message before
                 if (!__all_sync(kAll, mbar_wait<true>(&bar->credit[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                    tmem_wait_ld();  // no load left in flight
                     ok = false;
                     break;
                 }
                 if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
-                // group q of 8 tokens to the peer's slot u at offset (q * 128 +
-                // h) * 16; pairs [16g, 16g + 16) (tokens [32g, 32g + 32)) into
-                // SP[u] columns [32 + 16g, 48 + 16g) for this CTA's warpgroup g,
-                // over scores this thread has read
-                const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
-                const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
+                send(0);
+                tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_async_v4(dst + q * 128 * 16,
-                                make_float4(__uint_as_float(hv[q >> 2][4 * (q & 3)]),
-                                            __uint_as_float(hv[q >> 2][4 * (q & 3) + 1]),
-                                            __uint_as_float(hv[q >> 2][4 * (q & 3) + 2]),
-                                            __uint_as_float(hv[q >> 2][4 * (q & 3) + 3])),
-                                xb);
+                for (int q2 = 0; q2 < 2; ++q2) pin(rb[q2]);
+                convert(rb, hv[1]);
+                send(1);
+                // pairs [16g, 16g + 16) (tokens [32g, 32g + 32)) into SP[u]
+                // columns [32 + 16g, 48 + 16g) for this CTA's warpgroup g, over
+                // scores this thread has read
 #pragma unroll
                 for (int g2 = 0; g2 < 2; ++g2) tmem_st16(tmem + kColSP + 64 * u + 32 + 16 * g2 + lane_off, hv[g2]);
                 tmem_wait_st();
