@@ -3,8 +3,8 @@
 of 128) against the oracle's split attention: tile edges, one and several
 splits, both payload types and LSE bases, paged caches of every page size
 the path takes (bit-identical to the contiguous call), page indices outside
-the pool, stale cache rows past each rank's length, and a bounded wait that
-runs out.  Tolerances as in test_attention_gpu.py.
+the pool, stale cache rows past each rank's length, scores that keep moving
+the reference max, and a bounded wait that runs out.  Tolerances as in test_attention_gpu.py.
 """
 import math
 import os
@@ -153,6 +153,24 @@ def test_tensor_core_ignores_stale_rows_past_each_length():
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
+
+
+def test_tensor_core_rising_scores_move_the_reference_max():
+    """Keys that grow along the sequence make the lazily moved reference max
+    move (by more than 2^8) within a split, so the transposed output is
+    rescaled in place several times; the partials still match the oracle."""
+    N, H, Hkv, D = 2, 16, 2, 128
+    lens = [4000, 2500, 700, 1]
+    B = len(lens)
+    q, K, V, seq, L = make_case(N, B, H, Hkv, D, lens, torch.bfloat16, seed=57)
+    t = torch.arange(K.shape[1], device=DEV, dtype=torch.float32)
+    K = (K.float() * (1.0 + t / 250.0)[None, :, None, None]).to(K.dtype)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_attention(q, K, V, seq, L, N, scale, "2", 1024)
+    want, want_lse = oracle_partials(q, K, V, lens, N, scale, "2")
+    torch.cuda.synchronize()
+    assert_merge_close(o, want, "rank partial O, rising scores")
+    assert_attn_lse(lse, want_lse)
 
 
 _STALL_SCRIPT = r'''

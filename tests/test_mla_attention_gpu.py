@@ -214,6 +214,35 @@ def test_mla_schedule_leaves_every_item_bit_identical():
                   U[q.dtype], f"b={b} r={r} h={h}")
 
 
+def test_mla_rising_scores_move_the_reference_max_mid_item():
+    """Scores that grow along the sequence make the kernel's lazily moved
+    reference max move (by more than 2^8) inside items and across tiles, so
+    the accumulated output is rescaled several times per item; every row
+    still matches the oracle.  Several items per CTA pair (splits of 128)."""
+    N, H, max_len, split = 4, 64, 3000, 128
+    lens = [3000, 2500, 1700, 900, 64, 1]
+    B = len(lens)
+    q, kv, seq = draw(N, B, H, lens, max_len, torch.bfloat16, seed=31)
+    lc = kv.shape[2]
+    # local token i of rank r is global token i*N + r: scale its latent row by
+    # 1 + t/300 so that later tokens score higher (the row max climbs by ~50
+    # in log2 units over the longest request)
+    t = torch.arange(lc, device=DEV)[None, :] * N + torch.arange(N, device=DEV)[:, None]
+    kv = (kv.float() * (1.0 + t.float() / 300.0)[:, None, :, None]).to(torch.bfloat16)
+    scale = 192 ** -0.5
+    o, lse = run(q, kv, seq, max_len, scale, "2", split)
+    qn = q.double().cpu().numpy()
+    on = o.double().cpu().numpy()
+    ln = lse.double().cpu().numpy()
+    for b, L in enumerate(lens):
+        rows = global_rows(kv, b, L, N)
+        for h in (0, 17, H - 1):
+            want = oracle.split_attention_mla(qn[b, h], rows, DV, N, scale, base="2")
+            for r in range(N):
+                check_row(on[r, b, h], ln[r, b, h], qn[b, h], rows, r, N, scale, "2", U[q.dtype],
+                          f"rising scores b={b} r={r} h={h}", want)
+
+
 RANDOM_SEEDS = list(range(8))
 
 
