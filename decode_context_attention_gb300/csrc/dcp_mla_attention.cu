@@ -132,7 +132,7 @@ struct Barriers {
     uint64_t stg_free;     // the epilogue is done with the staging area (softmax warps)
     uint64_t mma_done;
     uint64_t s_full[2], own_full[2], p_full[2], pv_done[2];  // per score / probability buffer
-    uint64_t xfull[2];   // receive slot: the peer's partial scores arrived (st.async bytes)
+    uint64_t xfull[2][2];  // receive slot u, token half g2: the peer's partial scores arrived (st.async bytes)
     uint64_t credit[2];  // send slot: the peer has freed its receive slot (a st.async credit)
     uint64_t red_full, red_free;  // the softmax warpgroups' per-row values: written / read
     uint32_t tmem_base;
@@ -226,8 +226,9 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 //            item's first once the previous item's O has been read: o_free),
 //            then QK(gi + 2) into SP[u] (s_full[u]; an item's last also
 //            q_empty)
-//   softmax  the peer's S(gi) from slot u (xfull[u]) + the own from SP[u]
-//            (own_full[u]); re-arm xfull[u] and grant the slot back to the peer;
+//   softmax  the peer's S(gi) from slot u (xfull[u][g], one barrier per token
+//            half) + the own from SP[u] (own_full[u]); re-arm xfull[u][*]
+//            and grant the slot back to the peer;
 //            P(gi) into SP[u] columns [0, 32) (p_full[u]); after an item's
 //            last PV its O goes out (o_free once read) through the staging
 //            area, once the next item's query has left it (stg_free after)
@@ -273,8 +274,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
             mbar_init(&bar->pv_done[u], 1);
             // the peer's bytes complete these; this CTA's expect_tx is the one
             // arrival, armed here for the first phase
-            mbar_init(&bar->xfull[u], 1);
-            mbar_arrive_expect_tx(&bar->xfull[u], kXbufBytes);
+            for (int g2 = 0; g2 < 2; ++g2) {
+                mbar_init(&bar->xfull[u][g2], 1);
+                mbar_arrive_expect_tx(&bar->xfull[u][g2], kXbufBytes / 2);
+            }
             mbar_init(&bar->credit[u], 1);
             mbar_arrive_expect_tx(&bar->credit[u], 4);
         }
@@ -595,7 +598,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const float scale2x = p.sm_scale * kLog2eF;
         const uint32_t peer_slots = map_to_cta(slots, peer);
-        const uint32_t peer_xfull = map_to_cta(&bar->xfull[0], peer);  // slot u's barrier is 8u bytes further
+        const uint32_t peer_xfull = map_to_cta(&bar->xfull[0][0], peer);  // (u, g2)'s is 8 (2u + g2) bytes further
         int gt = 0, nq = 0, nbox = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -669,8 +672,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                     }
                 };
                 const uint32_t dst = peer_slots + (uint32_t)(u * kXbufBytes + h * 16);
-                const uint32_t xb = peer_xfull + 8u * (uint32_t)u;
-                auto send = [&](int g2) {  // token groups 4 g2 .. 4 g2 + 3
+                // token groups 4 g2 .. 4 g2 + 3: the half the peer's warpgroup g2
+                // reads, counted on its own barrier
+                auto send = [&](int g2) {
+                    const uint32_t xb = peer_xfull + 8u * (2u * (uint32_t)u + (uint32_t)g2);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         st_async_v4(dst + (4 * g2 + q) * 128 * 16,
@@ -777,7 +782,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 tmem_ld16(tmem + kColSP + 64 * u + 32 + 16 * g + lane_off, own);
                 tmem_wait_ld();
                 pin(own);
-                if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                if (!__all_sync(kAll, mbar_wait<true>(&bar->xfull[u][g], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
                     ok = false;
                     break;
                 }
@@ -817,7 +822,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 if (tid == 0) {
                     // every softmax thread has read slot u (before its red_full
                     // arrival): re-arm it for tile gi + 2 and grant it back to the peer
-                    mbar_arrive_expect_tx(&bar->xfull[u], kXbufBytes);
+                    mbar_arrive_expect_tx(&bar->xfull[u][0], kXbufBytes / 2);
+                    mbar_arrive_expect_tx(&bar->xfull[u][1], kXbufBytes / 2);
                     st_async_b32(peer_cword + 4u * (uint32_t)u, 1u, peer_credit + 8u * (uint32_t)u);
                 }
                 const float m_new = fmaxf(m_used, mt_all);
