@@ -131,7 +131,7 @@ struct Barriers {
     uint64_t o_free;       // the item's O has been read out (softmax threads)
     uint64_t stg_free;     // the epilogue is done with the staging area (softmax warps)
     uint64_t mma_done;
-    uint64_t s_full[2], own_full[2], p_full[2], pv_done[2];  // per score / probability buffer
+    uint64_t s_full[2], own_full[2][2], p_full[2], pv_done[2];  // per score / probability buffer (own: per half)
     uint64_t xfull[2][2];  // receive slot u, token half g2: the peer's partial scores arrived (st.async bytes)
     uint64_t credit[2];  // send slot: the peer has freed its receive slot (a st.async credit)
     uint64_t red_full, red_free;  // the softmax warpgroups' per-row values: written / read
@@ -220,14 +220,14 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 //            once item n-1's last score product has run (q_full); then S(gi)
 //            from SP[u] as fp16 pairs -> the peer's receive slot u by
 //            st.async once the peer granted it (credit[u]), and into SP[u]
-//            columns [32, 64) (own_full[u])
+//            columns [32, 64) (own_full[u][half])
 //   MMA      the scores run two tiles ahead of the value products, across
 //            items: PV(gi) after P(gi) (pv_done[u], kv_empty[stage]; an
 //            item's first once the previous item's O has been read: o_free),
 //            then QK(gi + 2) into SP[u] (s_full[u]; an item's last also
 //            q_empty)
 //   softmax  the peer's S(gi) from slot u (xfull[u][g], one barrier per token
-//            half) + the own from SP[u] (own_full[u]); re-arm xfull[u][*]
+//            half) + the own from SP[u] (own_full[u][g]); re-arm xfull[u][*]
 //            and grant the slot back to the peer;
 //            P(gi) into SP[u] columns [0, 32) (p_full[u]); after an item's
 //            last PV its O goes out (o_free once read) through the staging
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
         mbar_init(&bar->mma_done, 1);
         for (int u = 0; u < 2; ++u) {
             mbar_init(&bar->s_full[u], 1);
-            mbar_init(&bar->own_full[u], 4);
+            for (int g2 = 0; g2 < 2; ++g2) mbar_init(&bar->own_full[u][g2], 4);
             mbar_init(&bar->p_full[u], 8);
             mbar_init(&bar->pv_done[u], 1);
             // the peer's bytes complete these; this CTA's expect_tx is the one
@@ -691,21 +691,24 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                     break;
                 }
                 if (h == 0) mbar_arrive_expect_tx(&bar->credit[u], 4);  // arm the slot's next grant
+                // pairs [16 g2, 16 g2 + 16) (tokens [32 g2, 32 g2 + 32)) into
+                // SP[u] columns [32 + 16 g2, 48 + 16 g2) for this CTA's
+                // warpgroup g2, over scores this thread has read
+                auto keep = [&](int g2) {
+                    tmem_st16(tmem + kColSP + 64 * u + 32 + 16 * g2 + lane_off, hv[g2]);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar->own_full[u][g2]);
+                };
                 send(0);
-                tmem_wait_ld();
+                tmem_wait_ld();  // the second half is read before the first half's pairs go over it
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) pin(rb[q2]);
+                keep(0);
                 convert(rb, hv[1]);
                 send(1);
-                // pairs [16g, 16g + 16) (tokens [32g, 32g + 32)) into SP[u]
-                // columns [32 + 16g, 48 + 16g) for this CTA's warpgroup g, over
-                // scores this thread has read
-#pragma unroll
-                for (int g2 = 0; g2 < 2; ++g2) tmem_st16(tmem + kColSP + 64 * u + 32 + 16 * g2 + lane_off, hv[g2]);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar->own_full[u]);
+                keep(1);
             }
             gt += ntiles;
             ++nq;
@@ -773,7 +776,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_decode_kernel(const __grid
                 // the own partial scores of this thread's tokens, as the
                 // exchange warpgroup rounded them (fp16 pairs in SP[u]
                 // columns [32 + 16g, 48 + 16g)), the peer's from slot u
-                if (!__all_sync(kAll, mbar_wait(&bar->own_full[u], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
+                if (!__all_sync(kAll, mbar_wait(&bar->own_full[u][g], (gi >> 1) & 1, status, kStatusTimeout, abort))) {
                     ok = false;
                     break;
                 }
